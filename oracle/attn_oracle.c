@@ -1,0 +1,276 @@
+/*
+ * CPU oracle for exact softmax attention.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the benchmark's CPU-baseline leg and
+ * the smoke check may load this library. It shares no code with the CUDA path.
+ *
+ * What it computes is the plain definition of scaled-dot-product attention
+ * ("FlashAttention: not computing less, moving less", section 01, the formula
+ * O = softmax(Q K^T / sqrt(d)) V), which the tiled online-softmax kernels reach
+ * exactly in real arithmetic (same page, section 02, "professional extension":
+ * online softmax equals the full-row softmax). Per query row it is written out
+ * as three passes in float64:
+ *   s_j = scale * <q, k_j>           for every visible key j
+ *   m   = max_j s_j
+ *   l   = sum_j exp(s_j - m)
+ *   o   = sum_j (exp(s_j - m) / l) * v_j,   lse = m + ln(l)
+ * The log-sum-exp output follows the same page's section 03 ("the forward pass
+ * saves the output and log-sum-exp statistics"): natural log, of scaled scores.
+ *
+ * Readings where the pages are silent:
+ *  - causal masks are bottom-right aligned: key j is visible to query row i of a
+ *    sequence with Nq queries and Nk keys iff j <= i + (Nk - Nq);
+ *  - a row with no visible key has o = 0 and lse = -inf;
+ *  - query head h reads key/value head h / (Hq / Hkv).
+ *
+ * Paged decode ("Faster, more flexible FA4 for LLM inference", PR 1999/2104 and
+ * PR 1940 sections) is the same definition with one query per sequence and every
+ * cached key visible; the oracle first gathers the sequence's K/V rows through
+ * the page table into contiguous arrays, then applies the row routine.
+ *
+ * Inputs are bf16 bit patterns (uint16), widened exactly to double.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static inline double bf16d(uint16_t h) {
+    uint32_t b = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &b, 4);
+    return (double)f;
+}
+
+/* One query row against the first n_vis keys of a contiguous key/value array.
+ * krow(j) = k + j * kv_stride, vrow(j) = v + j * kv_stride (each d elements). */
+static void attend_row(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t kv_stride,
+                       int64_t n_vis, int d, double scale, double* s, double* qd, double* o, double* lse) {
+    if (n_vis <= 0) {
+        for (int c = 0; c < d; ++c) o[c] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    for (int c = 0; c < d; ++c) qd[c] = bf16d(q[c]);
+    /* scores */
+    for (int64_t j = 0; j < n_vis; ++j) {
+        const uint16_t* kr = k + j * kv_stride;
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c) acc += qd[c] * bf16d(kr[c]);
+        s[j] = scale * acc;
+    }
+    /* pass 1: row maximum */
+    double m = s[0];
+    for (int64_t j = 1; j < n_vis; ++j)
+        if (s[j] > m) m = s[j];
+    /* pass 2: normaliser */
+    double l = 0.0;
+    for (int64_t j = 0; j < n_vis; ++j) l += exp(s[j] - m);
+    /* pass 3: probabilities times values */
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (int64_t j = 0; j < n_vis; ++j) {
+        const double p = exp(s[j] - m) / l;
+        const uint16_t* vr = v + j * kv_stride;
+        for (int c = 0; c < d; ++c) o[c] += p * bf16d(vr[c]);
+    }
+    *lse = m + log(l);
+}
+
+/* ------------------------------------------------------------------ forward */
+
+typedef struct {
+    const uint16_t *q, *k, *v;
+    double *o, *lse;
+    int B, Hq, Hkv, Nq, Nk, d, causal;
+    double scale;
+    const int32_t* cu; /* host cu_seqlens or NULL */
+    const int64_t* rows;  /* optional (token * Hq + head) list */
+    int64_t n_rows;
+    int64_t next;         /* work counter */
+    int64_t max_keys;
+    int status;
+} fwd_job_t;
+
+/* Sequence geometry of query token t: sequence b, row i, Nq_b, Nk_b, first key token. */
+static int locate(const fwd_job_t* J, int64_t t, int64_t* i, int64_t* nq, int64_t* nk, int64_t* k0) {
+    if (J->cu) {
+        int lo = 0, hi = J->B; /* find b with cu[b] <= t < cu[b+1] */
+        if (t < J->cu[0] || t >= J->cu[J->B]) return -1;
+        while (hi - lo > 1) {
+            int mid = (lo + hi) / 2;
+            if (J->cu[mid] <= t) lo = mid; else hi = mid;
+        }
+        *i = t - J->cu[lo];
+        *nq = *nk = J->cu[lo + 1] - J->cu[lo];
+        *k0 = J->cu[lo];
+    } else {
+        const int64_t b = t / J->Nq;
+        if (b >= J->B) return -1;
+        *i = t % J->Nq;
+        *nq = J->Nq;
+        *nk = J->Nk;
+        *k0 = b * (int64_t)J->Nk;
+    }
+    return 0;
+}
+
+static void* fwd_worker(void* p) {
+    fwd_job_t* J = (fwd_job_t*)p;
+    const int d = J->d;
+    const int G = J->Hq / J->Hkv;
+    const int64_t total_tokens = J->cu ? J->cu[J->B] : (int64_t)J->B * J->Nq;
+    const int64_t n_items = J->rows ? J->n_rows : total_tokens * J->Hq;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(J->max_keys > 0 ? J->max_keys : 1));
+    double* qd = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!s || !qd) {
+        __atomic_store_n(&J->status, -2, __ATOMIC_RELAXED);
+        free(s);
+        free(qd);
+        return NULL;
+    }
+    for (;;) {
+        const int64_t it = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
+        if (it >= n_items) break;
+        const int64_t row = J->rows ? J->rows[it] : it;
+        const int64_t t = row / J->Hq;
+        const int h = (int)(row % J->Hq);
+        int64_t i, nq, nk, k0;
+        if (row < 0 || locate(J, t, &i, &nq, &nk, &k0) != 0) {
+            __atomic_store_n(&J->status, -3, __ATOMIC_RELAXED);
+            continue;
+        }
+        int64_t n_vis = nk;
+        if (J->causal) {
+            const int64_t last = i + (nk - nq); /* last visible key index */
+            n_vis = last + 1 < nk ? last + 1 : nk;
+        }
+        const int g = h / G;
+        const int64_t kv_stride = (int64_t)J->Hkv * d;
+        attend_row(J->q + (t * J->Hq + h) * d, J->k + k0 * kv_stride + (int64_t)g * d,
+                   J->v + k0 * kv_stride + (int64_t)g * d, kv_stride, n_vis, d, J->scale, s, qd,
+                   J->o + it * d, J->lse + it);
+    }
+    free(s);
+    free(qd);
+    return NULL;
+}
+
+static int run_threads(void* (*fn)(void*), void* job, int n_threads) {
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 512) n_threads = 512;
+    pthread_t th[512];
+    int ok[512];
+    for (int t = 0; t < n_threads; ++t) ok[t] = pthread_create(&th[t], NULL, fn, job) == 0;
+    int any = 0;
+    for (int t = 0; t < n_threads; ++t)
+        if (ok[t]) { pthread_join(th[t], NULL); any = 1; }
+    if (!any) fn(job);
+    return 0;
+}
+
+/*
+ * Forward attention. q: [T, Hq, d]; k, v: [Tk, Hkv, d] (bf16 bits, d fastest).
+ * Dense (cu_seqlens == NULL): T = B*Nq, Tk = B*Nk, sequence b owns rows b*Nq.. and keys b*Nk...
+ * Varlen (cu_seqlens = host int32[B+1]): sequence b owns tokens [cu[b], cu[b+1]) of both q and k.
+ * rows == NULL: o is [T, Hq, d], lse [T, Hq]. Otherwise only the listed rows
+ * (token*Hq + head) are computed and o is [n_rows, d], lse [n_rows], in list order.
+ * Returns 0, or negative on bad arguments.
+ */
+int oracle_attn_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, double* o, double* lse,
+                    int B, int Hq, int Hkv, int Nq, int Nk, int d, double scale, int causal,
+                    const int32_t* cu_seqlens, const int64_t* rows, int64_t n_rows, int n_threads) {
+    if (!q || !k || !v || !o || !lse || B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0) return -1;
+    fwd_job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.k = k; J.v = v; J.o = o; J.lse = lse;
+    J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.Nq = Nq; J.Nk = Nk; J.d = d; J.causal = causal;
+    J.scale = scale; J.cu = cu_seqlens; J.rows = rows; J.n_rows = n_rows;
+    if (cu_seqlens) {
+        int64_t mx = 0;
+        for (int b = 0; b < B; ++b) {
+            const int64_t L = (int64_t)cu_seqlens[b + 1] - cu_seqlens[b];
+            if (L < 0) return -1;
+            if (L > mx) mx = L;
+        }
+        J.max_keys = mx;
+    } else {
+        if (Nq < 0 || Nk < 0) return -1;
+        J.max_keys = Nk;
+    }
+    if (B == 0) return 0;
+    run_threads(fwd_worker, &J, n_threads);
+    return J.status;
+}
+
+/* ------------------------------------------------------------------ decode */
+
+typedef struct {
+    const uint16_t *q, *kc, *vc;
+    const int32_t *page_table, *seqlens;
+    int page_size, B, Hq, Hkv, d, max_pages;
+    double scale;
+    double *o, *lse;
+    int64_t next;
+    int status;
+} dec_job_t;
+
+static void* dec_worker(void* p) {
+    dec_job_t* J = (dec_job_t*)p;
+    const int d = J->d, Hkv = J->Hkv, G = J->Hq / J->Hkv;
+    for (;;) {
+        const int64_t b = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
+        if (b >= J->B) break;
+        const int64_t L = J->seqlens[b];
+        if (L < 0 || L > (int64_t)J->max_pages * J->page_size) {
+            __atomic_store_n(&J->status, -3, __ATOMIC_RELAXED);
+            continue;
+        }
+        /* gather this sequence's cached rows, [L, Hkv, d], through the page table */
+        const size_t row_elems = (size_t)Hkv * d;
+        uint16_t* kb = (uint16_t*)malloc(sizeof(uint16_t) * row_elems * (size_t)(L > 0 ? L : 1));
+        uint16_t* vb = (uint16_t*)malloc(sizeof(uint16_t) * row_elems * (size_t)(L > 0 ? L : 1));
+        double* s = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        double* qd = (double*)malloc(sizeof(double) * (size_t)d);
+        if (!kb || !vb || !s || !qd) {
+            __atomic_store_n(&J->status, -2, __ATOMIC_RELAXED);
+            free(kb); free(vb); free(s); free(qd);
+            continue;
+        }
+        for (int64_t t = 0; t < L; ++t) {
+            const int64_t page = J->page_table[b * J->max_pages + t / J->page_size];
+            const int64_t slot = t % J->page_size;
+            const size_t src = (size_t)(page * J->page_size + slot) * row_elems;
+            memcpy(kb + (size_t)t * row_elems, J->kc + src, sizeof(uint16_t) * row_elems);
+            memcpy(vb + (size_t)t * row_elems, J->vc + src, sizeof(uint16_t) * row_elems);
+        }
+        for (int h = 0; h < J->Hq; ++h) {
+            const int g = h / G;
+            attend_row(J->q + (b * J->Hq + h) * d, kb + (size_t)g * d, vb + (size_t)g * d, (int64_t)row_elems, L, d,
+                       J->scale, s, qd, J->o + (b * J->Hq + h) * d, J->lse + b * J->Hq + h);
+        }
+        free(kb); free(vb); free(s); free(qd);
+    }
+    return NULL;
+}
+
+/*
+ * Paged decode. q: [B, Hq, d]; k_cache, v_cache: [num_pages, page_size, Hkv, d];
+ * page_table: int32 [B, max_pages]; seqlens: int32 [B]. o: [B, Hq, d], lse: [B, Hq].
+ * One query per sequence; all seqlens[b] cached keys are visible.
+ */
+int oracle_attn_decode_paged(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                             const int32_t* page_table, const int32_t* seqlens, int page_size,
+                             double* o, double* lse, int B, int Hq, int Hkv, int d, int max_pages,
+                             double scale, int n_threads) {
+    if (!q || !k_cache || !v_cache || !page_table || !seqlens || !o || !lse) return -1;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || page_size <= 0 || max_pages < 0) return -1;
+    dec_job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.kc = k_cache; J.vc = v_cache; J.page_table = page_table; J.seqlens = seqlens;
+    J.page_size = page_size; J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.max_pages = max_pages;
+    J.scale = scale; J.o = o; J.lse = lse;
+    if (B == 0) return 0;
+    run_threads(dec_worker, &J, n_threads < B ? n_threads : B);
+    return J.status;
+}

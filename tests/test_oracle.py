@@ -1,0 +1,393 @@
+"""Pins for the CPU oracle: checks against what the pages print and against mathematics.
+
+Each test ties the oracle to something other than itself: the worked example
+printed on "FlashAttention: not computing less, moving less" (section 02), the
+exp2 error table of "FlashAttention4 精读" (section 3.1.3), closed forms,
+invariants, brute force in extended precision, and an independent library
+routine (PyTorch's float64 scaled_dot_product_attention on CPU).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth import workloads as W
+
+E = math.e
+
+
+def _golden(name):
+    with open(os.path.join(os.path.dirname(__file__), "golden", name)) as f:
+        return json.load(f)
+
+
+def _bf16(a):
+    return synth.f32_to_bf16(np.asarray(a, dtype=np.float32))
+
+
+def _f(a):
+    return synth.bf16_to_f32(a).astype(np.float64)
+
+
+def _rand_case(seed, T, H, d, mult=1.0):
+    return synth.normal_bf16((T, H, d), seed, mult)
+
+
+# --------------------------------------------------------------- worked example
+
+def test_worked_example_online_states():
+    g = _golden("worked_example.json")
+    s_blocks = [np.array([b["scores"]]) for b in g["blocks"]]
+    v_blocks = [np.array(b["values"])[:, None] for b in g["blocks"]]
+    o, lse, hist = oracle.online_attention(s_blocks, v_blocks, tau=0.0, history=True)
+    (m1, l1, a1), (m2, l2, a2) = hist
+    assert m1[0] == g["after_block_1"]["m"]
+    assert abs(l1[0] - g["after_block_1"]["l"]) < 5e-5
+    assert abs(a1[0, 0] - g["after_block_1"]["a"]) < 5e-5
+    assert abs(l2[0] - g["after_block_2"]["l"]) < 5e-5
+    # the page prints 38.710 for 38.7109...: truncated, so allow one unit of the last printed digit
+    assert abs(a2[0, 0] - g["after_block_2"]["a"]) < 1e-3
+    assert abs(o[0, 0] - g["o_approx"]) < 5e-3
+    closed = (10 * E + 20 * E**2 + 30 * E**3) / (E + E**2 + E**3)
+    assert abs(o[0, 0] - closed) < 1e-12
+    assert abs(lse[0] - math.log(E + E**2 + E**3)) < 1e-12
+
+
+def test_worked_example_three_pass():
+    g = _golden("worked_example.json")
+    scores = g["blocks"][0]["scores"] + g["blocks"][1]["scores"]
+    values = g["blocks"][0]["values"] + g["blocks"][1]["values"]
+    q = _bf16([[[1.0]]])
+    k = _bf16(np.array(scores)[:, None, None])
+    v = _bf16(np.array(values)[:, None, None])
+    o, lse = oracle.attn_fwd(q, k, v, B=1, Hq=1, Hkv=1, Nq=1, Nk=3, d=1, scale=1.0, causal=False)
+    closed = (10 * E + 20 * E**2 + 30 * E**3) / (E + E**2 + E**3)
+    assert abs(o[0, 0, 0] - closed) < 1e-12
+    assert abs(o[0, 0, 0] - g["o_approx"]) < 5e-3
+    assert abs(lse[0, 0] - math.log(E + E**2 + E**3)) < 1e-12
+
+
+# ------------------------------------------------------- independent library check
+
+torch = pytest.importorskip("torch")
+
+
+def _torch_reference(q, k, v, scale, causal, Nq, Nk, G):
+    """PyTorch float64 SDPA with an explicit bottom-right mask; LSE by torch.logsumexp."""
+    qt = torch.from_numpy(_f(q)).permute(1, 0, 2)[None]          # [1, Hq, Nq, d]
+    kt = torch.from_numpy(_f(k)).permute(1, 0, 2)[None].repeat_interleave(G, dim=1)
+    vt = torch.from_numpy(_f(v)).permute(1, 0, 2)[None].repeat_interleave(G, dim=1)
+    mask = None
+    if causal:
+        i = torch.arange(Nq)[:, None]
+        j = torch.arange(Nk)[None, :]
+        mask = j <= i + (Nk - Nq)
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale)
+    s = (qt @ kt.transpose(-1, -2)) * scale
+    if mask is not None:
+        s = s.masked_fill(~mask, float("-inf"))
+    lse = torch.logsumexp(s, dim=-1)
+    return o[0].permute(1, 0, 2).numpy(), lse[0].permute(1, 0).numpy()
+
+
+@pytest.mark.parametrize("Nq,Nk,Hq,Hkv,d,causal", [
+    (7, 7, 2, 2, 4, True), (5, 9, 4, 2, 8, True), (9, 9, 6, 3, 5, False), (16, 16, 4, 1, 16, True),
+    (3, 11, 8, 2, 3, False), (12, 12, 2, 2, 64, True)])
+def test_matches_torch_sdpa_float64(Nq, Nk, Hq, Hkv, d, causal):
+    seed = 1000 + Nq * 31 + Nk * 7 + Hq + d
+    q = _rand_case(seed, Nq, Hq, d)
+    k = _rand_case(seed + 1, Nk, Hkv, d)
+    v = _rand_case(seed + 2, Nk, Hkv, d)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = oracle.attn_fwd(q, k, v, 1, Hq, Hkv, Nq, Nk, d, scale, causal)
+    o_ref, lse_ref = _torch_reference(q, k, v, scale, causal, Nq, Nk, Hq // Hkv)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def test_brute_force_extended_precision():
+    """mpmath at 50 digits, no max subtraction, explicit S and P, on a tiny causal GQA case."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 50
+    Nq, Nk, Hq, Hkv, d = 4, 6, 4, 2, 3
+    q = _rand_case(77, Nq, Hq, d)
+    k = _rand_case(78, Nk, Hkv, d)
+    v = _rand_case(79, Nk, Hkv, d)
+    scale = 0.37
+    o, lse = oracle.attn_fwd(q, k, v, 1, Hq, Hkv, Nq, Nk, d, scale, True)
+    qf, kf, vf = _f(q), _f(k), _f(v)
+    for h in range(Hq):
+        g = h // (Hq // Hkv)
+        for i in range(Nq):
+            vis = [j for j in range(Nk) if j <= i + (Nk - Nq)]
+            S = [mp.mpf(scale) * mp.fsum(mp.mpf(float(qf[i, h, c])) * mp.mpf(float(kf[j, g, c])) for c in range(d))
+                 for j in vis]
+            P = [mp.e ** s for s in S]
+            Z = mp.fsum(P)
+            for c in range(d):
+                ref = mp.fsum(P[t] * mp.mpf(float(vf[j, g, c])) for t, j in enumerate(vis)) / Z
+                assert abs(float(ref) - o[i, h, c]) < 1e-14
+            assert abs(float(mp.log(Z)) - lse[i, h]) < 1e-14
+
+
+# ------------------------------------------------------------ invariants / closed forms
+
+def test_rows_sum_to_one():
+    Nq = Nk = 33
+    Hq, Hkv, d = 4, 2, 16
+    q = _rand_case(5, Nq, Hq, d, 2.0)
+    k = _rand_case(6, Nk, Hkv, d)
+    v = _rand_case(7, Nk, Hkv, d)
+    scale = 0.25
+    _, lse = oracle.attn_fwd(q, k, v, 1, Hq, Hkv, Nq, Nk, d, scale, True)
+    qf, kf = _f(q), _f(k)
+    for h in range(Hq):
+        g = h // 2
+        for i in range(Nq):
+            s = scale * (kf[: i + 1, g, :] @ qf[i, h, :])
+            assert abs(np.exp(s - lse[i, h]).sum() - 1.0) < 1e-12
+
+
+def test_causal_first_row_sees_only_first_key():
+    N, H, d = 20, 3, 8
+    q, k, v = _rand_case(11, N, H, d), _rand_case(12, N, H, d), _rand_case(13, N, H, d)
+    o, lse = oracle.attn_fwd(q, k, v, 1, H, H, N, N, d, 0.5, True)
+    np.testing.assert_array_equal(o[0], _f(v)[0])
+    np.testing.assert_allclose(lse[0], 0.5 * np.einsum("hc,hc->h", _f(q)[0], _f(k)[0]), rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("Nq,Nk", [(8, 8), (5, 12), (12, 5)])
+def test_zero_query_gives_mean_of_visible_values(Nq, Nk):
+    """Q = 0: every visible key has weight 1/count, so O is the mean of the visible V rows and
+    LSE = ln(count); count = i + 1 + (Nk - Nq) clipped to [0, Nk] (bottom-right alignment)."""
+    H, d = 2, 4
+    q = np.zeros((Nq, H, d), dtype=np.uint16)
+    k, v = _rand_case(21, Nk, H, d), _rand_case(22, Nk, H, d)
+    o, lse = oracle.attn_fwd(q, k, v, 1, H, H, Nq, Nk, d, 1.0, True)
+    vf = _f(v)
+    for i in range(Nq):
+        cnt = min(max(i + 1 + (Nk - Nq), 0), Nk)
+        for h in range(H):
+            if cnt == 0:
+                assert np.all(o[i, h] == 0) and lse[i, h] == -np.inf
+            else:
+                np.testing.assert_allclose(o[i, h], vf[:cnt, h].mean(axis=0), rtol=0, atol=1e-14)
+                assert abs(lse[i, h] - math.log(cnt)) < 1e-14
+
+
+def test_masked_positions_do_not_matter():
+    N, H, d = 16, 2, 8
+    q, k, v = _rand_case(31, N, H, d), _rand_case(32, N, H, d), _rand_case(33, N, H, d)
+    o1, l1 = oracle.attn_fwd(q, k, v, 1, H, H, N, N, d, 0.3, True)
+    k2, v2 = k.copy(), v.copy()
+    k2[N // 2:] = _rand_case(34, N - N // 2, H, d, 5.0)
+    v2[N // 2:] = _rand_case(35, N - N // 2, H, d, 5.0)
+    o2, l2 = oracle.attn_fwd(q, k2, v2, 1, H, H, N, N, d, 0.3, True)
+    np.testing.assert_array_equal(o1[: N // 2], o2[: N // 2])
+    np.testing.assert_array_equal(l1[: N // 2], l2[: N // 2])
+    assert not np.array_equal(o1[N // 2:], o2[N // 2:])
+
+
+def test_dominant_score_selects_its_value():
+    N, d = 10, 4
+    q = _bf16(np.ones((1, 1, d)))
+    kf = np.zeros((N, 1, d), dtype=np.float32)
+    kf[6] = 10.0  # score 40 on key 6, 0 elsewhere
+    v = _rand_case(41, N, 1, d)
+    o, lse = oracle.attn_fwd(q, _bf16(kf), v, 1, 1, 1, 1, N, d, 1.0, False)
+    w_other = math.exp(-40.0)
+    np.testing.assert_allclose(o[0, 0], _f(v)[6, 0], rtol=0, atol=N * w_other * 10)
+    assert abs(lse[0, 0] - (40.0 + math.log1p((N - 1) * w_other))) < 1e-12
+
+
+def test_gqa_equals_repeated_heads():
+    N, Hq, Hkv, d = 24, 8, 2, 16
+    q, k, v = _rand_case(51, N, Hq, d), _rand_case(52, N, Hkv, d), _rand_case(53, N, Hkv, d)
+    o1, l1 = oracle.attn_fwd(q, k, v, 1, Hq, Hkv, N, N, d, 0.2, True)
+    kr, vr = np.repeat(k, Hq // Hkv, axis=1), np.repeat(v, Hq // Hkv, axis=1)
+    o2, l2 = oracle.attn_fwd(q, kr, vr, 1, Hq, Hq, N, N, d, 0.2, True)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_varlen_equals_each_sequence_alone():
+    lens = [5, 17, 1, 9]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T, Hq, Hkv, d = int(cu[-1]), 4, 2, 8
+    q, k, v = _rand_case(61, T, Hq, d), _rand_case(62, T, Hkv, d), _rand_case(63, T, Hkv, d)
+    o, lse = oracle.attn_fwd(q, k, v, len(lens), Hq, Hkv, max(lens), max(lens), d, 0.35, True, cu_seqlens=cu)
+    for b, L in enumerate(lens):
+        s, e = cu[b], cu[b + 1]
+        ob, lb = oracle.attn_fwd(q[s:e], k[s:e], v[s:e], 1, Hq, Hkv, L, L, d, 0.35, True)
+        np.testing.assert_array_equal(o[s:e], ob)
+        np.testing.assert_array_equal(lse[s:e], lb)
+
+
+def test_dense_batches_are_independent():
+    B, N, H, d = 3, 6, 2, 4
+    q, k, v = _rand_case(71, B * N, H, d), _rand_case(72, B * N, H, d), _rand_case(73, B * N, H, d)
+    o, lse = oracle.attn_fwd(q, k, v, B, H, H, N, N, d, 0.5, False)
+    for b in range(B):
+        sl = slice(b * N, (b + 1) * N)
+        ob, lb = oracle.attn_fwd(q[sl], k[sl], v[sl], 1, H, H, N, N, d, 0.5, False)
+        np.testing.assert_array_equal(o[sl], ob)
+        np.testing.assert_array_equal(lse[sl], lb)
+
+
+def test_row_subset_matches_full():
+    case = W.PrefillCase("t", 2, 4, 2, 40, 40, 16, 0.25, True, 99)
+    q, k, v = case.generate()
+    o, lse = oracle.attn_fwd(q, k, v, 2, 4, 2, 40, 40, 16, 0.25, True)
+    rows = np.array([0, 5, 77, 159, 320 - 1, 100], dtype=np.int64)
+    os_, ls_ = oracle.attn_fwd(q, k, v, 2, 4, 2, 40, 40, 16, 0.25, True, rows=rows)
+    np.testing.assert_array_equal(os_, o.reshape(-1, 16)[rows])
+    np.testing.assert_array_equal(ls_, lse.reshape(-1)[rows])
+
+
+# ------------------------------------------------------- online recurrence == 3 pass
+
+@pytest.mark.parametrize("tau", [0.0, 8.0])
+@pytest.mark.parametrize("block", [1, 7, 128])
+@pytest.mark.parametrize("group", [1, 32])
+def test_online_recurrence_equals_three_pass(tau, block, group):
+    Nq = Nk = 160
+    Hq, d = 2, 16
+    q = _rand_case(81, Nq, Hq, d, 2.0)
+    k = _rand_case(82, Nk, Hq, d)
+    v = _rand_case(83, Nk, Hq, d)
+    scale = 1.0 / math.sqrt(d)
+    o3, l3 = oracle.attn_fwd(q, k, v, 1, Hq, Hq, Nq, Nk, d, scale, True)
+    s = oracle.scores_dense(_f(q), _f(k), scale, True, Nq, Nk, 1)
+    vf = _f(v)
+    for h in range(Hq):
+        sb = [s[h][:, j:j + block] for j in range(0, Nk, block)]
+        vb = [vf[j:j + block, h, :] for j in range(0, Nk, block)]
+        o, lse = oracle.online_attention(sb, vb, tau=tau, group=group)
+        np.testing.assert_allclose(o, o3[:, h], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse, l3[:, h], rtol=1e-12, atol=1e-12)
+
+
+def test_stale_max_lags_true_max_by_at_most_tau():
+    N, d, tau = 256, 16, 8.0
+    q, k = _rand_case(91, N, 1, d, 3.0), _rand_case(92, N, 1, d)
+    v = _rand_case(93, N, 1, d)
+    s = oracle.scores_dense(_f(q), _f(k), 0.25, False, N, N, 1)[0]
+    sb = [s[:, j:j + 16] for j in range(0, N, 16)]
+    vb = [_f(v)[j:j + 16, 0, :] for j in range(0, N, 16)]
+    _, _, hist = oracle.online_attention(sb, vb, tau=tau, history=True)
+    rescales = 0
+    prev = None
+    for n, (m, _, _) in enumerate(hist):
+        true_max = s[:, : (n + 1) * 16].max(axis=1)
+        assert np.all(m <= true_max)
+        assert np.all((true_max - m) * oracle.LOG2E <= tau + 1e-12)
+        if prev is not None:
+            assert np.all(m >= prev)
+            rescales += int((m != prev).sum())
+        prev = m
+    assert rescales < (len(hist) - 1) * N  # the threshold skips some updates
+
+
+# --------------------------------------------------------------------- decode
+
+def _small_decode(seed=123, extra_pages=0, page_size=16, B=5, Hq=8, Hkv=2, d=32):
+    lens = synth.uniform_ints(B, seed, 1, 150)
+    max_pages = int((lens.max() + page_size - 1) // page_size) + 1
+    return W.DecodeCase("small", B, Hq, Hkv, d, page_size, lens, max_pages, 1.0 / math.sqrt(d), seed,
+                        extra_pages=extra_pages)
+
+
+@pytest.mark.parametrize("page_size", [1, 3, 16])
+def test_decode_equals_contiguous_forward(page_size):
+    c = _small_decode(page_size=page_size)
+    q, kc, vc, pt, sl = c.generate()
+    o, lse = oracle.attn_decode_paged(q, kc, vc, pt, sl, c.page_size, c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.scale)
+    for b in range(c.B):
+        L = int(sl[b])
+        toks = np.arange(L)
+        phys = pt[b, toks // page_size] * page_size + toks % page_size
+        kb = kc.reshape(-1, c.Hkv, c.d)[phys]
+        vb = vc.reshape(-1, c.Hkv, c.d)[phys]
+        for causal in (False, True):
+            ob, lb = oracle.attn_fwd(q[b:b + 1], kb, vb, 1, c.Hq, c.Hkv, 1, L, c.d, c.scale, causal)
+            np.testing.assert_array_equal(o[b], ob[0])
+            np.testing.assert_array_equal(lse[b], lb[0])
+
+
+def test_decode_invariant_under_page_permutation():
+    c = _small_decode(seed=7)
+    q, kc, vc, pt, sl = c.generate()
+    o1, l1 = oracle.attn_decode_paged(q, kc, vc, pt, sl, c.page_size, c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.scale)
+    perm = synth.permutation(c.num_pages, 4242)
+    kc2, vc2 = np.empty_like(kc), np.empty_like(vc)
+    kc2[perm], vc2[perm] = kc, vc  # physical page p moves to perm[p]
+    pt2 = pt.copy()
+    for b in range(c.B):
+        n = int(c.pages_per_seq[b])
+        pt2[b, :n] = perm[pt[b, :n]]
+    o2, l2 = oracle.attn_decode_paged(q, kc2, vc2, pt2, sl, c.page_size, c.B, c.Hq, c.Hkv, c.d, c.max_pages,
+                                      c.scale)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_decode_ignores_unreferenced_nan_pages():
+    c = _small_decode(seed=9, extra_pages=6)
+    q, kc, vc, pt, sl = c.generate()
+    used = np.zeros(c.num_pages, dtype=bool)
+    for b in range(c.B):
+        used[pt[b, : int(c.pages_per_seq[b])]] = True
+    assert (~used).sum() == 6
+    kc[~used] = 0x7FC0
+    vc[~used] = 0x7FC0
+    o, lse = oracle.attn_decode_paged(q, kc, vc, pt, sl, c.page_size, c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.scale)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+
+
+# ----------------------------------------------------------------- exp2 model
+
+def test_exp2_cubic_error_table():
+    g = _golden("exp2_error_table.json")
+    mx, _, arg = oracle.exp2_cubic_sweep(0)   # every fp32 in [0, 1)
+    _, mean, _ = oracle.exp2_cubic_sweep(1)   # uniform grid for the mean
+    assert mx <= 2e-4
+    # with the four printed digits the maximum sits at f -> 1 (p(1) = 1.9998) ...
+    assert 0.99 < arg < 1.0 and abs(mx - 1.0e-4) < 1e-6
+    # ... and the mean matches the page's degree-3 row
+    assert abs(mean - g["table"]["degree_3"]["mean_rel"]) / g["table"]["degree_3"]["mean_rel"] < 0.01
+    # degree 3 is far below bf16 quantisation, as the page argues
+    assert mx < g["bf16_quantisation_error"] / 30
+
+
+def test_magic_bias_floor_is_floor():
+    xs = np.concatenate([np.linspace(-127.0, 8.0, 100001, dtype=np.float32),
+                         np.arange(-127, 9, dtype=np.float32),
+                         np.nextafter(np.arange(-127, 9, dtype=np.float32), np.float32(-200)),
+                         np.nextafter(np.arange(-127, 9, dtype=np.float32), np.float32(200))])
+    for x in xs[::97]:
+        assert oracle.floor_magic(float(x)) == math.floor(float(x))
+
+
+def test_exp2_poly_full_range():
+    rng = np.random.default_rng(3)
+    x = rng.uniform(-126.0, 8.0, 200000).astype(np.float32)
+    y = oracle.exp2_poly(x).astype(np.float64)
+    rel = np.abs(y - np.exp2(x.astype(np.float64))) / np.exp2(x.astype(np.float64))
+    assert rel.max() <= 2e-4
+    ints = np.arange(-126, 9, dtype=np.float32)
+    np.testing.assert_array_equal(oracle.exp2_poly(ints), np.exp2(ints.astype(np.float64)).astype(np.float32))
+    assert oracle.exp2_poly([-127.0])[0] == 0.0
+    assert oracle.exp2_poly([-500.0])[0] == 0.0
+    assert oracle.exp2_poly([-np.inf])[0] == 0.0
+    assert oracle.exp2_cubic(0.0) == 1.0
+
+
+def test_exp2_poly_scaling_by_powers_of_two_is_exact():
+    f = (np.arange(1024, dtype=np.float32) / np.float32(1024))  # exact after adding the integers below
+    base = oracle.exp2_poly(f)
+    for n in (-100, -7, 3):
+        np.testing.assert_array_equal(oracle.exp2_poly(f + np.float32(n)), base * np.float32(2.0**n))
