@@ -1,0 +1,390 @@
+// C ABI of the attention library: argument checks, TMA descriptors, launch planning,
+// the device status word and process-wide options. Every compute step runs in the
+// kernels of attn_fwd.cu and attn_decode.cu.
+#include "attn.h"
+#include "kernels.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <math.h>
+#include <mutex>
+#include <string.h>
+
+namespace {
+
+using attn::DecodeParams;
+using attn::FwdParams;
+using attn::FwdTmaps;
+
+constexpr int kMaxDevices = 64;
+
+__device__ int g_status[4];
+__device__ unsigned long long g_counters[attn::kNumCounters];
+
+struct Options {
+    int exp_poly = 0;
+    double rescale_threshold = 8.0;
+    int decode_chunk = 0;
+    int sec_heads = 0;
+    int count = 0;
+    double watchdog_ms = 4000.0;
+};
+
+std::mutex g_mu;
+Options g_opt;
+
+struct DeviceState {
+    bool init = false;
+    bool arch_ok = false;
+    int num_sms = 0;
+    int* status = nullptr;
+    unsigned long long* counters = nullptr;
+    cudaMemPool_t pool = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+attn_status_t device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.init) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        st.arch_ok = (major == 10 && minor == 3);
+        st.num_sms = sms;
+        if (st.arch_ok) {
+            if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status), g_status) != cudaSuccess) return ATTN_ERR_CUDA;
+            if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.counters), g_counters) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+        }
+        st.init = true;
+    }
+    if (!st.arch_ok) return ATTN_ERR_UNSUPPORTED_ARCH;
+    *out = &st;
+    return ATTN_OK;
+}
+
+attn_status_t encode_fn() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode) return ATTN_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return ATTN_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return ATTN_OK;
+}
+
+// 3-D map over a [rows, heads, d] bf16 tensor; box = 64 elements of d x 1 head x 128 rows,
+// 128-byte swizzle (the K-major / MN-major canonical layout the MMAs read), zero fill
+// outside [0, rows).
+attn_status_t make_map(CUtensorMap* m, const void* base, long long rows, int heads, int d) {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+Options options() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_opt;
+}
+
+int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_version(void) { return "exact_softmax_attention_gb300 0.1 (sm_103a)"; }
+
+const char* attn_status_string(attn_status_t s) {
+    switch (s) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_NULL_PTR: return "a required pointer is NULL";
+        case ATTN_ERR_BAD_SHAPE: return "unsupported or inconsistent sizes";
+        case ATTN_ERR_ALIGN: return "a pointer is not aligned as required";
+        case ATTN_ERR_UNSUPPORTED_ARCH: return "the current device is not an sm_103 GPU";
+        case ATTN_ERR_CUDA: return "a CUDA call failed";
+        case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting on its pipeline (device watchdog)";
+        case ATTN_ERR_DEVICE_BAD_INDEX: return "a page index or sequence length was out of range";
+        case ATTN_ERR_BAD_ARG: return "unknown option or invalid value";
+        default: return "unknown status";
+    }
+}
+
+attn_status_t attn_set_option(const char* name, double value) {
+    if (!name) return ATTN_ERR_NULL_PTR;
+    if (!isfinite(value)) return ATTN_ERR_BAD_ARG;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!strcmp(name, "exp_poly")) {
+        if (value != 0 && value != 1) return ATTN_ERR_BAD_ARG;
+        g_opt.exp_poly = (int)value;
+    } else if (!strcmp(name, "rescale_threshold")) {
+        if (value < 0 || value > 60) return ATTN_ERR_BAD_ARG;
+        g_opt.rescale_threshold = value;
+    } else if (!strcmp(name, "decode_chunk")) {
+        if (value < 0 || value > (1 << 24)) return ATTN_ERR_BAD_ARG;
+        g_opt.decode_chunk = (int)value;
+    } else if (!strcmp(name, "sec_heads")) {
+        if (value < 0 || value > 65536) return ATTN_ERR_BAD_ARG;
+        g_opt.sec_heads = (int)value;
+    } else if (!strcmp(name, "count")) {
+        if (value != 0 && value != 1) return ATTN_ERR_BAD_ARG;
+        g_opt.count = (int)value;
+    } else if (!strcmp(name, "watchdog_ms")) {
+        if (value < 1 || value > 600000) return ATTN_ERR_BAD_ARG;
+        g_opt.watchdog_ms = value;
+    } else {
+        return ATTN_ERR_BAD_ARG;
+    }
+    return ATTN_OK;
+}
+
+attn_status_t attn_get_option(const char* name, double* value) {
+    if (!name || !value) return ATTN_ERR_NULL_PTR;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!strcmp(name, "exp_poly")) *value = g_opt.exp_poly;
+    else if (!strcmp(name, "rescale_threshold")) *value = g_opt.rescale_threshold;
+    else if (!strcmp(name, "decode_chunk")) *value = g_opt.decode_chunk;
+    else if (!strcmp(name, "sec_heads")) *value = g_opt.sec_heads;
+    else if (!strcmp(name, "count")) *value = g_opt.count;
+    else if (!strcmp(name, "watchdog_ms")) *value = g_opt.watchdog_ms;
+    else return ATTN_ERR_BAD_ARG;
+    return ATTN_OK;
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                       int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens, void* stream) {
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL_PTR;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq < 0 || Nk < 0 || (d != 64 && d != 128))
+        return ATTN_ERR_BAD_SHAPE;
+    if (causal != 0 && causal != 1) return ATTN_ERR_BAD_SHAPE;
+    if (!isfinite(scale)) return ATTN_ERR_BAD_SHAPE;
+    if (Hq > 65535 || Hkv > 65535) return ATTN_ERR_BAD_SHAPE;
+    if (cu_seqlens && B > attn::fwd_max_varlen_batch()) return ATTN_ERR_BAD_SHAPE;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+        (cu_seqlens && !aligned(cu_seqlens, 4)))
+        return ATTN_ERR_ALIGN;
+    // rows of q/o and of k/v: dense B*N; packed: Nq and Nk are the total packed rows
+    const long long Tq = cu_seqlens ? (long long)Nq : (long long)B * Nq;
+    const long long Tk = cu_seqlens ? (long long)Nk : (long long)B * Nk;
+    if (Tq > INT32_MAX - 1024 || Tk > INT32_MAX - 1024) return ATTN_ERR_BAD_SHAPE;
+    if (B == 0 || Tq == 0) return ATTN_OK;
+    DeviceState* ds = nullptr;
+    attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+    if ((st = encode_fn()) != ATTN_OK) return st;
+    FwdTmaps tm;
+    if (make_map(&tm.q, q, Tq, Hq, d) != ATTN_OK || make_map(&tm.k, k, Tk, Hkv, d) != ATTN_OK ||
+        make_map(&tm.v, v, Tk, Hkv, d) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    const Options opt = options();
+    FwdParams p;
+    memset(&p, 0, sizeof p);
+    p.o = reinterpret_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.cu_seqlens = cu_seqlens;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.causal = causal;
+    p.scale = scale;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.rescale_thr = (float)opt.rescale_threshold;
+    // scheduling section: largest multiple of G dividing Hq that is <= target heads
+    int target = opt.sec_heads > 0 ? opt.sec_heads : 8;
+    if (target < p.G) target = p.G;
+    int sec = p.G;
+    for (int c = p.G; c <= Hq && c <= target; c += p.G)
+        if (Hq % c == 0) sec = c;
+    p.sec_q = sec;
+    p.status = ds->status;
+    p.counters = opt.count ? ds->counters : nullptr;
+    p.watchdog_ns = (unsigned long long)(opt.watchdog_ms * 1e6);
+    int grid = ds->num_sms;
+    if (!cu_seqlens) {
+        const long long tiles = (long long)B * Hq * cdiv(Nq, 256);
+        if (tiles > INT32_MAX) return ATTN_ERR_BAD_SHAPE;
+        p.total_tiles = (int)tiles;
+        if (tiles < grid) grid = (int)tiles;
+    } else {
+        p.total_tiles = 0;
+    }
+    if (grid <= 0) return ATTN_OK;
+    const cudaError_t e = attn::launch_attn_fwd(tm, p, d, opt.exp_poly, grid, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_decode_plan(int B, int Hkv, int max_pages_per_seq, int page_size, int num_splits, int num_sms,
+                               int* chunk, int* max_splits) {
+    if (!chunk || !max_splits) return ATTN_ERR_NULL_PTR;
+    if (B < 0 || Hkv <= 0 || max_pages_per_seq <= 0 || page_size <= 0 || num_splits < 0) return ATTN_ERR_BAD_SHAPE;
+    const long long lmax = (long long)max_pages_per_seq * page_size;
+    if (lmax > INT32_MAX / 2) return ATTN_ERR_BAD_SHAPE;
+    if (num_sms <= 0) {
+        DeviceState* ds = nullptr;
+        const attn_status_t st = device_state(&ds);
+        if (st != ATTN_OK) return st;
+        num_sms = ds->num_sms;
+    }
+    const Options opt = options();
+    long long c;
+    if (num_splits > 0) {
+        c = (lmax + num_splits - 1) / num_splits;
+    } else if (opt.decode_chunk > 0) {
+        c = opt.decode_chunk;
+    } else {
+        // Enough (sequence, kv head, split) items for ~32 per SM, assuming the average
+        // sequence fills half of its page-table row; at least 256 tokens per split.
+        const long long work = (long long)(B > 0 ? B : 1) * Hkv * ((lmax + 1) / 2);
+        const long long items = 32LL * num_sms;
+        c = (work + items - 1) / items;
+        if (c < 256) c = 256;
+        if (c > 8192) c = 8192;
+    }
+    c = ((c + 63) / 64) * 64;
+    if (c > lmax) c = ((lmax + 63) / 64) * 64;
+    if (c < 64) c = 64;
+    *chunk = (int)c;
+    *max_splits = cdiv(lmax, c);
+    return ATTN_OK;
+}
+
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* page_table,
+                                const int* seqlens, int page_size, void* o, float* lse, void* stream, int B, int Hq,
+                                int Hkv, int d, int max_pages_per_seq, int num_pages, float scale, int num_splits) {
+    if (!q || !k_cache || !v_cache || !page_table || !seqlens || !o || !lse) return ATTN_ERR_NULL_PTR;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq / Hkv > 16 || (d != 64 && d != 128) || page_size <= 0 ||
+        max_pages_per_seq <= 0 || num_pages <= 0 || num_splits < 0 || B > 65535 || Hkv > 65535)
+        return ATTN_ERR_BAD_SHAPE;
+    if (!isfinite(scale)) return ATTN_ERR_BAD_SHAPE;
+    if (!aligned(q, 16) || !aligned(o, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(lse, 4) ||
+        !aligned(page_table, 4) || !aligned(seqlens, 4))
+        return ATTN_ERR_ALIGN;
+    if (B == 0) return ATTN_OK;
+    DeviceState* ds = nullptr;
+    attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+    int chunk = 0, max_splits = 0;
+    st = attn_decode_plan(B, Hkv, max_pages_per_seq, page_size, num_splits, ds->num_sms, &chunk, &max_splits);
+    if (st != ATTN_OK) return st;
+    const Options opt = options();
+    DecodeParams p;
+    memset(&p, 0, sizeof p);
+    p.q = reinterpret_cast<const __nv_bfloat16*>(q);
+    p.k_cache = reinterpret_cast<const __nv_bfloat16*>(k_cache);
+    p.v_cache = reinterpret_cast<const __nv_bfloat16*>(v_cache);
+    p.page_table = page_table;
+    p.seqlens = seqlens;
+    p.o = reinterpret_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.page_size = page_size;
+    p.max_pages = max_pages_per_seq;
+    p.num_pages = num_pages;
+    p.chunk = chunk;
+    p.max_splits = max_splits;
+    p.scale = scale;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.rescale_thr = (float)opt.rescale_threshold;
+    p.status = ds->status;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void* ws = nullptr;
+    if (max_splits > 1) {
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            if (!ds->pool) {
+                int dev = 0;
+                if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+                cudaMemPoolProps props;
+                memset(&props, 0, sizeof props);
+                props.allocType = cudaMemAllocationTypePinned;
+                props.location.type = cudaMemLocationTypeDevice;
+                props.location.id = dev;
+                if (cudaMemPoolCreate(&ds->pool, &props) != cudaSuccess) return ATTN_ERR_CUDA;
+                uint64_t keep = UINT64_MAX;
+                cudaMemPoolSetAttribute(ds->pool, cudaMemPoolAttrReleaseThreshold, &keep);
+            }
+        }
+        const size_t n_o = (size_t)B * Hq * max_splits * d;
+        const size_t n_l = (size_t)B * Hq * max_splits;
+        if (cudaMallocFromPoolAsync(&ws, (n_o + n_l) * sizeof(float), ds->pool, s) != cudaSuccess) return ATTN_ERR_CUDA;
+        p.ws_o = reinterpret_cast<float*>(ws);
+        p.ws_lse = p.ws_o + n_o;
+    }
+    const cudaError_t e = attn::launch_attn_decode(p, d, s);
+    if (ws) cudaFreeAsync(ws, s);
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_get_device_status(void* stream) {
+    DeviceState* ds = nullptr;
+    attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    int h[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(h, ds->status, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+    const int zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(ds->status, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+    return h[0];
+}
+
+attn_status_t attn_read_counters(unsigned long long* out, int n) {
+    if (!out) return ATTN_ERR_NULL_PTR;
+    if (n < 0) return ATTN_ERR_BAD_ARG;
+    DeviceState* ds = nullptr;
+    attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+    unsigned long long h[attn::kNumCounters] = {};
+    if (cudaMemcpy(h, ds->counters, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+    unsigned long long z[attn::kNumCounters] = {};
+    if (cudaMemcpy(ds->counters, z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+    for (int i = 0; i < n && i < attn::kNumCounters; ++i) out[i] = h[i];
+    return ATTN_OK;
+}
+
+attn_status_t attn_debug_exp2(const float* x, float* y, long long n, int mode, void* stream) {
+    if (!x || !y) return ATTN_ERR_NULL_PTR;
+    if (n < 0 || (mode != 0 && mode != 1)) return ATTN_ERR_BAD_ARG;
+    if (!aligned(x, 4) || !aligned(y, 4)) return ATTN_ERR_ALIGN;
+    DeviceState* ds = nullptr;
+    attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+    return attn::launch_exp2_probe(x, y, n, mode, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_debug_watchdog(unsigned long long limit_ns, void* stream) {
+    if (limit_ns == 0 || limit_ns > 10000000000ull) return ATTN_ERR_BAD_ARG;
+    DeviceState* ds = nullptr;
+    attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+    return attn::launch_watchdog_probe(ds->status, limit_ns, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,398 @@
+// Paged-KV split-KV decode for sm_103a (GB300): one query token per sequence.
+//
+// "Faster, more flexible FA4 for LLM inference":
+//  - PR 1999/2104: pages of any size are gathered with per-thread cp.async rather than
+//    TMA, and the 64-bit row addresses are generated once per row and handed out by
+//    warp shuffles ("transposed" address generation) instead of being recomputed by
+//    every thread that copies a piece of the row;
+//  - PR 1940: split-KV (Flash-Decoding): several CTAs share one sequence's keys, each
+//    writes a partial output and its log-sum-exp, and a separate combine kernel merges
+//    them; num_splits = 0 picks the split size from the SM count and the lengths;
+//  - PR 2186: GQA packing: all query heads of one key/value head are computed from one
+//    copy of each K/V row.
+// The online-softmax recurrence ("FlashAttention: not computing less, moving less",
+// section 02) runs per warp over its tokens; the warps of a CTA and then the splits
+// are merged with the same max-shifted LSE weighting.
+//
+// Split kernel: grid (split, kv head, sequence), 4 warps. Each warp owns a private
+// cp.async ring of NST stages of 16 tokens (K and V rows, 128-byte XOR swizzle) and
+// processes token groups w, w+4, w+8, ... of the split, so the main loop needs no
+// CTA-wide barrier. Scores S = Q K^T use m16n8k16 bf16 MMAs with the (up to 16) query
+// heads of the group as rows; O^T += V^T P^T reuses the score accumulators as the B
+// operand directly.
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+#include <math.h>
+
+namespace attn {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kGroup = 16;  // tokens per warp-stage
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+template <int D>
+struct DecLayout {
+    static constexpr int kRowBytes = D * 2;
+    static constexpr int kTileBytes = kGroup * kRowBytes;  // one K or V warp-stage
+    static constexpr int kChunksPerRow = D / 8;             // 16-byte chunks
+};
+
+// Byte offset of 16-byte chunk c of row r inside a [16 x D] bf16 warp-stage tile.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+    return (uint32_t)(r * (D * 2) + ((c ^ (r & 7)) << 4));
+}
+
+template <int D, int GN, int NST>
+__global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeParams p) {
+    using L = DecLayout<D>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long max_len = (long long)p.max_pages * p.page_size;
+
+    int len = __ldg(p.seqlens + b);
+    if (len < 0 || len > max_len) {
+        if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevBadIndex);
+        len = len < 0 ? 0 : (int)max_len;
+    }
+    const int nsplit = cdiv(len, p.chunk);
+    const int t_begin = split * p.chunk;
+    if (len == 0) {
+        // No cached keys: the output is 0 and the log-sum-exp is -inf (written by split 0).
+        if (split == 0) {
+            for (int i = threadIdx.x; i < p.G * D; i += blockDim.x) {
+                const int h = kvh * p.G + i / D;
+                p.o[((long long)b * p.Hq + h) * D + (i % D)] = __float2bfloat16(0.0f);
+            }
+            if (threadIdx.x < p.G) p.lse[(long long)b * p.Hq + kvh * p.G + threadIdx.x] = -INFINITY;
+        }
+        return;
+    }
+    if (t_begin >= len) return;
+    const int t_end = min(len, t_begin + p.chunk);
+
+    // ---- query fragments: rows = query heads of this kv head (padded to 16), k = d
+    const int g0 = lane >> 2;
+    const int h0 = kvh * p.G + g0, h1 = kvh * p.G + g0 + 8;
+    const bool v0 = g0 < p.G, v1 = (GN == 16) && (g0 + 8 < p.G);
+    const uint32_t* q0p = reinterpret_cast<const uint32_t*>(p.q + ((long long)b * p.Hq + h0) * D);
+    const uint32_t* q1p = reinterpret_cast<const uint32_t*>(p.q + ((long long)b * p.Hq + h1) * D);
+    uint32_t aq[D / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const int c = kk * 8 + (lane & 3);  // u32 index of columns kk*16 + 2*(lane%4)
+        aq[kk][0] = v0 ? __ldg(q0p + c) : 0u;
+        aq[kk][1] = v1 ? __ldg(q1p + c) : 0u;
+        aq[kk][2] = v0 ? __ldg(q0p + c + 4) : 0u;
+        aq[kk][3] = v1 ? __ldg(q1p + c + 4) : 0u;
+    }
+
+    // ---- per-warp ring
+    uint8_t* ring = smem + warp * NST * 2 * L::kTileBytes;
+    const uint32_t ring_s = smem_u32(ring);
+    const long long row_stride = (long long)p.Hkv * D;  // elements between consecutive cache rows
+    const int* pt = p.page_table + (long long)b * p.max_pages;
+    constexpr int kRowsPerIter = 32 / L::kChunksPerRow;
+    constexpr int kIters = kGroup / kRowsPerIter;
+    const int my_chunk = lane % L::kChunksPerRow;
+    const int my_row0 = lane / L::kChunksPerRow;
+
+    // groups handled by this warp: t_begin + 16 * (warp + 4 * i)
+    const int n_groups_total = cdiv(t_end - t_begin, kGroup);
+    const int my_groups = n_groups_total > warp ? cdiv(n_groups_total - warp, kWarps) : 0;
+
+    auto issue = [&](int i) {
+        const int slot = i % NST;
+        const int g = t_begin + kGroup * (warp + kWarps * i);
+        // lane r (r < 16) resolves row r of the group once; others mirror lanes 0-15
+        const int tok = g + (lane & 15);
+        long long off = 0;
+        int ok = 0;
+        if (tok < t_end) {
+            const int pg = __ldg(pt + tok / p.page_size);
+            if (pg >= 0 && pg < p.num_pages) {
+                off = ((long long)pg * p.page_size + (tok % p.page_size)) * row_stride + (long long)kvh * D;
+                ok = 1;
+            } else {
+                atomicCAS(p.status, 0, kDevBadIndex);
+            }
+        }
+        const uint32_t kdst = ring_s + slot * 2 * L::kTileBytes;
+        const uint32_t vdst = kdst + L::kTileBytes;
+#pragma unroll
+        for (int it = 0; it < kIters; ++it) {
+            const int r = it * kRowsPerIter + my_row0;
+            const long long ro = __shfl_sync(0xffffffffu, off, r);
+            const int rok = __shfl_sync(0xffffffffu, ok, r);
+            const __nv_bfloat16* ks = rok ? p.k_cache + ro + my_chunk * 8 : p.k_cache;
+            const __nv_bfloat16* vs = rok ? p.v_cache + ro + my_chunk * 8 : p.v_cache;
+            cp_async16(kdst + swz<D>(r, my_chunk), ks, rok ? 16u : 0u);
+            cp_async16(vdst + swz<D>(r, my_chunk), vs, rok ? 16u : 0u);
+        }
+    };
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+    constexpr int NH = GN / 8;
+    float oacc[NH][D / 16][4];
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) oacc[nh][mt][e] = 0.0f;
+
+    const float sl2 = p.scale_log2;
+    // ldmatrix row/chunk for this lane: token (lane % 8) + 8 * (lane / 16), chunk parity (lane / 8) & 1
+    const int lm_row = (lane & 7) + ((lane >> 4) << 3);
+    const int lm_par = (lane >> 3) & 1;
+
+#pragma unroll
+    for (int i = 0; i < NST - 1; ++i) {
+        if (i < my_groups) issue(i);
+        cp_async_commit();
+    }
+    for (int i = 0; i < my_groups; ++i) {
+        cp_async_wait<NST - 2>();
+        __syncwarp();
+        if (i + NST - 1 < my_groups) issue(i + NST - 1);
+        cp_async_commit();
+
+        const int slot = i % NST;
+        const uint32_t kt = ring_s + slot * 2 * L::kTileBytes;
+        const uint32_t vt = kt + L::kTileBytes;
+        const int g = t_begin + kGroup * (warp + kWarps * i);
+
+        // S = Q K^T : rows = heads, columns = 16 tokens (two n8 tiles)
+        float sc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4(kt + swz<D>(lm_row, 2 * kk + lm_par), b0, b1, b2, b3);
+            mma_bf16_16816(sc[0], aq[kk], b0, b1);
+            mma_bf16_16816(sc[1], aq[kk], b2, b3);
+        }
+        // mask tokens past the split end
+        const int tk = g + 2 * (lane & 3);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (tk + nt * 8 + (e & 1) >= t_end) sc[nt][e] = -INFINITY;
+
+        // online softmax per head row (row0 = head g0, row1 = head g0 + 8)
+        float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+        float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mc0 = fmaxf(m0, mx0), mc1 = fmaxf(m1, mx1);
+        const bool need = ((mc0 - m0) * sl2 > p.rescale_thr) || (GN == 16 && (mc1 - m1) * sl2 > p.rescale_thr);
+        if (__any_sync(0xffffffffu, need)) {
+            const float a0 = (m0 == -INFINITY) ? 0.0f : ex2_mufu((m0 - mc0) * sl2);
+            const float a1 = (m1 == -INFINITY) ? 0.0f : ex2_mufu((m1 - mc1) * sl2);
+            l0 *= a0;
+            l1 *= a1;
+            m0 = mc0;
+            m1 = mc1;
+            // O^T columns are heads 2*(lane%4) and +1 (and +8 for the second n8 tile)
+            const int src = (lane & 3) * 8;  // lane holding row 2*(lane%4): lane = 4 * head
+            const float c00 = __shfl_sync(0xffffffffu, a0, src);
+            const float c01 = __shfl_sync(0xffffffffu, a0, src + 4);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                oacc[0][mt][0] *= c00;
+                oacc[0][mt][1] *= c01;
+                oacc[0][mt][2] *= c00;
+                oacc[0][mt][3] *= c01;
+            }
+            if (GN == 16) {
+                const float c10 = __shfl_sync(0xffffffffu, a1, src);
+                const float c11 = __shfl_sync(0xffffffffu, a1, src + 4);
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    oacc[NH - 1][mt][0] *= c10;
+                    oacc[NH - 1][mt][1] *= c11;
+                    oacc[NH - 1][mt][2] *= c10;
+                    oacc[NH - 1][mt][3] *= c11;
+                }
+            }
+        }
+        const float n0 = (m0 == -INFINITY) ? 0.0f : -m0 * sl2;
+        const float n1 = (m1 == -INFINITY) ? 0.0f : -m1 * sl2;
+        float pr[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            pr[nt][0] = ex2_mufu(fmaf(sc[nt][0], sl2, n0));
+            pr[nt][1] = ex2_mufu(fmaf(sc[nt][1], sl2, n0));
+            pr[nt][2] = ex2_mufu(fmaf(sc[nt][2], sl2, n1));
+            pr[nt][3] = ex2_mufu(fmaf(sc[nt][3], sl2, n1));
+        }
+        l0 += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+        l1 += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+        // P^T as the B operand: k = tokens 2*(lane%4) (+8), n = head lane/4 (+8)
+        const uint32_t pb0 = pack_bf16x2(pr[0][0], pr[0][1]);
+        const uint32_t pb1 = pack_bf16x2(pr[1][0], pr[1][1]);
+        const uint32_t pb2 = pack_bf16x2(pr[0][2], pr[0][3]);
+        const uint32_t pb3 = pack_bf16x2(pr[1][2], pr[1][3]);
+        // O^T += V^T P^T : rows = d (16 per m-tile), k = 16 tokens
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            uint32_t a[4];
+            ldmatrix_x4_trans(vt + swz<D>(lm_row, 2 * mt + lm_par), a[0], a[1], a[2], a[3]);
+            mma_bf16_16816(oacc[0][mt], a, pb0, pb1);
+            if (GN == 16) mma_bf16_16816(oacc[NH - 1][mt], a, pb2, pb3);
+        }
+    }
+    cp_async_wait<0>();
+    // row sums over the quad
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    __syncthreads();  // every warp is done with its ring: reuse shared memory for the merge
+
+    // ---- merge the 4 warps: sm_o[w][head][d], sm_m[w][head], sm_l[w][head]
+    float* sm_o = reinterpret_cast<float*>(smem);
+    float* sm_m = sm_o + kWarps * GN * D;
+    float* sm_l = sm_m + kWarps * GN;
+    if ((lane & 3) == 0) {
+        sm_m[warp * GN + g0] = m0;
+        sm_l[warp * GN + g0] = l0;
+        if (GN == 16) {
+            sm_m[warp * GN + g0 + 8] = m1;
+            sm_l[warp * GN + g0 + 8] = l1;
+        }
+    }
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            const int hd = nh * 8 + 2 * (lane & 3);
+            const int dr = mt * 16 + (lane >> 2);
+            float* base = sm_o + (long long)warp * GN * D;
+            base[hd * D + dr] = oacc[nh][mt][0];
+            base[(hd + 1) * D + dr] = oacc[nh][mt][1];
+            base[hd * D + dr + 8] = oacc[nh][mt][2];
+            base[(hd + 1) * D + dr + 8] = oacc[nh][mt][3];
+        }
+    __syncthreads();
+
+    const bool direct = nsplit == 1;
+    for (int idx = threadIdx.x; idx < p.G * D; idx += blockDim.x) {
+        const int hh = idx / D, d = idx - hh * D;
+        float mm = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, sm_m[w * GN + hh]);
+        float ll = 0.0f, acc = 0.0f;
+        if (mm != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float sw = ex2_mufu((sm_m[w * GN + hh] - mm) * sl2);
+                ll += sw * sm_l[w * GN + hh];
+                acc += sw * sm_o[(w * GN + hh) * D + d];
+            }
+        }
+        const float o = ll > 0.0f ? acc / ll : 0.0f;
+        const float lse = ll > 0.0f ? mm * p.scale + logf(ll) : -INFINITY;
+        const long long bh = (long long)b * p.Hq + kvh * p.G + hh;
+        if (direct) {
+            p.o[bh * D + d] = __float2bfloat16(o);
+            if (d == 0) p.lse[bh] = lse;
+        } else {
+            p.ws_o[(bh * p.max_splits + split) * D + d] = o;
+            if (d == 0) p.ws_lse[bh * p.max_splits + split] = lse;
+        }
+    }
+}
+
+// One warp per (sequence, query head): LSE = log sum_s exp(lse_s) (max-shifted, warp
+// shuffles over the splits), O = sum_s exp(lse_s - LSE) O_s.
+template <int D>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long bh = (long long)blockIdx.x * 4 + warp;
+    if (bh >= (long long)p.B * p.Hq) return;
+    const int b = (int)(bh / p.Hq);
+    const long long max_len = (long long)p.max_pages * p.page_size;
+    int len = __ldg(p.seqlens + b);
+    len = len < 0 ? 0 : (len > max_len ? (int)max_len : len);
+    const int ns = cdiv(len, p.chunk);
+    if (ns <= 1) return;  // written directly by the split kernel
+    const float* wl = p.ws_lse + bh * p.max_splits;
+    float mx = -INFINITY;
+    for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, wl[s]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float sum = 0.0f;
+    if (mx != -INFINITY)
+        for (int s = lane; s < ns; s += 32) sum += __expf(wl[s] - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float lse = sum > 0.0f ? mx + logf(sum) : -INFINITY;
+    constexpr int PER = D / 32;
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.0f;
+    if (sum > 0.0f) {
+        const float* wo = p.ws_o + bh * p.max_splits * D;
+        for (int s = 0; s < ns; ++s) {
+            const float w = __expf(wl[s] - lse);
+            if (PER == 4) {
+                const float4 v = *reinterpret_cast<const float4*>(wo + (long long)s * D + lane * 4);
+                acc[0] += w * v.x;
+                acc[1 % PER] += w * v.y;
+                acc[2 % PER] += w * v.z;
+                acc[3 % PER] += w * v.w;
+            } else {
+                const float2 v = *reinterpret_cast<const float2*>(wo + (long long)s * D + lane * 2);
+                acc[0] += w * v.x;
+                acc[1 % PER] += w * v.y;
+            }
+        }
+    }
+    __nv_bfloat16* out = p.o + bh * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t*>(out + e) = pack_bf16x2(acc[e], acc[e + 1]);
+    if (lane == 0) p.lse[bh] = lse;
+}
+
+template <int D, int GN, int NST>
+cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
+    constexpr int ring = kWarps * NST * 2 * DecLayout<D>::kTileBytes;
+    constexpr int merge = (kWarps * GN * D + 2 * kWarps * GN) * 4;
+    constexpr int bytes = ring > merge ? ring : merge;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(decode_split_kernel<D, GN, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const dim3 grid(p.max_splits, p.Hkv, p.B);
+    decode_split_kernel<D, GN, NST><<<grid, kWarps * 32, bytes, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (p.max_splits > 1) {
+        const long long rows = (long long)p.B * p.Hq;
+        decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_decode(const DecodeParams& p, int d, cudaStream_t stream) {
+    constexpr int NST = 3;
+    if (d == 128) return p.G <= 8 ? launch_t<128, 8, NST>(p, stream) : launch_t<128, 16, NST>(p, stream);
+    return p.G <= 8 ? launch_t<64, 8, NST>(p, stream) : launch_t<64, 16, NST>(p, stream);
+}
+
+}  // namespace attn

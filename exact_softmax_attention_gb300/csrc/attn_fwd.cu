@@ -1,0 +1,649 @@
+// Exact softmax attention forward for sm_103a (GB300).
+//
+// Computes O = softmax(scale * Q K^T + mask) V and the per-row log-sum-exp with the
+// online-softmax recurrence ("FlashAttention: not computing less, moving less",
+// section 02: running max m, sum l, unnormalised accumulator a, rescale by
+// exp(m - m'), o = a / l at the end), so no score tile ever leaves the SM.
+//
+// One persistent CTA per SM walks a list of work tiles (sequence, query head,
+// 256-row query block = two 128-row Q tiles). Warp roles (16 warps):
+//   warp 0       TMA producer: Q tiles once per work tile, then a ring of K/V tiles
+//   warp 1       MMA issuer (one thread): S = Q K^T and O += P V with tcgen05.mma,
+//                accumulators in tensor memory; owns the TMEM allocation
+//   warps 4-7    softmax for Q tile 0, warps 8-11 softmax for Q tile 1: one thread per
+//                row reads S from TMEM, masks, takes the row max, decides whether to
+//                rescale O (warp-uniform, only when the max grew by more than the
+//                threshold), computes exponentials (MUFU ex2 and, optionally, a cubic
+//                polynomial on the FMA pipes for a fraction of columns), row sums, and
+//                writes P as bf16 into TMEM over S
+//   warps 12-15  epilogue: O / l, LSE, bf16 store of finished rows
+// The GEMM issue order per KV step follows the two-tile ping-pong of
+// "Low-precision FA4" section 2.1.1 (S0 = Q0 K0, S1 = Q1 K0; then O0 += P0 V_n,
+// S0 = Q0 K_{n+1}, O1 += P1 V_n, S1 = Q1 K_{n+1}; then the last two PV products).
+// The conditional rescale follows "FlashAttention-4: Blackwell algorithm-pipeline
+// co-design", section "conditional softmax rescaling", and "FlashAttention4 精读"
+// section 3.1.4 (warp-uniform decision).
+//
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); P_s (bf16,
+// 64 columns) overlays the first half of S_s. Because S_s(n) is issued after
+// PV_s(n-1) from the same thread, the S_s(n) completion barrier also covers
+// PV_s(n-1), so the softmax warps may rescale O_s right after reading S_s(n).
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+#include <math.h>
+
+namespace attn {
+namespace {
+
+constexpr int BM = 128;  // rows per Q tile
+constexpr int BN = 128;  // keys per K/V tile
+constexpr int kThreads = 512;
+constexpr int kMaxVarlenB = 1024;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct Layout {
+    static constexpr int kQBytes = BM * D * 2;
+    static constexpr int kKVBytes = BN * D * 2;
+    static constexpr int kStages = (D == 128) ? 4 : 6;
+    static constexpr int kChunks = D / 64;                // 128-byte swizzle chunks along d
+    static constexpr int kChunkBytesQ = BM * 128;         // one [128 rows x 64 d] chunk
+    static constexpr int kChunkBytesKV = BN * 128;
+    static constexpr int kQOff = 0;
+    static constexpr int kKVOff = 2 * kQBytes;
+    static constexpr int kBarOff = kKVOff + kStages * kKVBytes;
+    // barrier indices
+    static constexpr int bQFull = 0, bQEmpty = 2, bKVFull = 4, bKVEmpty = 4 + kStages;
+    static constexpr int bSFull = 4 + 2 * kStages, bPFull = bSFull + 2, bOFull = bSFull + 4, bOEmpty = bSFull + 6;
+    static constexpr int bStats = bSFull + 8, bDrain = bSFull + 10;
+    static constexpr int kNumBars = bDrain + 1;
+    static constexpr int kStatsOff = kBarOff + ((kNumBars * 8 + 15) / 16) * 16;
+    static constexpr int kMiscOff = kStatsOff + 2 * 2 * BM * 4;   // m[2][128], l[2][128]
+    static constexpr int kPrefixOff = kMiscOff + 16;               // tmem base, abort flag
+    static constexpr int kBytes = kPrefixOff + (kMaxVarlenB + 1) * 4;
+    static constexpr int kAlloc = kBytes + 1024;                   // slack for 1024-byte alignment
+};
+
+struct Tile {
+    int h, kvh;
+    int q0, k0;   // first token of the sequence in q/o and in k/v
+    int Lq, Lk;   // sequence lengths
+    int r0;       // first row (within the sequence) of Q tile 0
+    int n[2];     // K/V tiles for Q tile 0 and Q tile 1 (0 = tile not computed)
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Packed sequence b: first token and length. Offsets outside [0, Nq] (total packed
+// query rows) or [0, Nk] (total key rows), or decreasing, make the sequence empty; the
+// prefix scan records that as a device error.
+__device__ __forceinline__ bool packed_seq(const FwdParams& p, int b, int& first, int& len) {
+    const int a = __ldg(p.cu_seqlens + b), e = __ldg(p.cu_seqlens + b + 1);
+    const bool ok = a >= 0 && e >= a && e <= p.Nq && e <= p.Nk;
+    first = ok ? a : 0;
+    len = ok ? e - a : 0;
+    return ok;
+}
+
+// Map a work-tile index to its tile. Order inside a sequence: head sections of
+// sec_q query heads (whose key/value heads fit the L2 together), then query
+// blocks heaviest first under a causal mask, then the heads of the section (the
+// query heads of one key/value head are adjacent). Sequences are outermost.
+__device__ __forceinline__ void get_tile(const FwdParams& p, const int* prefix, int w, Tile& t) {
+    int b, u, Lq, Lk, q0, k0;
+    if (p.cu_seqlens) {
+        int lo = 0, hi = p.B;  // prefix[b] <= w < prefix[b+1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (prefix[mid] <= w) lo = mid; else hi = mid;
+        }
+        b = lo;
+        u = w - prefix[b];
+        int first, len;
+        packed_seq(p, b, first, len);
+        q0 = k0 = first;
+        Lq = Lk = len;
+    } else {
+        const int per_b = p.Hq * cdiv(p.Nq, 2 * BM);
+        b = w / per_b;
+        u = w - b * per_b;
+        Lq = p.Nq;
+        Lk = p.Nk;
+        q0 = b * p.Nq;
+        k0 = b * p.Nk;
+    }
+    const int nblk = cdiv(Lq, 2 * BM);
+    const int sec = p.sec_q;
+    const int per_sec = nblk * sec;
+    const int si = u / per_sec;
+    const int rem = u - si * per_sec;
+    const int jj = rem / sec;
+    const int hh = rem - jj * sec;
+    const int j = p.causal ? (nblk - 1 - jj) : jj;
+    t.h = si * sec + hh;
+    t.kvh = t.h / p.G;
+    t.q0 = q0;
+    t.k0 = k0;
+    t.Lq = Lq;
+    t.Lk = Lk;
+    t.r0 = j * 2 * BM;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        const int r = t.r0 + s * BM;
+        int n = 0;
+        if (r < Lq && Lk > 0) {
+            if (p.causal) {
+                const int rl = min(r + BM - 1, Lq - 1);
+                const int kmax = min(Lk, rl + (Lk - Lq) + 1);
+                n = kmax > 0 ? cdiv(kmax, BN) : 0;
+            } else {
+                n = cdiv(Lk, BN);
+            }
+        }
+        t.n[s] = n;
+    }
+}
+
+// Software 2^x on the FMA/ALU pipes ("FlashAttention-4: Blackwell algorithm-pipeline
+// co-design", section "hybrid exponential"; "FlashAttention4 精读" section 3.1.3):
+// clamp at -127; n = floor(x) from the round-down add of the magic bias 1.5 * 2^23,
+// whose low mantissa bits then hold n; 2^f by the Horner cubic with the printed
+// coefficients; 2^n applied by adding n to the exponent field (the bias bits of the
+// magic constant vanish when shifted left by 23).
+__device__ __forceinline__ float ex2_poly(float x) {
+    x = fmaxf(x, -127.0f);
+    const float t = __fadd_rd(x, 12582912.0f);
+    const float f = __fsub_rn(x, __fsub_rn(t, 12582912.0f));
+    float q = __fmaf_rn(0.0771f, f, 0.2276f);
+    q = __fmaf_rn(q, f, 0.6951f);
+    q = __fmaf_rn(q, f, 1.0f);
+    return __uint_as_float(__float_as_uint(q) + (__float_as_uint(t) << 23));
+}
+
+template <int D, int POLY_EVERY>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+    using L = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+    float* st_m = reinterpret_cast<float*>(smem + L::kStatsOff);  // [2][128]
+    float* st_l = st_m + 2 * BM;                                    // [2][128]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+    int* prefix = reinterpret_cast<int*>(smem + L::kPrefixOff);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[L::bQFull + 0], 1);
+        mbar_init(&bars[L::bQFull + 1], 1);
+        mbar_init(&bars[L::bQEmpty + 0], 1);
+        mbar_init(&bars[L::bQEmpty + 1], 1);
+        for (int i = 0; i < L::kStages; ++i) {
+            mbar_init(&bars[L::bKVFull + i], 1);
+            mbar_init(&bars[L::bKVEmpty + i], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[L::bSFull + s], 1);
+            mbar_init(&bars[L::bPFull + s], 4);
+            mbar_init(&bars[L::bOFull + s], 1);
+            mbar_init(&bars[L::bOEmpty + s], 4);
+            mbar_init(&bars[L::bStats + s], 4);
+        }
+        mbar_init(&bars[L::bDrain], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    // Work-tile prefix over packed sequences (warp 2, 32-wide scan).
+    int total = p.total_tiles;
+    if (p.cu_seqlens) {
+        if (warp == 2) {
+            int carry = 0;
+            for (int base = 0; base < p.B; base += 32) {
+                const int b = base + lane;
+                int cnt = 0;
+                if (b < p.B) {
+                    int first, len;
+                    if (!packed_seq(p, b, first, len) && p.status && blockIdx.x == 0) atomicCAS(p.status, 0, kDevBadIndex);
+                    cnt = len > 0 ? p.Hq * cdiv(len, 2 * BM) : 0;
+                }
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                if (b < p.B) prefix[b] = carry + incl - cnt;
+                carry += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) prefix[p.B] = carry;
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (p.cu_seqlens) total = prefix[p.B];
+    const uint32_t tmem = *tmem_slot;
+    const uint64_t wd = p.watchdog_ns;
+
+    // Register split per warpgroup: producer/MMA 56, softmax 184 each, epilogue 80
+    // (sum 504 <= 4 x 128, the registers the CTA is launched with).
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, qphase[2] = {0, 0};
+            int issued = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                Tile t;
+                get_tile(p, prefix, w, t);
+                const int nmax = max(t.n[0], t.n[1]);
+                for (int s = 0; s < 2 && ok; ++s) {
+                    if (t.n[s] == 0) continue;
+                    if (!mbar_wait(&bars[L::bQEmpty + s], qphase[s] ^ 1u, abort_flag, wd)) { ok = false; break; }
+                    qphase[s] ^= 1u;
+                    uint8_t* dst = smem + L::kQOff + s * L::kQBytes;
+                    mbar_arrive_expect_tx(&bars[L::bQFull + s], L::kQBytes);
+#pragma unroll
+                    for (int c = 0; c < L::kChunks; ++c)
+                        tma_load_3d(dst + c * L::kChunkBytesQ, &tmQ, &bars[L::bQFull + s], c * 64, t.h,
+                                    t.q0 + t.r0 + s * BM);
+                }
+                for (int n = 0; n < nmax && ok; ++n) {
+                    for (int kv = 0; kv < 2; ++kv) {
+                        if (!mbar_wait(&bars[L::bKVEmpty + stage], phase ^ 1u, abort_flag, wd)) { ok = false; break; }
+                        uint8_t* dst = smem + L::kKVOff + stage * L::kKVBytes;
+                        mbar_arrive_expect_tx(&bars[L::bKVFull + stage], L::kKVBytes);
+#pragma unroll
+                        for (int c = 0; c < L::kChunks; ++c)
+                            tma_load_3d(dst + c * L::kChunkBytesKV, kv == 0 ? (const void*)&tmK : (const void*)&tmV,
+                                        &bars[L::bKVFull + stage], c * 64, t.kvh, t.k0 + n * BN);
+                        ++issued;
+                        if (++stage == (uint32_t)L::kStages) { stage = 0; phase ^= 1u; }
+                    }
+                }
+            }
+            if (!ok) {
+                // Let copies already in flight land before the CTA can exit.
+                uint32_t st = stage, ph = phase;
+                for (int i = 0; i < L::kStages && i < issued; ++i) {
+                    if (st == 0) { st = L::kStages; ph ^= 1u; }
+                    --st;
+                    int dummy = 0;
+                    mbar_wait(&bars[L::bKVFull + st], ph, &dummy, 20000000ull);
+                }
+                for (int s = 0; s < 2; ++s) {
+                    int dummy = 0;
+                    mbar_wait(&bars[L::bQFull + s], qphase[s] ^ 1u, &dummy, 20000000ull);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0);
+            constexpr uint32_t idO = idesc_bf16_f32(BM, D, 1);
+            uint32_t stage = 0, phase = 0;
+            uint32_t qf[2] = {0, 0}, pf[2] = {0, 0}, oe[2] = {0, 0};
+            const uint32_t q_base = smem_u32(smem + L::kQOff);
+            const uint32_t kv_base = smem_u32(smem + L::kKVOff);
+            bool ok = true, any = false;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                Tile t;
+                get_tile(p, prefix, w, t);
+                const int nmax = max(t.n[0], t.n[1]);
+                if (nmax == 0) continue;
+                for (int s = 0; s < 2 && ok; ++s) {
+                    if (t.n[s] == 0) continue;
+                    if (!mbar_wait(&bars[L::bQFull + s], qf[s], abort_flag, wd)) ok = false;
+                    qf[s] ^= 1u;
+                }
+                if (!ok) break;
+                any = true;
+                for (int n = 0; n <= nmax && ok; ++n) {
+                    const bool has_v = n >= 1, has_k = n < nmax;
+                    uint32_t v_slot = 0, k_slot = 0;
+                    if (has_v) {
+                        v_slot = stage;
+                        if (!mbar_wait(&bars[L::bKVFull + stage], phase, abort_flag, wd)) { ok = false; break; }
+                        if (++stage == (uint32_t)L::kStages) { stage = 0; phase ^= 1u; }
+                    }
+                    bool k_ready = false;
+                    if (has_k) k_slot = stage;
+                    const uint32_t k_par = phase;
+                    if (has_k) {
+                        if (++stage == (uint32_t)L::kStages) { stage = 0; phase ^= 1u; }
+                    }
+                    tc_fence_after();
+                    for (int s = 0; s < 2 && ok; ++s) {
+                        const uint32_t colS = s ? kColS1 : kColS0;
+                        const uint32_t colO = s ? kColO1 : kColO0;
+                        if (has_v && n - 1 < t.n[s]) {
+                            if (!mbar_wait(&bars[L::bPFull + s], pf[s], abort_flag, wd)) { ok = false; break; }
+                            pf[s] ^= 1u;
+                            if (n - 1 == 0) {
+                                if (!mbar_wait(&bars[L::bOEmpty + s], oe[s] ^ 1u, abort_flag, wd)) { ok = false; break; }
+                                oe[s] ^= 1u;
+                            }
+                            tc_fence_after();
+                            const uint32_t vb = kv_base + v_slot * L::kKVBytes;
+#pragma unroll
+                            for (int k = 0; k < BN / 16; ++k) {
+                                const uint64_t bdesc = smem_desc_sw128(vb + k * 2048, L::kChunkBytesKV, 1024);
+                                tc_mma_ts(tmem + colO, tmem + colS + k * 8, bdesc, idO, (n - 1 > 0 || k > 0) ? 1u : 0u);
+                            }
+                            if (n - 1 == t.n[s] - 1) tc_commit(&bars[L::bOFull + s]);
+                        }
+                        if (has_k && n < t.n[s]) {
+                            if (!k_ready) {
+                                if (!mbar_wait(&bars[L::bKVFull + k_slot], k_par, abort_flag, wd)) { ok = false; break; }
+                                tc_fence_after();
+                                k_ready = true;
+                            }
+                            const uint32_t qb = q_base + s * L::kQBytes;
+                            const uint32_t kb = kv_base + k_slot * L::kKVBytes;
+#pragma unroll
+                            for (int k = 0; k < D / 16; ++k) {
+                                const uint32_t off = (k >> 2) * L::kChunkBytesQ + (k & 3) * 32;
+                                const uint32_t offk = (k >> 2) * L::kChunkBytesKV + (k & 3) * 32;
+                                tc_mma_ss(tmem + colS, smem_desc_sw128(qb + off, 16, 1024),
+                                          smem_desc_sw128(kb + offk, 16, 1024), idS, k > 0 ? 1u : 0u);
+                            }
+                            tc_commit(&bars[L::bSFull + s]);
+                            if (n == t.n[s] - 1) tc_commit(&bars[L::bQEmpty + s]);
+                        }
+                    }
+                    if (!ok) break;
+                    if (has_v) tc_commit(&bars[L::bKVEmpty + v_slot]);
+                    if (has_k) {
+                        if (!k_ready) {  // a K tile no Q tile used (cannot happen for n < nmax, kept for safety)
+                            if (!mbar_wait(&bars[L::bKVFull + k_slot], k_par, abort_flag, wd)) { ok = false; break; }
+                        }
+                        tc_commit(&bars[L::bKVEmpty + k_slot]);
+                    }
+                }
+            }
+            if (any) {
+                // Wait until every issued MMA has completed before TMEM can be released.
+                tc_commit(&bars[L::bDrain]);
+                int dummy = 0;
+                mbar_wait(&bars[L::bDrain], 0, &dummy, 50000000ull);
+            }
+        }
+    }
+    } else if (warp < 12) {
+        // ------------------------------------------------------------------ softmax
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
+        const int s = (warp - 4) >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + (s ? kColS1 : kColS0);
+        const uint32_t tO = tmem + lane_off + (s ? kColO1 : kColO0);
+        const float sl2 = p.scale_log2;
+        uint32_t sf = 0, oe = 0;
+        unsigned long long c_dec = 0, c_res = 0;
+        bool ok = true;
+        for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            Tile t;
+            get_tile(p, prefix, w, t);
+            const int ns = t.n[s];
+            if (ns == 0) continue;
+            const int tile_row0 = t.r0 + s * BM;
+            const int qrow = tile_row0 + row;
+            const int off = t.Lk - t.Lq;
+            float m = -INFINITY, l = 0.0f;
+            for (int n = 0; n < ns; ++n) {
+                if (!mbar_wait(&bars[L::bSFull + s], sf, abort_flag, wd)) { ok = false; break; }
+                sf ^= 1u;
+                tc_fence_after();
+                uint32_t r[4][32];
+                tmem_ld32(tS + 0, r[0]);
+                tmem_ld32(tS + 32, r[1]);
+                tmem_ld32(tS + 64, r[2]);
+                tmem_ld32(tS + 96, r[3]);
+                tc_wait_ld();
+                reg_fence(r[0]);
+                reg_fence(r[1]);
+                reg_fence(r[2]);
+                reg_fence(r[3]);
+                float sv[BN];
+#pragma unroll
+                for (int c = 0; c < BN; ++c) sv[c] = __uint_as_float(r[c >> 5][c & 31]);
+                const int kb = n * BN;
+                const bool need_mask = (kb + BN > t.Lk) || (p.causal && kb + BN - 1 > tile_row0 + off);
+                if (need_mask) {
+                    const int lim = (p.causal ? min(t.Lk, qrow + off + 1) : t.Lk) - kb;
+#pragma unroll
+                    for (int c = 0; c < BN; ++c)
+                        if (c >= lim) sv[c] = -INFINITY;
+                }
+                float mx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = sv[i];
+#pragma unroll
+                for (int c = 8; c < BN; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
+                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                const float m_cand = fmaxf(m, mt);
+                const bool need = (m_cand - m) * sl2 > p.rescale_thr;  // NaN (both -inf) is false
+                const bool warp_need = __any_sync(0xffffffffu, need);
+                if (warp_need) {
+                    const float alpha = (m == -INFINITY) ? 0.0f : ex2_mufu((m - m_cand) * sl2);
+                    if (n > 0) {
+#pragma unroll 1
+                        for (int c = 0; c < D; c += 16) {
+                            uint32_t o[16];
+                            tmem_ld16(tO + c, o);
+                            tc_wait_ld();
+                            reg_fence(o);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            tmem_st16(tO + c, o);
+                        }
+                    }
+                    l *= alpha;
+                    m = m_cand;
+                    ++c_res;
+                }
+                ++c_dec;
+                const float neg = (m == -INFINITY) ? 0.0f : -m * sl2;
+                float sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                uint32_t pk[64];
+#pragma unroll
+                for (int c = 0; c < BN; c += 2) {
+                    const float x0 = fmaf(sv[c], sl2, neg);
+                    const float x1 = fmaf(sv[c + 1], sl2, neg);
+                    float p0, p1;
+                    if (POLY_EVERY > 0 && (c % (POLY_EVERY > 0 ? POLY_EVERY : 1)) == POLY_EVERY - 2) {
+                        p0 = ex2_mufu(x0);
+                        p1 = ex2_poly(x1);
+                    } else {
+                        p0 = ex2_mufu(x0);
+                        p1 = ex2_mufu(x1);
+                    }
+                    sum[(c >> 1) & 7] += p0 + p1;
+                    pk[c >> 1] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tS + 0, &pk[0]);
+                tmem_st32(tS + 32, &pk[32]);
+                l += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[L::bPFull + s]);
+            }
+            if (!ok) break;
+            // Publish (m, l) once the epilogue has drained the previous tile of this stage.
+            if (!mbar_wait(&bars[L::bOEmpty + s], oe ^ 1u, abort_flag, wd)) { ok = false; break; }
+            oe ^= 1u;
+            st_m[s * BM + row] = m;
+            st_l[s * BM + row] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[L::bStats + s]);
+        }
+        if (p.counters && lane == 0) {
+            atomicAdd(p.counters + 0, c_dec);
+            atomicAdd(p.counters + 1, c_res);
+            const unsigned long long ex = c_dec * 32ull * BN;
+            const unsigned long long poly = POLY_EVERY > 0 ? ex / POLY_EVERY : 0ull;
+            atomicAdd(p.counters + 2, poly);
+            atomicAdd(p.counters + 3, ex - poly);
+        }
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        uint32_t of[2] = {0, 0}, sp[2] = {0, 0};
+        bool ok = true;
+        for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            Tile t;
+            get_tile(p, prefix, w, t);
+            for (int s = 0; s < 2; ++s) {
+                const int qrow = t.r0 + s * BM + row;
+                if (t.r0 + s * BM >= t.Lq) continue;
+                const bool valid = qrow < t.Lq;
+                const long long tok = (long long)t.q0 + qrow;
+                __nv_bfloat16* orow = p.o + (tok * p.Hq + t.h) * D;
+                if (t.n[s] == 0) {
+                    if (valid) {
+                        uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                        for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+                        p.lse[tok * p.Hq + t.h] = -INFINITY;
+                    }
+                    continue;
+                }
+                if (!mbar_wait(&bars[L::bOFull + s], of[s], abort_flag, wd)) { ok = false; break; }
+                of[s] ^= 1u;
+                if (!mbar_wait(&bars[L::bStats + s], sp[s], abort_flag, wd)) { ok = false; break; }
+                sp[s] ^= 1u;
+                tc_fence_after();
+                const float m = st_m[s * BM + row];
+                const float l = st_l[s * BM + row];
+                const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+                const uint32_t tO = tmem + lane_off + (s ? kColO1 : kColO0);
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c, o);
+                    tc_wait_ld();
+                    reg_fence(o);
+                    if (valid) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+                        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[L::bOEmpty + s]);
+                if (valid) p.lse[tok * p.Hq + t.h] = l > 0.0f ? m * p.scale + logf(l) : -INFINITY;
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------------- teardown
+    __syncwarp();
+    tc_fence_before();
+    named_bar_sync(1, kThreads);
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (threadIdx.x == 0 && *abort_flag && p.status) {
+        atomicCAS(p.status, 0, kDevTimeout);
+        atomicAdd(p.status + 1, 1);
+    }
+}
+
+template <int D, int POLY>
+cudaError_t launch_t(const FwdTmaps& tm, const FwdParams& p, int grid, cudaStream_t stream) {
+    using L = Layout<D>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(attn_fwd_kernel<D, POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    attn_fwd_kernel<D, POLY><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.k, tm.v, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int fwd_max_varlen_batch() { return kMaxVarlenB; }
+
+cudaError_t launch_attn_fwd(const FwdTmaps& tm, const FwdParams& p, int d, int exp_poly, int grid,
+                            cudaStream_t stream) {
+    if (d == 128) {
+        return exp_poly ? launch_t<128, 8>(tm, p, grid, stream) : launch_t<128, 0>(tm, p, grid, stream);
+    }
+    return exp_poly ? launch_t<64, 8>(tm, p, grid, stream) : launch_t<64, 0>(tm, p, grid, stream);
+}
+
+// ------------------------------------------------------------------------------ diagnostics
+
+namespace {
+__global__ void exp2_probe_kernel(const float* x, float* y, long long n, int mode) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+        y[i] = mode == 0 ? ex2_poly(x[i]) : ex2_mufu(x[i]);
+}
+
+// Waits on an mbarrier that nothing ever arrives on, with the same bounded wait the
+// attention kernels use, and reports the timeout through the status word.
+__global__ void watchdog_probe_kernel(int* status, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait(&bar, 0, &abort_flag, limit_ns);
+    __syncthreads();
+    if (threadIdx.x == 0 && !ok) {
+        atomicCAS(status, 0, kDevTimeout);
+        atomicAdd(status + 1, 1);
+    }
+}
+}  // namespace
+
+cudaError_t launch_exp2_probe(const float* x, float* y, long long n, int mode, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    long long blocks = (n + 255) / 256;
+    if (blocks > 65535) blocks = 65535;
+    exp2_probe_kernel<<<(unsigned)blocks, 256, 0, stream>>>(x, y, n, mode);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_watchdog_probe(int* status, unsigned long long limit_ns, cudaStream_t stream) {
+    watchdog_probe_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,70 @@
+// Internal interface between the C-ABI layer (attn_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+// Device status word layout (int[4]): [0] first error code (0 = ok), [1] detail, [2..3] reserved.
+enum DeviceErr : int {
+    kDevOk = 0,
+    kDevTimeout = -6,   // matches ATTN_ERR_DEVICE_TIMEOUT
+    kDevBadIndex = -7,  // matches ATTN_ERR_DEVICE_BAD_INDEX
+};
+
+// Counters (unsigned long long[4]) when enabled: [0] softmax warp-tile decisions, [1] of which rescaled O,
+// [2] polynomial exponentials evaluated, [3] MUFU exponentials evaluated.
+constexpr int kNumCounters = 4;
+
+struct FwdParams {
+    __nv_bfloat16* o;
+    float* lse;
+    const int* cu_seqlens;  // device int32 [B+1] or nullptr for dense batches
+    int B, Hq, Hkv, G, Nq, Nk;
+    int causal;
+    float scale;        // softmax scale applied to q.k
+    float scale_log2;   // scale * log2(e)
+    float rescale_thr;  // rescale O only when the row max grows by more than this (base-2 exponent units)
+    int sec_q;          // query heads per scheduling section (multiple of G, divides Hq)
+    int total_tiles;    // dense: number of work tiles; varlen: ignored (computed on device)
+    int* status;
+    unsigned long long* counters;  // nullptr unless counting is enabled
+    unsigned long long watchdog_ns;
+};
+
+struct FwdTmaps {
+    CUtensorMap q, k, v;
+};
+
+// Launch the forward kernel for head dim d in {64, 128}; exp_poly selects the MUFU/polynomial split.
+cudaError_t launch_attn_fwd(const FwdTmaps& tm, const FwdParams& p, int d, int exp_poly, int grid,
+                            cudaStream_t stream);
+int fwd_max_varlen_batch();
+
+struct DecodeParams {
+    const __nv_bfloat16* q;        // [B, Hq, d]
+    const __nv_bfloat16* k_cache;  // [num_pages, page_size, Hkv, d]
+    const __nv_bfloat16* v_cache;
+    const int* page_table;         // [B, max_pages]
+    const int* seqlens;            // [B]
+    __nv_bfloat16* o;              // [B, Hq, d]
+    float* lse;                    // [B, Hq]
+    float* ws_o;                   // [B, Hq, max_splits, d] partial outputs
+    float* ws_lse;                 // [B, Hq, max_splits] partial LSE
+    int B, Hq, Hkv, G, page_size, max_pages, num_pages;
+    int chunk;       // tokens per split (multiple of 64)
+    int max_splits;  // splits per sequence the workspace holds
+    float scale, scale_log2, rescale_thr;
+    int* status;
+};
+
+cudaError_t launch_attn_decode(const DecodeParams& p, int d, cudaStream_t stream);
+
+// Diagnostics
+cudaError_t launch_exp2_probe(const float* x, float* y, long long n, int mode, cudaStream_t stream);
+cudaError_t launch_watchdog_probe(int* status, unsigned long long limit_ns, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,177 @@
+/*
+ * Exact softmax attention for one GB300 GPU (sm_103a): C ABI.
+ *
+ * Two operations:
+ *   attn_fwd           O = softmax(scale * Q K^T + mask) V and the per-row log-sum-exp,
+ *                      tiled with the online-softmax recurrence so that the score matrix
+ *                      never reaches device memory ("FlashAttention: not computing less,
+ *                      moving less", sections 01-03; "FlashAttention-4: Blackwell
+ *                      algorithm-pipeline co-design", all sections on the forward pass).
+ *   attn_decode_paged  one query token per sequence against a paged KV cache, split over
+ *                      the keys and merged by log-sum-exp ("Faster, more flexible FA4 for
+ *                      LLM inference", PR 1999/2104, PR 1940, PR 2186 sections).
+ *
+ * Conventions shared by every entry point
+ *  - All pointers named as device pointers must point to device memory of the current
+ *    CUDA device; the caller owns every buffer and keeps it alive until the work on
+ *    `stream` completes.
+ *  - `stream` is a cudaStream_t passed as void* (NULL selects the legacy default stream).
+ *    Every compute call is asynchronous on `stream` and never synchronises the host.
+ *  - bf16 tensors are IEEE bfloat16 bit patterns; the innermost dimension (d) is
+ *    contiguous. Results are identical to the exact definition up to floating-point
+ *    rounding: fp32 accumulation of bf16 products, bf16 probabilities and bf16 output.
+ *  - A call that returns an error code other than ATTN_ERR_CUDA has launched nothing and
+ *    written nothing. Errors found by the device while a kernel runs (a timed-out wait,
+ *    an out-of-range page index or sequence length) are recorded in a per-device status
+ *    word read by attn_get_device_status(); kernels never trap.
+ */
+#ifndef EXACT_SOFTMAX_ATTENTION_GB300_ATTN_H
+#define EXACT_SOFTMAX_ATTENTION_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int attn_status_t;
+
+#define ATTN_OK 0
+#define ATTN_ERR_NULL_PTR (-1)          /* a required pointer is NULL */
+#define ATTN_ERR_BAD_SHAPE (-2)         /* unsupported or inconsistent sizes */
+#define ATTN_ERR_ALIGN (-3)             /* a pointer is not aligned as documented */
+#define ATTN_ERR_UNSUPPORTED_ARCH (-4)  /* the current device is not sm_103 */
+#define ATTN_ERR_CUDA (-5)              /* a CUDA runtime or driver call failed */
+#define ATTN_ERR_DEVICE_TIMEOUT (-6)    /* a kernel gave up on a pipeline wait (device status) */
+#define ATTN_ERR_DEVICE_BAD_INDEX (-7)  /* a page index or sequence length was out of range (device status) */
+#define ATTN_ERR_BAD_ARG (-8)           /* an unknown option name or an invalid value */
+
+/*
+ * Forward attention ("FlashAttention: not computing less, moving less", section 01
+ * formula O = softmax(QK^T / sqrt(d)) V with a general scale; section 02 online-softmax
+ * recurrence; section 03 log-sum-exp statistics; causal masking as in "FlashAttention4
+ * 精读" section 3.3; grouped-query heads as in section 3.3, GQA paragraph; packed
+ * variable-length sequences as in "FlashAttention: not computing less, moving less",
+ * section 05, training paragraph).
+ *
+ * q   device, bf16 [T, Hq, d]    queries, T = B*Nq (dense) or Nq (packed)
+ * k   device, bf16 [Tk, Hkv, d]  keys,    Tk = B*Nk (dense) or Nk (packed)
+ * v   device, bf16 [Tk, Hkv, d]  values
+ * o   device, bf16 [T, Hq, d]    output (written)
+ * lse device, fp32 [T, Hq]       natural-log log-sum-exp of the scaled scores of each row,
+ *                                so softmax_ij = exp(scale * q_i.k_j - lse_i) (written)
+ * B         number of sequences (>= 0)
+ * Hq, Hkv   query and key/value heads; Hq % Hkv == 0, query head h reads kv head h/(Hq/Hkv)
+ * Nq, Nk    dense: query and key length of every sequence. Packed: the rows of q/o and of
+ *           k/v (the sequence lengths come from cu_seqlens and queries and keys share them;
+ *           a sequence reaching past Nq or Nk is treated as empty and recorded as
+ *           ATTN_ERR_DEVICE_BAD_INDEX)
+ * d         head dimension, 64 or 128
+ * scale     multiplier of q.k (typically 1/sqrt(d)); must be finite
+ * causal    0: every key is visible. 1: bottom-right aligned mask, key j visible to query
+ *           row i of its sequence iff j <= i + (Nk - Nq). Rows that see no key get o = 0
+ *           and lse = -inf.
+ * cu_seqlens NULL for dense batches, else device int32 [B+1] prefix offsets of packed
+ *           sequences (non-decreasing; B <= 1024).
+ * Alignment: q, k, v, o 16 bytes; lse 4 bytes.
+ * Returns ATTN_OK or an error code; see the conventions above.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                       int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens, void* stream);
+
+/*
+ * Paged-KV decode ("Faster, more flexible FA4 for LLM inference": PR 1999/2104 arbitrary
+ * page sizes gathered with cp.async, PR 1940 split-KV with a separate combine kernel,
+ * PR 2186 query heads of one kv head packed into one tile; "FlashAttention: not computing
+ * less, moving less", section 05, inference paragraph: decode over a paged KV cache).
+ * One query token per sequence; every cached key of the sequence is visible.
+ *
+ * q          device, bf16 [B, Hq, d]
+ * k_cache    device, bf16 [num_pages, page_size, Hkv, d]  physical pages of keys
+ * v_cache    device, bf16 [num_pages, page_size, Hkv, d]  physical pages of values
+ * page_table device, int32 [B, max_pages_per_seq]; token t of sequence b lives in physical
+ *            page page_table[b][t / page_size], slot t % page_size. Entries may repeat
+ *            (shared prefixes); entries past a sequence's last page are never read.
+ * seqlens    device, int32 [B], cached tokens per sequence, 0 <= seqlens[b] <=
+ *            max_pages_per_seq * page_size. A sequence of length 0 gets o = 0, lse = -inf.
+ * page_size  tokens per page, >= 1 (any value)
+ * o          device, bf16 [B, Hq, d] (written);  lse device, fp32 [B, Hq] (written)
+ * B, Hq, Hkv, d  as for attn_fwd; Hq / Hkv <= 16
+ * max_pages_per_seq  columns of page_table (>= 1)
+ * num_pages  physical pages in each cache (>= 1); a page index outside [0, num_pages) is
+ *            not read: its rows count as zeros and ATTN_ERR_DEVICE_BAD_INDEX is recorded
+ * scale      as for attn_fwd
+ * num_splits 0: choose the number of key splits from the SM count and the sizes;
+ *            n > 0: split every sequence's keys into at most n chunks.
+ * Workspace: partial outputs of the splits live in memory taken from a library-owned
+ * stream-ordered pool on `stream` and returned to it on `stream` after the combine.
+ * Alignment: q, o, k_cache, v_cache 16 bytes; lse, page_table, seqlens 4 bytes.
+ */
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* page_table,
+                                const int* seqlens, int page_size, void* o, float* lse, void* stream, int B, int Hq,
+                                int Hkv, int d, int max_pages_per_seq, int num_pages, float scale, int num_splits);
+
+/*
+ * Host-side split choice of attn_decode_paged (the num_splits = 0 heuristic of "Faster,
+ * more flexible FA4 for LLM inference", PR 1940 section; the pages give no formula).
+ * Writes the tokens per split (*chunk, a multiple of 64) and the splits the workspace
+ * holds per sequence (*max_splits) for the given sizes. num_sms <= 0 uses the current
+ * device's SM count. Pure host arithmetic; needs no GPU when num_sms > 0.
+ */
+attn_status_t attn_decode_plan(int B, int Hkv, int max_pages_per_seq, int page_size, int num_splits, int num_sms,
+                               int* chunk, int* max_splits);
+
+/* Static description of a status code. Never NULL. */
+const char* attn_status_string(attn_status_t status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status word.
+ * Returns ATTN_OK, the first device-side error recorded since the last call
+ * (ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_DEVICE_BAD_INDEX), or ATTN_ERR_CUDA.
+ */
+attn_status_t attn_get_device_status(void* stream);
+
+/*
+ * Process-wide tuning options (not needed for correct use):
+ *   "exp_poly"           0: every exponential on MUFU.EX2 (default); 1: one column in
+ *                        eight on the Cody-Waite cubic polynomial ("FlashAttention4 精读"
+ *                        section 3.1.3, partial emulation)
+ *   "rescale_threshold"  rescale O only when the row maximum grows by more than this many
+ *                        powers of two (default 8, i.e. a factor 256, "FlashAttention4 精读"
+ *                        section 3.1.4); 0 rescales on every increase
+ *   "decode_chunk"       tokens per decode split when num_splits = 0 (0 = heuristic)
+ *   "sec_heads"          query heads per forward scheduling section (0 = heuristic)
+ *   "count"              1: count softmax rescale decisions and exponentials (attn_read_counters)
+ *   "watchdog_ms"        device wait limit before a kernel gives up (default 4000)
+ * Returns ATTN_ERR_BAD_ARG for an unknown name or an invalid value.
+ */
+attn_status_t attn_set_option(const char* name, double value);
+attn_status_t attn_get_option(const char* name, double* value);
+
+/*
+ * Reads and clears the current device's counters (enabled by option "count"):
+ * out[0] softmax warp-tile steps, out[1] of which rescaled O, out[2] exponentials on the
+ * polynomial, out[3] exponentials on MUFU. n <= 4 values are written. Synchronises the device.
+ */
+attn_status_t attn_read_counters(unsigned long long* out, int n);
+
+/*
+ * Diagnostics. attn_debug_exp2 evaluates the device exponentials on n fp32 inputs:
+ * mode 0 the software 2^x of the hybrid exponential ("FlashAttention-4: Blackwell
+ * algorithm-pipeline co-design", section "hybrid exponential"), mode 1 MUFU ex2.approx.ftz.
+ * x, y device fp32 [n]. attn_debug_watchdog launches a kernel that waits on a barrier no
+ * thread ever arrives on, with the bounded wait of the attention kernels and the given
+ * limit, so that the next attn_get_device_status() reports ATTN_ERR_DEVICE_TIMEOUT.
+ */
+attn_status_t attn_debug_exp2(const float* x, float* y, long long n, int mode, void* stream);
+attn_status_t attn_debug_watchdog(unsigned long long limit_ns, void* stream);
+
+/* Library version string. */
+const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_SOFTMAX_ATTENTION_GB300_ATTN_H */

@@ -1,0 +1,37 @@
+"""Shared helpers of the GPU tests: device copies of generated inputs and the parity bar."""
+import importlib.util
+import os
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# Parity bar for the bf16-in / fp32-accumulate path (max over all compared elements)
+TOL_O = 1.5e-2
+TOL_LSE = 2e-3
+
+
+def ensure_built():
+    spec = importlib.util.spec_from_file_location("_attn_gb300_build",
+                                                  os.path.join(ROOT, "exact_softmax_attention_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()
+
+
+def to_dev(a, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def compare(o_gpu, lse_gpu, o_ref, lse_ref):
+    """(max|dO|, max|dLSE|) with -inf LSE required to match exactly."""
+    o = o_gpu.float().cpu().numpy().reshape(o_ref.shape)
+    lse = lse_gpu.float().cpu().numpy().reshape(lse_ref.shape)
+    ninf_ref = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lse), ninf_ref), "rows with no visible key differ"
+    assert np.isfinite(o).all(), "non-finite output"
+    do = float(np.abs(o - o_ref).max()) if o.size else 0.0
+    fin = ~ninf_ref
+    dl = float(np.abs(lse[fin] - lse_ref[fin]).max()) if fin.any() else 0.0
+    return do, dl

@@ -1,0 +1,104 @@
+"""The C-ABI library on the CPU: it loads, exports every declared symbol, and rejects bad
+arguments on the host before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from helpers import ROOT, ensure_built
+
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ctypes.CDLL(ensure_built())
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "attn_fwd" in names and "attn_decode_paged" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in attn.h but not exported"
+
+
+def test_python_binding_lists_the_header():
+    import exact_softmax_attention_gb300 as A
+    assert sorted(A.EXPORTS) == declared_functions()
+
+
+def _fwd(lib, q=16, k=16, v=16, o=16, lse=16, B=1, Hq=2, Hkv=2, Nq=8, Nk=8, d=64, scale=0.125, causal=0, cu=None):
+    f = lib.attn_fwd
+    vp = ctypes.c_void_p
+    f.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int, vp, vp]
+    return f(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu, None)
+
+
+def test_fwd_host_validation(lib):
+    import exact_softmax_attention_gb300 as A
+    assert _fwd(lib, q=None) == A.ATTN_ERR_NULL_PTR
+    assert _fwd(lib, lse=None) == A.ATTN_ERR_NULL_PTR
+    assert _fwd(lib, d=96) == A.ATTN_ERR_BAD_SHAPE
+    assert _fwd(lib, Hq=6, Hkv=4) == A.ATTN_ERR_BAD_SHAPE
+    assert _fwd(lib, Nq=-1) == A.ATTN_ERR_BAD_SHAPE
+    assert _fwd(lib, B=-1) == A.ATTN_ERR_BAD_SHAPE
+    assert _fwd(lib, causal=2) == A.ATTN_ERR_BAD_SHAPE
+    assert _fwd(lib, scale=float("nan")) == A.ATTN_ERR_BAD_SHAPE
+    assert _fwd(lib, q=0x1008) == A.ATTN_ERR_ALIGN
+    assert _fwd(lib, lse=0x1002) == A.ATTN_ERR_ALIGN
+    assert _fwd(lib, B=2000, cu=64) == A.ATTN_ERR_BAD_SHAPE
+    # nothing to do: returns before any CUDA call
+    assert _fwd(lib, B=0) == A.ATTN_OK
+    assert _fwd(lib, Nq=0) == A.ATTN_OK
+
+
+def _dec(lib, q=16, kc=16, vc=16, pt=16, sl=16, ps=16, o=16, lse=16, B=1, Hq=8, Hkv=2, d=128, mp=4, npg=4,
+         scale=0.1, ns=0):
+    f = lib.attn_decode_paged
+    vp = ctypes.c_void_p
+    f.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp] + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int]
+    return f(q, kc, vc, pt, sl, ps, o, lse, None, B, Hq, Hkv, d, mp, npg, scale, ns)
+
+
+def test_decode_host_validation(lib):
+    import exact_softmax_attention_gb300 as A
+    assert _dec(lib, pt=None) == A.ATTN_ERR_NULL_PTR
+    assert _dec(lib, Hq=36, Hkv=2) == A.ATTN_ERR_BAD_SHAPE   # 18 query heads per kv head
+    assert _dec(lib, ps=0) == A.ATTN_ERR_BAD_SHAPE
+    assert _dec(lib, npg=0) == A.ATTN_ERR_BAD_SHAPE
+    assert _dec(lib, ns=-1) == A.ATTN_ERR_BAD_SHAPE
+    assert _dec(lib, kc=0x1004) == A.ATTN_ERR_ALIGN
+    assert _dec(lib, sl=0x1002) == A.ATTN_ERR_ALIGN
+    assert _dec(lib, B=0) == A.ATTN_OK
+
+
+@pytest.mark.parametrize("B,Hkv,mp,ps,ns", [(64, 8, 2048, 16, 0), (1, 1, 1, 1, 0), (3, 2, 10, 7, 4),
+                                            (64, 8, 2048, 16, 5), (8, 1, 100, 1, 1)])
+def test_decode_plan(B, Hkv, mp, ps, ns):
+    import exact_softmax_attention_gb300 as A
+    chunk, splits = A.attn_decode_plan(B, Hkv, mp, ps, ns, num_sms=152)
+    lmax = mp * ps
+    assert chunk % 64 == 0 and chunk >= 64
+    assert splits * chunk >= lmax and (splits - 1) * chunk < lmax
+    if ns > 0:
+        assert splits <= ns
+
+
+def test_options_roundtrip():
+    import exact_softmax_attention_gb300 as A
+    A.attn_set_option("rescale_threshold", 4.0)
+    assert A.attn_get_option("rescale_threshold") == 4.0
+    A.attn_set_option("rescale_threshold", 8.0)
+    with pytest.raises(A.AttnError):
+        A.attn_set_option("no_such_option", 1)
+    with pytest.raises(A.AttnError):
+        A.attn_set_option("exp_poly", 3)
+    assert "sm_103a" in A.attn_version()
+    assert A.status_string(A.ATTN_ERR_DEVICE_TIMEOUT).startswith("a kernel gave up")

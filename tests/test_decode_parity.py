@@ -1,0 +1,110 @@
+"""attn_decode_paged on the GPU against the float64 CPU oracle (full comparison)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import TOL_LSE, TOL_O, compare, ensure_built, to_dev
+from synth import workloads as W
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def A():
+    ensure_built()
+    import exact_softmax_attention_gb300 as mod
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return mod
+
+
+def run_decode(A, c, q, kc, vc, pt, sl, num_splits=0):
+    o = torch.full((c.B, c.Hq, c.d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((c.B, c.Hq), float("nan"), dtype=torch.float32, device=DEV)
+    A.attn_decode_paged(to_dev(q, DEV), to_dev(kc, DEV), to_dev(vc, DEV), torch.from_numpy(pt).to(DEV),
+                        torch.from_numpy(sl).to(DEV), c.page_size, o, lse, None, c.B, c.Hq, c.Hkv, c.d, c.max_pages,
+                        c.num_pages, c.scale, num_splits)
+    return o, lse
+
+
+def check(A, c, num_splits=0, canary=False):
+    q, kc, vc, pt, sl = c.generate()
+    if canary:  # unreferenced pool pages hold NaN: they must never be read
+        used = np.zeros(c.num_pages, dtype=bool)
+        for b in range(c.B):
+            used[pt[b, : int(c.pages_per_seq[b])]] = True
+        kc[~used] = 0x7FC0
+        vc[~used] = 0x7FC0
+    o, lse = run_decode(A, c, q, kc, vc, pt, sl, num_splits)
+    st = A.attn_get_device_status()
+    assert st == 0, A.status_string(st)
+    ro, rl = oracle.attn_decode_paged(q, kc, vc, pt, sl, c.page_size, c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.scale)
+    do, dl = compare(o, lse, ro, rl)
+    assert do <= TOL_O and dl <= TOL_LSE, f"{c.name}: max|dO|={do:.3e} max|dLSE|={dl:.3e}"
+
+
+def dcase(name, B, Hq, Hkv, d, page_size, lo, hi, seed, extra=0, lens=None):
+    if lens is None:
+        lens = synth.uniform_ints(B, seed, lo, hi)
+    lens = np.asarray(lens, dtype=np.int32)
+    max_pages = int((max(int(lens.max()), 1) + page_size - 1) // page_size) + 2
+    return W.DecodeCase(name, len(lens), Hq, Hkv, d, page_size, lens, max_pages, 1.0 / math.sqrt(d), seed,
+                        extra_pages=extra)
+
+
+CASES = [
+    (dcase("p16_g4", 9, 32, 8, 128, 16, 1, 3000, 1), 0),
+    (dcase("p16_g4_split3", 5, 8, 2, 128, 16, 500, 2500, 2), 3),
+    (dcase("p1", 4, 8, 2, 128, 1, 1, 700, 3), 0),
+    (dcase("p7_d64", 6, 12, 3, 64, 7, 1, 1500, 4), 0),
+    (dcase("mqa_g16", 3, 16, 1, 128, 16, 100, 5000, 5), 0),
+    (dcase("g12", 3, 24, 2, 128, 32, 100, 2000, 6), 2),
+    (dcase("g1", 4, 4, 4, 64, 16, 1, 900, 7), 0),
+    (dcase("edge_lengths", 0, 8, 2, 128, 16, 0, 0, 8, lens=[0, 1, 15, 16, 17, 63, 64, 65, 1024, 1025]), 0),
+    (dcase("one_split", 4, 8, 2, 128, 16, 1, 4000, 9), 1),
+]
+
+
+@pytest.mark.parametrize("c,ns", CASES, ids=[c.name for c, _ in CASES])
+def test_decode_cases(A, c, ns):
+    check(A, c, ns)
+
+
+def test_nan_pages_never_read(A):
+    check(A, dcase("canary", 6, 8, 2, 128, 16, 1, 2000, 10, extra=12), canary=True)
+
+
+def test_split_count_does_not_change_result(A):
+    c = dcase("splits", 4, 8, 2, 128, 16, 3000, 6000, 11)
+    q, kc, vc, pt, sl = c.generate()
+    outs = []
+    for ns in (1, 2, 5, 0):
+        o, lse = run_decode(A, c, q, kc, vc, pt, sl, ns)
+        outs.append((o.float(), lse))
+    for o, lse in outs[1:]:
+        assert (o - outs[0][0]).abs().max().item() <= 2e-2
+        assert (lse - outs[0][1]).abs().max().item() <= 2e-3
+
+
+def test_decode_workload_full(A):
+    check(A, W.decode())
+
+
+def test_bad_page_index_is_reported(A):
+    c = dcase("badpage", 2, 8, 2, 128, 16, 40, 60, 12)
+    q, kc, vc, pt, sl = c.generate()
+    pt = pt.copy()
+    pt[1, 1] = c.num_pages + 5  # out of range: must be skipped and reported, not read
+    o, lse = run_decode(A, c, q, kc, vc, pt, sl)
+    assert A.attn_get_device_status() == A.ATTN_ERR_DEVICE_BAD_INDEX
+    assert A.attn_get_device_status() == 0  # cleared by the read
+    # sequence 0 is unaffected
+    ro, rl = oracle.attn_decode_paged(q, kc, vc, pt * (pt < c.num_pages), sl, c.page_size, c.B, c.Hq, c.Hkv, c.d,
+                                      c.max_pages, c.scale)
+    do, dl = compare(o[:1], lse[:1], ro[:1], rl[:1])
+    assert do <= TOL_O and dl <= TOL_LSE
