@@ -1,0 +1,426 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention hot path on GB300.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+  * attn_fwd on the long-context causal prefill workload (B=1, H=32, N=8192,
+    d=128, bf16, Q scaled by 2, causal), and
+  * attn_decode_paged on the paged decode workload (B=64, Hq=32, Hkv=8, d=128,
+    lengths U[1024, 32768], page_size=16, split-KV with LSE combine).
+``value`` is the forward leg's throughput in TFLOP/s (algorithmic FLOPs: 4*d per
+visible (query, key) pair and head); the decode leg's HBM GB/s is reported under
+``decode``. Both legs are timed with CUDA events on the stream they launch on;
+inputs are larger than L2, so no flush is needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+With --gpus N > 1 the script runs under torch.distributed.run, one rank per GPU,
+each rank processing its own copy of the workload (weak scaling, no data-path
+collective). ``--impl reference`` times the float64 CPU oracle on a bounded
+sample of the same workload on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import workloads as W  # noqa: E402
+
+METRIC = "attn fwd TFLOP/s (bf16 hd128 causal) & paged-decode HBM GB/s vs roofline"
+FWD_KERNEL = "attn_fwd_kernel"
+DEC_KERNEL = "decode_split_kernel"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU-baseline leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_softmax_attention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """Per-launch DRAM bytes of ``kernel`` from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            t = json.load(f)
+        e = t[kernel]
+        return float(e["dram_bytes_per_launch"]) if e.get("source_sha") == source_sha() else None
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle (CPU) legs
+
+def oracle_fwd_sample(case, q, k, v, n_rows, seed, n_threads):
+    import oracle
+    T = case.total_q
+    rng = np.random.default_rng(seed)
+    rows = rng.choice(T * case.Hq, size=n_rows, replace=False).astype(np.int64)
+    tok = rows // case.Hq
+    pairs = int(np.minimum(tok + 1, case.Nk).sum())  # causal, Nq == Nk
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, case.B, case.Hq, case.Hkv, case.Nq, case.Nk, case.d, case.scale, case.causal,
+                    rows=rows, n_threads=n_threads)
+    dt = time.perf_counter() - t0
+    return 4 * case.d * pairs, dt
+
+
+def oracle_decode_sample(case, inputs, n_seq, n_threads):
+    import oracle
+    q, kc, vc, pt, sl = inputs
+    sel = np.arange(n_seq)
+    t0 = time.perf_counter()
+    oracle.attn_decode_paged(q[sel], kc, vc, pt[sel], sl[sel], case.page_size, n_seq, case.Hq, case.Hkv, case.d,
+                             case.max_pages, case.scale, n_threads=n_threads)
+    dt = time.perf_counter() - t0
+    L = sl[sel].astype(np.int64)
+    nbytes = int(L.sum()) * case.Hkv * case.d * 4 + 2 * n_seq * case.Hq * case.d * 2 + n_seq * case.Hq * 4
+    return nbytes, dt
+
+
+def cpu_baseline(fwd_case, fwd_inputs, dec_case, dec_inputs, budget_s=12.0):
+    """The oracle as it stands, on a bounded sample sized for ~budget_s of CPU time."""
+    threads = os.cpu_count() or 1
+    # calibrate on a small sample, then size the measured one
+    f0, t0 = oracle_fwd_sample(fwd_case, *fwd_inputs, 64, 7, threads)
+    rate = f0 / max(t0, 1e-6)
+    rows = int(min(fwd_case.total_q * fwd_case.Hq, max(64, 64 * (budget_s * 0.7) / max(t0, 1e-6))))
+    f, t = oracle_fwd_sample(fwd_case, *fwd_inputs, rows, 8, threads)
+    d_seq = 2
+    b, td = oracle_decode_sample(dec_case, dec_inputs, d_seq, threads)
+    return {
+        "value": f / t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+        "sample": f"{rows} random (token, head) rows of the long causal prefill ({f / 1e9:.1f} GFLOP, {t:.1f} s); "
+                  f"decode: {d_seq} sequences ({b / 1e9:.2f} GB, {td:.1f} s)",
+        "decode_gbs": b / td / 1e9,
+        "calibration_gflops": rate / 1e9,
+    }
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if world > 1 and rank != 0:
+        return
+    fc, dc = W.long_causal(), W.decode()
+    fin = fc.generate()
+    din = dc.generate()
+    threads = os.cpu_count() or 1
+    # each step: ~4 s of oracle work on a row sample of the prefill and one decode sequence
+    f0, t0 = oracle_fwd_sample(fc, *fin, 64, 1, threads)
+    rows = int(max(64, 64 * 3.0 / max(t0, 1e-6)))
+    for i in range(args.warmup):
+        oracle_fwd_sample(fc, *fin, rows, 100 + i, threads)
+    tot_f = tot_t = tot_b = tot_td = 0.0
+    for i in range(args.steps):
+        f, t = oracle_fwd_sample(fc, *fin, rows, 200 + i, threads)
+        b, td = oracle_decode_sample(dc, din, 1, threads)
+        tot_f += f
+        tot_t += t
+        tot_b += b
+        tot_td += td
+    value = tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": (tot_t + tot_td) / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "long_causal_prefill+paged_decode", "sample": f"{rows} rows/step, 1 decode seq/step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} random (token, head) rows of the long causal prefill and one decode "
+                                   f"sequence per step"},
+        "decode": {"value": tot_b / tot_td / 1e9, "unit": "GB/s"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU leg
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import exact_softmax_attention_gb300 as A
+
+    fc, dc = W.long_causal(), W.decode()
+    q, k, v = fc.generate()
+    dq, kc, vc, pt, sl = dc.generate()
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        Q, K, V = to_dev(q), to_dev(k), to_dev(v)
+        O = torch.empty((fc.total_q, fc.Hq, fc.d), dtype=torch.bfloat16, device=dev)
+        LSE = torch.empty((fc.total_q, fc.Hq), dtype=torch.float32, device=dev)
+        DQ, KC, VC = to_dev(dq), to_dev(kc), to_dev(vc)
+        PT, SL = torch.from_numpy(pt).to(dev), torch.from_numpy(sl).to(dev)
+        DO = torch.empty((dc.B, dc.Hq, dc.d), dtype=torch.bfloat16, device=dev)
+        DLSE = torch.empty((dc.B, dc.Hq), dtype=torch.float32, device=dev)
+    stream.synchronize()
+    s_handle = stream.cuda_stream
+
+    def fwd():
+        A.attn_fwd(Q, K, V, O, LSE, fc.B, fc.Hq, fc.Hkv, fc.Nq, fc.Nk, fc.d, fc.scale, fc.causal, None, s_handle)
+
+    def dec():
+        A.attn_decode_paged(DQ, KC, VC, PT, SL, dc.page_size, DO, DLSE, s_handle, dc.B, dc.Hq, dc.Hkv, dc.d,
+                            dc.max_pages, dc.num_pages, dc.scale, 0)
+
+    _, max_splits = A.attn_decode_plan(dc.B, dc.Hkv, dc.max_pages, dc.page_size, 0)
+    launches_per_step = 1 + (2 if max_splits > 1 else 1)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        fwd()
+        dec()
+    st = A.attn_get_device_status(s_handle)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {A.status_string(st)}")
+
+    K_ = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_)]
+    barrier()
+    gpu_index = torch.cuda.current_device()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_index = int(vis.split(",")[gpu_index])
+        except (ValueError, IndexError):
+            pass
+    with ClockSampler(gpu_index) as clk:
+        t_wall0 = time.perf_counter()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(K_):
+            ev[i][0].record(stream)
+            fwd()
+            ev[i][1].record(stream)
+            dec()
+            ev[i][2].record(stream)
+        end.record(stream)
+        barrier()
+        t_wall = time.perf_counter() - t_wall0
+    st = A.attn_get_device_status(s_handle)
+    if st != 0:
+        raise RuntimeError(f"device status after timed region: {A.status_string(st)}")
+    total_ms = start.elapsed_time(end)
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    total_ms = max_over_ranks(total_ms)
+    fwd_ms = max_over_ranks(fwd_ms)
+    dec_ms = max_over_ranks(dec_ms)
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (torch.from_numpy(a.view(np.int16)).pin_memory() for a in (q, k, v))
+        hdq, hkc, hvc = (torch.from_numpy(a.view(np.int16)).pin_memory() for a in (dq, kc, vc))
+        hpt, hsl = torch.from_numpy(pt).pin_memory(), torch.from_numpy(sl).pin_memory()
+        ho = torch.empty(O.shape, dtype=torch.bfloat16).pin_memory()
+        hlse = torch.empty(LSE.shape, dtype=torch.float32).pin_memory()
+        hdo = torch.empty(DO.shape, dtype=torch.bfloat16).pin_memory()
+        hdlse = torch.empty(DLSE.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdq, hkc, hvc, hpt, hsl))
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdo, hdlse))
+        n_e2e = max(1, min(K_, 5))
+        with torch.cuda.stream(stream):
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_e2e)]
+            barrier()
+            for i in range(n_e2e):
+                evs[i][0].record(stream)
+                Q.view(torch.int16).copy_(hq, non_blocking=True)
+                K.view(torch.int16).copy_(hk, non_blocking=True)
+                V.view(torch.int16).copy_(hv, non_blocking=True)
+                fwd()
+                ho.copy_(O, non_blocking=True)
+                hlse.copy_(LSE, non_blocking=True)
+                evs[i][1].record(stream)
+                DQ.view(torch.int16).copy_(hdq, non_blocking=True)
+                KC.view(torch.int16).copy_(hkc, non_blocking=True)
+                VC.view(torch.int16).copy_(hvc, non_blocking=True)
+                PT.copy_(hpt, non_blocking=True)
+                SL.copy_(hsl, non_blocking=True)
+                dec()
+                hdo.copy_(DO, non_blocking=True)
+                hdlse.copy_(DLSE, non_blocking=True)
+                evs[i][2].record(stream)
+            barrier()
+        e_f = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs))
+        e_d = max_over_ranks(sum(e[1].elapsed_time(e[2]) for e in evs))
+        e2e = {"value": world * n_e2e * fc.flops() / (e_f * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "decode": {"value": world * n_e2e * dc.bytes() / (e_d * 1e-3) / 1e9, "unit": "GB/s"}}
+        if not np.isfinite(ho.float().numpy()).all():
+            raise RuntimeError("non-finite output in the end-to-end leg")
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    hbm, bf16, src = peaks()
+    fwd_avg_s = fwd_ms / K_ * 1e-3
+    dec_avg_s = dec_ms / K_ * 1e-3
+    f_ach = fc.flops() / fwd_avg_s / 1e12
+    d_ach = dc.bytes() / dec_avg_s / 1e9
+    value = world * K_ * fc.flops() / (fwd_ms * 1e-3) / 1e12
+    dvalue = world * K_ * dc.bytes() / (dec_ms * 1e-3) / 1e9
+    tr_f = ncu_traffic(FWD_KERNEL)
+    tr_d = ncu_traffic(DEC_KERNEL)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K_, "warmup": args.warmup,
+        "ms_per_step": total_ms / K_, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "long_causal_prefill(B1,H32,N8192,d128,causal,Qx2)+paged_decode(B64,Hq32,Hkv8,d128,"
+                               "L~U[1024,32768],page16)",
+                   "prefill_flops_per_step": fc.flops(), "decode_bytes_per_step": dc.bytes(),
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
+                   "decode_splits_max": max_splits},
+        "roofline": {"bound": "tensor", "achieved": f_ach, "peak": bf16, "unit": "TFLOP/s", "frac": f_ach / bf16,
+                     "traffic": tr_f, "kernel": FWD_KERNEL, "peak_source": f"{src} bf16 burst"},
+        "decode": {"value": dvalue, "unit": "GB/s", "ms_per_step": dec_ms / K_,
+                   "roofline": {"bound": "hbm", "achieved": d_ach, "peak": hbm, "unit": "GB/s", "frac": d_ach / hbm,
+                                "traffic": tr_d, "kernel": DEC_KERNEL, "peak_source": f"{src} copy"}},
+        "prefill_ms_per_step": fwd_ms / K_,
+        "gpu_launches": K_ * launches_per_step,
+        "clocks": clk.summary(),
+        "wall_s_timed": t_wall,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(fc, (q, k, v), dc, (dq, kc, vc, pt, sl))
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

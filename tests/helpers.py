@@ -11,6 +11,14 @@ TOL_O = 1.5e-2
 TOL_LSE = 2e-3
 
 
+def tol_o_stress(o_ref):
+    """Bar for stress inputs outside the stated workloads (very sharp softmax, |O| up to ~5):
+    the stated 1.5e-2 plus one bf16 unit in the last place of |O| (2^-7 |O|), since rounding
+    O to bf16 alone costs up to half of that and bf16 probabilities (relative error 2^-9 each)
+    can add as much again when a few keys dominate."""
+    return TOL_O + float(np.abs(o_ref).max()) * 2.0**-7
+
+
 def ensure_built():
     spec = importlib.util.spec_from_file_location("_attn_gb300_build",
                                                   os.path.join(ROOT, "exact_softmax_attention_gb300", "build.py"))

@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import TOL_LSE, TOL_O, compare, ensure_built, to_dev
+from helpers import TOL_LSE, TOL_O, compare, ensure_built, to_dev, tol_o_stress
 from synth import workloads as W
 
 torch = pytest.importorskip("torch")
@@ -43,13 +43,14 @@ def run_fwd(A, case, q, k, v):
     return o, lse
 
 
-def check_full(A, case):
+def check_full(A, case, stress=False):
     q, k, v = case.generate()
     o, lse = run_fwd(A, case, q, k, v)
     ro, rl = oracle.attn_fwd(q, k, v, case.B, case.Hq, case.Hkv, case.Nq, case.Nk, case.d, case.scale, case.causal,
                              cu_seqlens=case.cu_seqlens)
     do, dl = compare(o, lse, ro, rl)
-    assert do <= TOL_O and dl <= TOL_LSE, f"{case.name}: max|dO|={do:.3e} max|dLSE|={dl:.3e}"
+    tol = tol_o_stress(ro) if stress else TOL_O
+    assert do <= tol and dl <= TOL_LSE, f"{case.name}: max|dO|={do:.3e} (bar {tol:.3e}) max|dLSE|={dl:.3e}"
     return do, dl
 
 
@@ -83,7 +84,7 @@ SMALL = [
 
 @pytest.mark.parametrize("c", SMALL, ids=[c.name for c in SMALL])
 def test_small_cases(A, c):
-    check_full(A, c)
+    check_full(A, c, stress=c.q_mult > 2.0)
 
 
 def test_tiny_workload(A):
@@ -141,7 +142,7 @@ def test_rescale_threshold_is_exact(A, thr):
     """The threshold only changes when O is rescaled, never the result (beyond rounding)."""
     A.attn_set_option("rescale_threshold", thr)
     try:
-        check_full(A, case(f"thr{thr}", 1, 4, 4, 1024, 1024, 128, True, 17, 3.0))
+        check_full(A, case(f"thr{thr}", 1, 4, 4, 1024, 1024, 128, True, 17, 3.0), stress=True)
     finally:
         A.attn_set_option("rescale_threshold", 8.0)
 
