@@ -8,8 +8,8 @@
 // One persistent CTA per SM walks a list of work tiles (sequence, query head,
 // 256-row query block = two 128-row Q tiles). Warp roles (16 warps):
 //   warp 0       TMA producer: Q tiles once per work tile, then a ring of K/V tiles
-//   warp 1       MMA issuer (one thread): S = Q K^T and O += P V with tcgen05.mma,
-//                accumulators in tensor memory; owns the TMEM allocation
+//   warp 1       MMA issuer: S = Q K^T and O += P V with tcgen05.mma, accumulators in
+//                tensor memory; owns the TMEM allocation
 //   warps 4-7    softmax for Q tile 0, warps 8-11 softmax for Q tile 1: one thread per
 //                row reads S from TMEM, masks, takes the row max, decides whether to
 //                rescale O (warp-uniform, only when the max grew by more than the
@@ -26,7 +26,7 @@
 //
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); P_s (bf16,
 // 64 columns) overlays the first half of S_s. Because S_s(n) is issued after
-// PV_s(n-1) from the same thread, the S_s(n) completion barrier also covers
+// PV_s(n-1) by the same thread, the S_s(n) completion barrier also covers
 // PV_s(n-1), so the softmax warps may rescale O_s right after reading S_s(n).
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -47,16 +47,19 @@ template <int D>
 struct Layout {
     static constexpr int kQBytes = BM * D * 2;
     static constexpr int kKVBytes = BN * D * 2;
-    static constexpr int kStages = (D == 128) ? 4 : 6;
+    // Ring entry n holds what burst n reads: K tile n (for S = Q K_n^T) and V tile n-1
+    // (for O += P_{n-1} V_{n-1}).
+    static constexpr int kEntryBytes = 2 * kKVBytes;
+    static constexpr int kEntries = (D == 128) ? 2 : 4;
     static constexpr int kChunks = D / 64;                // 128-byte swizzle chunks along d
     static constexpr int kChunkBytesQ = BM * 128;         // one [128 rows x 64 d] chunk
     static constexpr int kChunkBytesKV = BN * 128;
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = 2 * kQBytes;
-    static constexpr int kBarOff = kKVOff + kStages * kKVBytes;
+    static constexpr int kBarOff = kKVOff + kEntries * kEntryBytes;
     // barrier indices
-    static constexpr int bQFull = 0, bQEmpty = 2, bKVFull = 4, bKVEmpty = 4 + kStages;
-    static constexpr int bSFull = 4 + 2 * kStages, bPFull = bSFull + 2, bOFull = bSFull + 4, bOEmpty = bSFull + 6;
+    static constexpr int bQFull = 0, bQEmpty = 2, bEFull = 4, bEEmpty = 4 + kEntries;
+    static constexpr int bSFull = 4 + 2 * kEntries, bPFull = bSFull + 2, bOFull = bSFull + 4, bOEmpty = bSFull + 6;
     static constexpr int bStats = bSFull + 8, bDrain = bSFull + 10;
     static constexpr int kNumBars = bDrain + 1;
     static constexpr int kStatsOff = kBarOff + ((kNumBars * 8 + 15) / 16) * 16;
@@ -75,6 +78,31 @@ struct Tile {
 };
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Wait of a converged warp: every lane polls the same phase (measured faster than one lane
+// polling and broadcasting), and the result is made warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
+    const bool ok = mbar_wait(bar, parity, abort, limit_ns);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Optional event timeline of CTA 0 for pipeline tuning (compile with -DATTN_TIMELINE).
+#ifdef ATTN_TIMELINE
+__device__ long long g_timeline[5][4096][4];
+__device__ int g_timeline_n[5];
+#define ATTN_TL_DECL(x) x
+#define ATTN_TL(role, a, b, c, d)                                                         \
+    do {                                                                                  \
+        if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && tl_idx < 4096) {                \
+            g_timeline[role][tl_idx][0] = (a); g_timeline[role][tl_idx][1] = (b);        \
+            g_timeline[role][tl_idx][2] = (c); g_timeline[role][tl_idx][3] = (d);        \
+            g_timeline_n[role] = ++tl_idx;                                                \
+        }                                                                                 \
+    } while (0)
+#else
+#define ATTN_TL_DECL(x)
+#define ATTN_TL(role, a, b, c, d) ((void)0)
+#endif
 
 // Packed sequence b: first token and length. Offsets outside [0, Nq] (total packed
 // query rows) or [0, Nk] (total key rows), or decreasing, make the sequence empty; the
@@ -178,15 +206,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    ATTN_TL_DECL(int tl_idx = 0);
 
     if (threadIdx.x == 0) {
         mbar_init(&bars[L::bQFull + 0], 1);
         mbar_init(&bars[L::bQFull + 1], 1);
         mbar_init(&bars[L::bQEmpty + 0], 1);
         mbar_init(&bars[L::bQEmpty + 1], 1);
-        for (int i = 0; i < L::kStages; ++i) {
-            mbar_init(&bars[L::bKVFull + i], 1);
-            mbar_init(&bars[L::bKVEmpty + i], 1);
+        for (int i = 0; i < L::kEntries; ++i) {
+            mbar_init(&bars[L::bEFull + i], 1);
+            mbar_init(&bars[L::bEEmpty + i], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[L::bSFull + s], 1);
@@ -240,156 +269,166 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const uint64_t wd = p.watchdog_ns;
 
-    // Register split per warpgroup: producer/MMA 56, softmax 184 each, epilogue 80
+    // Register split per warpgroup: producer/MMA 80, softmax 176 each, epilogue 72
     // (sum 504 <= 4 x 128, the registers the CTA is launched with).
     if (warp < 4) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0, qphase[2] = {0, 0};
-            int issued = 0;
-            bool ok = true;
-            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-                Tile t;
-                get_tile(p, prefix, w, t);
-                const int nmax = max(t.n[0], t.n[1]);
-                for (int s = 0; s < 2 && ok; ++s) {
-                    if (t.n[s] == 0) continue;
-                    if (!mbar_wait(&bars[L::bQEmpty + s], qphase[s] ^ 1u, abort_flag, wd)) { ok = false; break; }
-                    qphase[s] ^= 1u;
-                    uint8_t* dst = smem + L::kQOff + s * L::kQBytes;
-                    mbar_arrive_expect_tx(&bars[L::bQFull + s], L::kQBytes);
+        // The whole warp walks the schedule so that addresses and coordinates stay
+        // warp-uniform; lane 0 issues the copies.
+        const uint32_t leader = lane == 0;
+        uint32_t stage = 0, phase = 0, qphase[2] = {0, 0};
+        int issued = 0;
+        bool ok = true;
+        for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            Tile t;
+            get_tile(p, prefix, w, t);
+            const int nmax = max(t.n[0], t.n[1]);
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                if (!ok || t.n[s] == 0) continue;
+                ATTN_TL_DECL(long long tq = clock64());
+                if (!(ok = warp_wait(&bars[L::bQEmpty + s], qphase[s] ^ 1u, abort_flag, wd))) continue;
+                qphase[s] ^= 1u;
+                uint8_t* dst = smem + L::kQOff + s * L::kQBytes;
+                mbar_arrive_expect_tx_by(leader, &bars[L::bQFull + s], L::kQBytes);
+#pragma unroll
+                for (int c = 0; c < L::kChunks; ++c)
+                    tma_load_3d_by(leader, dst + c * L::kChunkBytesQ, &tmQ, &bars[L::bQFull + s], c * 64, t.h,
+                                   t.q0 + t.r0 + s * BM);
+                ATTN_TL(0, 10 + s, w, tq, clock64());
+            }
+            for (int e = 0; e <= nmax && ok; ++e) {
+                ATTN_TL_DECL(long long tw = clock64());
+                if (!(ok = warp_wait(&bars[L::bEEmpty + stage], phase ^ 1u, abort_flag, wd))) break;
+                uint8_t* ent = smem + L::kKVOff + stage * L::kEntryBytes;
+                const uint32_t bytes = (e < nmax ? (uint32_t)L::kKVBytes : 0u) + (e >= 1 ? (uint32_t)L::kKVBytes : 0u);
+                mbar_arrive_expect_tx_by(leader, &bars[L::bEFull + stage], bytes);
+                if (e < nmax) {
 #pragma unroll
                     for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d(dst + c * L::kChunkBytesQ, &tmQ, &bars[L::bQFull + s], c * 64, t.h,
-                                    t.q0 + t.r0 + s * BM);
+                        tma_load_3d_by(leader, ent + c * L::kChunkBytesKV, &tmK, &bars[L::bEFull + stage], c * 64, t.kvh,
+                                       t.k0 + e * BN);
                 }
-                for (int n = 0; n < nmax && ok; ++n) {
-                    for (int kv = 0; kv < 2; ++kv) {
-                        if (!mbar_wait(&bars[L::bKVEmpty + stage], phase ^ 1u, abort_flag, wd)) { ok = false; break; }
-                        uint8_t* dst = smem + L::kKVOff + stage * L::kKVBytes;
-                        mbar_arrive_expect_tx(&bars[L::bKVFull + stage], L::kKVBytes);
+                if (e >= 1) {
 #pragma unroll
-                        for (int c = 0; c < L::kChunks; ++c)
-                            tma_load_3d(dst + c * L::kChunkBytesKV, kv == 0 ? (const void*)&tmK : (const void*)&tmV,
-                                        &bars[L::bKVFull + stage], c * 64, t.kvh, t.k0 + n * BN);
-                        ++issued;
-                        if (++stage == (uint32_t)L::kStages) { stage = 0; phase ^= 1u; }
-                    }
+                    for (int c = 0; c < L::kChunks; ++c)
+                        tma_load_3d_by(leader, ent + L::kKVBytes + c * L::kChunkBytesKV, &tmV, &bars[L::bEFull + stage],
+                                       c * 64, t.kvh, t.k0 + (e - 1) * BN);
                 }
+                ATTN_TL(0, 0, e, tw, clock64());
+                ++issued;
+                if (++stage == (uint32_t)L::kEntries) { stage = 0; phase ^= 1u; }
             }
-            if (!ok) {
-                // Let copies already in flight land before the CTA can exit.
-                uint32_t st = stage, ph = phase;
-                for (int i = 0; i < L::kStages && i < issued; ++i) {
-                    if (st == 0) { st = L::kStages; ph ^= 1u; }
-                    --st;
-                    int dummy = 0;
-                    mbar_wait(&bars[L::bKVFull + st], ph, &dummy, 20000000ull);
-                }
-                for (int s = 0; s < 2; ++s) {
-                    int dummy = 0;
-                    mbar_wait(&bars[L::bQFull + s], qphase[s] ^ 1u, &dummy, 20000000ull);
-                }
+        }
+        if (!ok) {
+            // Let copies already in flight land before the CTA can exit.
+            uint32_t st = stage, ph = phase;
+            for (int i = 0; i < L::kEntries && i < issued; ++i) {
+                if (st == 0) { st = L::kEntries; ph ^= 1u; }
+                --st;
+                int dummy = 0;
+                mbar_wait(&bars[L::bEFull + st], ph, &dummy, 20000000ull);
+            }
+            for (int s = 0; s < 2; ++s) {
+                int dummy = 0;
+                mbar_wait(&bars[L::bQFull + s], qphase[s] ^ 1u, &dummy, 20000000ull);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0);
-            constexpr uint32_t idO = idesc_bf16_f32(BM, D, 1);
-            uint32_t stage = 0, phase = 0;
-            uint32_t qf[2] = {0, 0}, pf[2] = {0, 0}, oe[2] = {0, 0};
-            const uint32_t q_base = smem_u32(smem + L::kQOff);
-            const uint32_t kv_base = smem_u32(smem + L::kKVOff);
-            bool ok = true, any = false;
-            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-                Tile t;
-                get_tile(p, prefix, w, t);
-                const int nmax = max(t.n[0], t.n[1]);
-                if (nmax == 0) continue;
-                for (int s = 0; s < 2 && ok; ++s) {
-                    if (t.n[s] == 0) continue;
-                    if (!mbar_wait(&bars[L::bQFull + s], qf[s], abort_flag, wd)) ok = false;
-                    qf[s] ^= 1u;
-                }
-                if (!ok) break;
-                any = true;
-                for (int n = 0; n <= nmax && ok; ++n) {
-                    const bool has_v = n >= 1, has_k = n < nmax;
-                    uint32_t v_slot = 0, k_slot = 0;
-                    if (has_v) {
-                        v_slot = stage;
-                        if (!mbar_wait(&bars[L::bKVFull + stage], phase, abort_flag, wd)) { ok = false; break; }
-                        if (++stage == (uint32_t)L::kStages) { stage = 0; phase ^= 1u; }
+        // The whole warp walks the schedule (descriptors and slots stay warp-uniform); lane 0
+        // issues every tcgen05 instruction. Per KV step n the tensor pipe receives
+        //   burst 0: PV0(n-1), S0(n)     burst 1: PV1(n-1), S1(n)
+        // so it computes one tile's products while the other tile's softmax works; S_s(n) is
+        // issued after PV_s(n-1) by the same thread, so its completion covers PV_s(n-1).
+        // Completion signals go out back to back after each burst: a commit briefly drains
+        // the tensor pipe, and consecutive commits share that drain.
+        const uint32_t leader = lane == 0;
+        constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0);
+        constexpr uint32_t idO = idesc_bf16_f32(BM, D, 1);
+        uint32_t stage = 0, phase = 0;
+        uint32_t ph = 0;  // phase bits: 0-1 Q full, 2-3 P full, 4-5 O empty (per Q tile)
+        const uint32_t q_base = smem_u32(smem + L::kQOff);
+        const uint32_t kv_base = smem_u32(smem + L::kKVOff);
+        const uint64_t dq0 = smem_desc_sw128(q_base, 16, 1024), dq1 = smem_desc_sw128(q_base + L::kQBytes, 16, 1024);
+        const uint64_t dk0 = smem_desc_sw128(kv_base, 16, 1024);
+        const uint64_t dv0 = smem_desc_sw128(kv_base, L::kChunkBytesKV, 1024);
+        bool ok = true, any = false;
+        for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            Tile t;
+            get_tile(p, prefix, w, t);
+            const int nmax = max(t.n[0], t.n[1]);
+            if (nmax == 0) continue;
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                if (!ok || t.n[s] == 0) continue;
+                ok = warp_wait(&bars[L::bQFull + s], (ph >> s) & 1u, abort_flag, wd);
+                ph ^= 1u << s;
+            }
+            if (!ok) break;
+            any = true;
+            for (int n = 0; n <= nmax && ok; ++n) {
+                const uint32_t e_slot = stage, e_par = phase;
+                if (++stage == (uint32_t)L::kEntries) { stage = 0; phase ^= 1u; }
+                ATTN_TL_DECL(long long te = clock64());
+                if (!(ok = warp_wait(&bars[L::bEFull + e_slot], e_par, abort_flag, wd))) break;
+                ATTN_TL(1, 300, n, te, clock64());
+                const uint32_t ent_off = e_slot * L::kEntryBytes;
+                const uint64_t vd = dv0 + (uint64_t)((ent_off + L::kKVBytes) >> 4);
+                const uint64_t kd = dk0 + (uint64_t)(ent_off >> 4);
+#pragma unroll 1
+                for (int s = 0; s < 2; ++s) {
+                    const int ns = s ? t.n[1] : t.n[0];
+                    const bool do_pv = n >= 1 && n - 1 < ns, do_s = n < ns;
+                    const uint32_t colS = s ? kColS1 : kColS0;
+                    const uint32_t colO = s ? kColO1 : kColO0;
+                    ATTN_TL_DECL(long long tp = clock64());
+                    if (do_pv) {
+                        if (!(ok = warp_wait(&bars[L::bPFull + s], (ph >> (2 + s)) & 1u, abort_flag, wd))) break;
+                        ph ^= 4u << s;
+                        if (n - 1 == 0) {
+                            if (!(ok = warp_wait(&bars[L::bOEmpty + s], ((ph >> (4 + s)) & 1u) ^ 1u, abort_flag, wd))) break;
+                            ph ^= 16u << s;
+                        }
                     }
-                    bool k_ready = false;
-                    if (has_k) k_slot = stage;
-                    const uint32_t k_par = phase;
-                    if (has_k) {
-                        if (++stage == (uint32_t)L::kStages) { stage = 0; phase ^= 1u; }
-                    }
+                    ATTN_TL(1, 100 + s, n, tp, clock64());
                     tc_fence_after();
-                    for (int s = 0; s < 2 && ok; ++s) {
-                        const uint32_t colS = s ? kColS1 : kColS0;
-                        const uint32_t colO = s ? kColO1 : kColO0;
-                        if (has_v && n - 1 < t.n[s]) {
-                            if (!mbar_wait(&bars[L::bPFull + s], pf[s], abort_flag, wd)) { ok = false; break; }
-                            pf[s] ^= 1u;
-                            if (n - 1 == 0) {
-                                if (!mbar_wait(&bars[L::bOEmpty + s], oe[s] ^ 1u, abort_flag, wd)) { ok = false; break; }
-                                oe[s] ^= 1u;
-                            }
-                            tc_fence_after();
-                            const uint32_t vb = kv_base + v_slot * L::kKVBytes;
+                    if (do_pv) {
+                        const uint32_t acc0 = n - 1 > 0 ? 1u : 0u;
 #pragma unroll
-                            for (int k = 0; k < BN / 16; ++k) {
-                                const uint64_t bdesc = smem_desc_sw128(vb + k * 2048, L::kChunkBytesKV, 1024);
-                                tc_mma_ts(tmem + colO, tmem + colS + k * 8, bdesc, idO, (n - 1 > 0 || k > 0) ? 1u : 0u);
-                            }
-                            if (n - 1 == t.n[s] - 1) tc_commit(&bars[L::bOFull + s]);
-                        }
-                        if (has_k && n < t.n[s]) {
-                            if (!k_ready) {
-                                if (!mbar_wait(&bars[L::bKVFull + k_slot], k_par, abort_flag, wd)) { ok = false; break; }
-                                tc_fence_after();
-                                k_ready = true;
-                            }
-                            const uint32_t qb = q_base + s * L::kQBytes;
-                            const uint32_t kb = kv_base + k_slot * L::kKVBytes;
+                        for (int k = 0; k < BN / 16; ++k)
+                            tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO,
+                                         k == 0 ? acc0 : 1u);
+                    }
+                    if (do_s) {
+                        const uint64_t qd = s ? dq1 : dq0;
 #pragma unroll
-                            for (int k = 0; k < D / 16; ++k) {
-                                const uint32_t off = (k >> 2) * L::kChunkBytesQ + (k & 3) * 32;
-                                const uint32_t offk = (k >> 2) * L::kChunkBytesKV + (k & 3) * 32;
-                                tc_mma_ss(tmem + colS, smem_desc_sw128(qb + off, 16, 1024),
-                                          smem_desc_sw128(kb + offk, 16, 1024), idS, k > 0 ? 1u : 0u);
-                            }
-                            tc_commit(&bars[L::bSFull + s]);
-                            if (n == t.n[s] - 1) tc_commit(&bars[L::bQEmpty + s]);
+                        for (int k = 0; k < D / 16; ++k) {
+                            const uint64_t off = (uint64_t)(((k >> 2) * L::kChunkBytesQ + (k & 3) * 32) >> 4);
+                            tc_mma_ss_by(leader, tmem + colS, qd + off, kd + off, idS, k > 0 ? 1u : 0u);
                         }
+                        tc_commit_by(leader, &bars[L::bSFull + s]);
                     }
-                    if (!ok) break;
-                    if (has_v) tc_commit(&bars[L::bKVEmpty + v_slot]);
-                    if (has_k) {
-                        if (!k_ready) {  // a K tile no Q tile used (cannot happen for n < nmax, kept for safety)
-                            if (!mbar_wait(&bars[L::bKVFull + k_slot], k_par, abort_flag, wd)) { ok = false; break; }
-                        }
-                        tc_commit(&bars[L::bKVEmpty + k_slot]);
-                    }
+                    if (do_pv && n - 1 == ns - 1) tc_commit_by(leader, &bars[L::bOFull + s]);
+                    if (do_s && n == ns - 1) tc_commit_by(leader, &bars[L::bQEmpty + s]);
+                    if (s == 1) tc_commit_by(leader, &bars[L::bEEmpty + e_slot]);  // entry n read by both bursts
+                    ATTN_TL(1, 200 + s, n, clock64(), 0);
                 }
             }
-            if (any) {
-                // Wait until every issued MMA has completed before TMEM can be released.
-                tc_commit(&bars[L::bDrain]);
-                int dummy = 0;
-                mbar_wait(&bars[L::bDrain], 0, &dummy, 50000000ull);
-            }
+        }
+        if (any) {
+            // Wait until every issued MMA has completed before TMEM can be released.
+            tc_commit_by(leader, &bars[L::bDrain]);
+            int dummy = 0;
+            if (leader) mbar_wait(&bars[L::bDrain], 0, &dummy, 50000000ull);
+            __syncwarp();
         }
     }
     } else if (warp < 12) {
         // ------------------------------------------------------------------ softmax
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
         const int s = (warp - 4) >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
@@ -403,16 +442,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
             Tile t;
             get_tile(p, prefix, w, t);
-            const int ns = t.n[s];
+            const int ns = s ? t.n[1] : t.n[0];
             if (ns == 0) continue;
             const int tile_row0 = t.r0 + s * BM;
             const int qrow = tile_row0 + row;
             const int off = t.Lk - t.Lq;
             float m = -INFINITY, l = 0.0f;
             for (int n = 0; n < ns; ++n) {
-                if (!mbar_wait(&bars[L::bSFull + s], sf, abort_flag, wd)) { ok = false; break; }
+                ATTN_TL_DECL(long long ts0 = clock64());
+                if (!warp_wait(&bars[L::bSFull + s], sf, abort_flag, wd)) { ok = false; break; }
                 sf ^= 1u;
                 tc_fence_after();
+                ATTN_TL_DECL(long long ts1 = clock64());
                 uint32_t r[4][32];
                 tmem_ld32(tS + 0, r[0]);
                 tmem_ld32(tS + 32, r[1]);
@@ -488,10 +529,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[L::bPFull + s]);
+                if (quarter == 0) ATTN_TL(2 + s, n, ts0, ts1, clock64());
             }
             if (!ok) break;
             // Publish (m, l) once the epilogue has drained the previous tile of this stage.
-            if (!mbar_wait(&bars[L::bOEmpty + s], oe ^ 1u, abort_flag, wd)) { ok = false; break; }
+            if (!warp_wait(&bars[L::bOEmpty + s], oe ^ 1u, abort_flag, wd)) { ok = false; break; }
             oe ^= 1u;
             st_m[s * BM + row] = m;
             st_l[s * BM + row] = l;
@@ -508,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------------ epilogue
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -532,9 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     continue;
                 }
-                if (!mbar_wait(&bars[L::bOFull + s], of[s], abort_flag, wd)) { ok = false; break; }
+                if (!warp_wait(&bars[L::bOFull + s], of[s], abort_flag, wd)) { ok = false; break; }
                 of[s] ^= 1u;
-                if (!mbar_wait(&bars[L::bStats + s], sp[s], abort_flag, wd)) { ok = false; break; }
+                if (!warp_wait(&bars[L::bStats + s], sp[s], abort_flag, wd)) { ok = false; break; }
                 sp[s] ^= 1u;
                 tc_fence_after();
                 const float m = st_m[s * BM + row];
@@ -647,3 +689,14 @@ cudaError_t launch_watchdog_probe(int* status, unsigned long long limit_ns, cuda
 }
 
 }  // namespace attn
+
+#ifdef ATTN_TIMELINE
+extern "C" int attn_timeline_read(long long* out, int* counts) {
+    cudaDeviceSynchronize();
+    cudaMemcpyFromSymbol(out, attn::g_timeline, sizeof(long long) * 5 * 4096 * 4);
+    cudaMemcpyFromSymbol(counts, attn::g_timeline_n, sizeof(int) * 5);
+    int z[5] = {0, 0, 0, 0, 0};
+    cudaMemcpyToSymbol(attn::g_timeline_n, z, sizeof(z));
+    return 0;
+}
+#endif
