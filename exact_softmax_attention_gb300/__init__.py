@@ -27,9 +27,10 @@ ATTN_ERR_CUDA = -5
 ATTN_ERR_DEVICE_TIMEOUT = -6
 ATTN_ERR_DEVICE_BAD_INDEX = -7
 ATTN_ERR_BAD_ARG = -8
+ATTN_ERR_SCRATCH_TOO_SMALL = -9
 
 #: every symbol the header declares
-EXPORTS = ("attn_fwd", "attn_decode_paged", "attn_decode_plan", "attn_status_string", "attn_get_device_status",
+EXPORTS = ("attn_fwd", "attn_decode_paged", "attn_decode_paged_noalloc", "attn_decode_plan", "attn_status_string", "attn_get_device_status",
            "attn_set_option", "attn_get_option", "attn_read_counters", "attn_debug_exp2", "attn_debug_watchdog",
            "attn_version")
 
@@ -50,6 +51,8 @@ lib.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i
 lib.attn_fwd.restype = _i
 lib.attn_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i]
 lib.attn_decode_paged.restype = _i
+lib.attn_decode_paged_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i]
+lib.attn_decode_paged_noalloc.restype = _i
 lib.attn_decode_plan.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]
 lib.attn_decode_plan.restype = _i
 lib.attn_status_string.argtypes = [_i]
@@ -117,6 +120,16 @@ def attn_decode_paged(q, k_cache, v_cache, page_table, seqlens, page_size, o, ls
                                int(page_size), _ptr(o), _ptr(lse), _stream(stream), int(B), int(Hq), int(Hkv), int(d),
                                int(max_pages_per_seq), int(num_pages), float(scale), int(num_splits))
     return _check(rc, "attn_decode_paged", raise_on_error)
+
+
+def attn_decode_paged_noalloc(q, k_cache, v_cache, page_table, seqlens, page_size, o, lse, stream, B, Hq, Hkv, d,
+                              max_pages_per_seq, num_pages, scale, num_splits=0, raise_on_error=True):
+    """attn_decode_paged without allocating: split partials use the library's fixed 32 MiB
+    device array (see include/attn.h for the size limit and the sharing rules)."""
+    rc = lib.attn_decode_paged_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(seqlens),
+                                       int(page_size), _ptr(o), _ptr(lse), _stream(stream), int(B), int(Hq), int(Hkv),
+                                       int(d), int(max_pages_per_seq), int(num_pages), float(scale), int(num_splits))
+    return _check(rc, "attn_decode_paged_noalloc", raise_on_error)
 
 
 def attn_decode_plan(B, Hkv, max_pages_per_seq, page_size, num_splits=0, num_sms=0):

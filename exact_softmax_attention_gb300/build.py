@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libattn_gb300.so")
-SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_decode.cu"]
+SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_decode.cu", "attn_decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

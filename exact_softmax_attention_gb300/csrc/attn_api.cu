@@ -123,6 +123,7 @@ const char* attn_status_string(attn_status_t s) {
         case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting on its pipeline (device watchdog)";
         case ATTN_ERR_DEVICE_BAD_INDEX: return "a page index or sequence length was out of range";
         case ATTN_ERR_BAD_ARG: return "unknown option or invalid value";
+        case ATTN_ERR_SCRATCH_TOO_SMALL: return "the sizes need more split workspace than the fixed scratch array holds";
         default: return "unknown status";
     }
 }
@@ -388,3 +389,14 @@ attn_status_t attn_debug_watchdog(unsigned long long limit_ns, void* stream) {
 }
 
 }  // extern "C"
+
+namespace attn {
+int current_device_info(int** status, int* num_sms) {
+    DeviceState* ds = nullptr;
+    const attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+    *status = ds->status;
+    *num_sms = ds->num_sms;
+    return ATTN_OK;
+}
+}  // namespace attn

@@ -63,6 +63,10 @@ struct DecodeParams {
 
 cudaError_t launch_attn_decode(const DecodeParams& p, int d, cudaStream_t stream);
 
+// Status word and SM count of the current device (checks that it is an sm_103 GPU);
+// returns an attn_status_t code.
+int current_device_info(int** status, int* num_sms);
+
 // Diagnostics
 cudaError_t launch_exp2_probe(const float* x, float* y, long long n, int mode, cudaStream_t stream);
 cudaError_t launch_watchdog_probe(int* status, unsigned long long limit_ns, cudaStream_t stream);

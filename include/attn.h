@@ -46,6 +46,7 @@ typedef int attn_status_t;
 #define ATTN_ERR_DEVICE_TIMEOUT (-6)    /* a kernel gave up on a pipeline wait (device status) */
 #define ATTN_ERR_DEVICE_BAD_INDEX (-7)  /* a page index or sequence length was out of range (device status) */
 #define ATTN_ERR_BAD_ARG (-8)           /* an unknown option name or an invalid value */
+#define ATTN_ERR_SCRATCH_TOO_SMALL (-9) /* attn_decode_paged_noalloc: sizes exceed its fixed scratch */
 
 /*
  * Forward attention ("FlashAttention: not computing less, moving less", section 01
@@ -111,6 +112,33 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* page_table,
                                 const int* seqlens, int page_size, void* o, float* lse, void* stream, int B, int Hq,
                                 int Hkv, int d, int max_pages_per_seq, int num_pages, float scale, int num_splits);
+
+/*
+ * attn_decode_paged without any memory allocation. The pages have no counterpart to this
+ * call; it exists for callers that cannot allocate device memory when they run decode:
+ * a serving engine that has already given nearly all of the GPU's memory to its own
+ * KV-cache pool, or code that must not enter the driver's allocator, which can block the
+ * device or fail late under memory pressure.
+ *
+ * Same arguments, layouts, results and error behaviour as attn_decode_paged. The split
+ * partials go to one fixed 32 MiB device array built into the library (every GPU that
+ * loads the library holds it until the process exits) instead of memory taken per call.
+ * - Sizes whose partials need more than 32 MiB, that is B * Hq * splits * (d + 1) * 4
+ *   bytes with splits from attn_decode_plan, are rejected with
+ *   ATTN_ERR_SCRATCH_TOO_SMALL before anything is launched (lower num_splits to fit).
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call before any
+ *   stream capture begins.
+ * - All calls on a device share the one array, and it keeps the last call's contents.
+ *   Nothing in it needs clearing, because the combine step reads only partials the same
+ *   call wrote. Calls whose work overlaps on the GPU (on different streams, say) race on
+ *   the array and may produce wrong results: order them.
+ * - No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_cache, const void* v_cache, const int* page_table,
+                                        const int* seqlens, int page_size, void* o, float* lse, void* stream, int B,
+                                        int Hq, int Hkv, int d, int max_pages_per_seq, int num_pages, float scale,
+                                        int num_splits);
 
 /*
  * Host-side split choice of attn_decode_paged (the num_splits = 0 heuristic of "Faster,
