@@ -45,8 +45,8 @@ DEC_KERNEL = "decode_split_kernel"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
@@ -67,10 +67,15 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-def source_sha() -> str:
+KERNEL_SOURCES = {FWD_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"],
+                  DEC_KERNEL: ["attn_decode.cu", "ptx.cuh", "kernels.cuh"]}
+
+
+def source_sha(kernel: str) -> str:
+    """Hash of the sources a kernel is compiled from (to tell whether a profile is stale)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_softmax_attention_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
@@ -83,64 +88,110 @@ def ncu_traffic(kernel: str):
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             t = json.load(f)
         e = t[kernel]
-        return float(e["dram_bytes_per_launch"]) if e.get("source_sha") == source_sha() else None
+        return float(e["dram_bytes_per_launch"]) if e.get("source_sha") == source_sha(kernel) else None
     except (OSError, KeyError, ValueError):
         return None
 
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+    """Samples SM clocks and clock-event (throttle) reasons while the timed region runs.
 
-    def __init__(self, gpu_index: int):
-        self.idx = gpu_index
-        self.proc = None
-        self.lines = []
+    Reads NVML through ctypes every ~2 ms (read-only queries); falls back to nvidia-smi
+    at 100 ms when NVML cannot be loaded. Changes no GPU setting."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device):
+        self.dev = torch_device
+        self.samples = []  # (sm_mhz, reasons_mask)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._nvml = None
+        self._handle = None
+        self.source = None
+
+    def _open_nvml(self):
+        import ctypes
+        import torch
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        ok = False
+        uuid = getattr(torch.cuda.get_device_properties(self.dev), "uuid", None)
+        if uuid is not None:
+            ok = nv.nvmlDeviceGetHandleByUUID(f"GPU-{uuid}".encode(), ctypes.byref(h)) == 0
+        if not ok:
+            cnt = ctypes.c_uint()
+            if nv.nvmlDeviceGetCount_v2(ctypes.byref(cnt)) == 0 and cnt.value == 1:
+                ok = nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) == 0
+        if not ok:
+            return False
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        self._nvml, self._handle = nv, h
+        return True
+
+    def _run_nvml(self):
+        import ctypes
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        get_r = getattr(self._nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self._nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if self._nvml.nvmlDeviceGetClockInfo(self._handle, 1, ctypes.byref(clk)) == 0:
+                r = rs.value if get_r(self._handle, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((float(clk.value), int(r)))
+            time.sleep(0.002)
+
+    def _run_smi(self):
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or "0"
+        try:
+            proc = subprocess.Popen(["nvidia-smi", "-i", vis, f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                     "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        bits = [0x8, 0x40, 0x20, 0x4]
+        while not self._stop.is_set():
+            line = proc.stdout.readline()
+            if not line:
+                break
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                sm, mx = float(parts[0]), float(parts[1])
+            except (ValueError, IndexError):
+                continue
+            self.max_mhz = mx
+            mask = sum(b for b, v in zip(bits, parts[2:6]) if v.lower().startswith("active"))
+            self.samples.append((sm, mask))
+        proc.terminate()
 
     def __enter__(self):
-        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
-             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-             "clocks_event_reasons.sw_power_cap")
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
-        except OSError:
-            self.proc = None
+            use_nvml = self._open_nvml()
+        except (OSError, AttributeError):
+            use_nvml = False
+        self.source = "nvml" if use_nvml else "nvidia-smi"
+        self._t = threading.Thread(target=self._run_nvml if use_nvml else self._run_smi, daemon=True)
+        self._t.start()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *a):
-        if self.proc:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+        self._stop.set()
+        self._t.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 7:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[3:7]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": self.source}
+        mask = 0
+        for _, r in self.samples:
+            mask |= r
+        return {"sm_mhz": statistics.median(x for x, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in self.REASONS.items() if mask & b), "samples": len(self.samples),
+                "source": self.source}
 
 
 # ------------------------------------------------------------------ oracle (CPU) legs
@@ -287,14 +338,7 @@ def run_ours(args):
     K_ = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_)]
     barrier()
-    gpu_index = torch.cuda.current_device()
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
-    if vis:
-        try:
-            gpu_index = int(vis.split(",")[gpu_index])
-        except (ValueError, IndexError):
-            pass
-    with ClockSampler(gpu_index) as clk:
+    with ClockSampler(dev) as clk:
         t_wall0 = time.perf_counter()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
