@@ -194,6 +194,24 @@ class ClockSampler:
                 "source": self.source}
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Maximum of a per-rank timing over all ranks (a tiny all-reduce; no data-path collective)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def decode_sample_case(dc, n_seq):
+    """The first ``n_seq`` sequences of a decode workload as a workload of their own (same
+    lengths, same recipe), so a CPU sample does not have to materialise the whole pool."""
+    return W.DecodeCase(dc.name + "_sample", n_seq, dc.Hq, dc.Hkv, dc.d, dc.page_size, dc.seqlens[:n_seq].copy(),
+                        dc.max_pages, dc.scale, dc.seed)
+
+
 # ------------------------------------------------------------------ oracle (CPU) legs
 
 def oracle_fwd_sample(case, q, k, v, n_rows, seed, n_threads):
@@ -246,7 +264,8 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if world > 1 and rank != 0:
         return
-    fc, dc = W.long_causal(), W.decode()
+    fc = W.long_causal()
+    dc = decode_sample_case(W.decode(), 1)
     fin = fc.generate()
     din = dc.generate()
     threads = os.cpu_count() or 1
@@ -359,17 +378,9 @@ def run_ours(args):
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
     dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    total_ms = max_over_ranks(total_ms)
-    fwd_ms = max_over_ranks(fwd_ms)
-    dec_ms = max_over_ranks(dec_ms)
+    total_ms = max_over_ranks(total_ms, world, dev)
+    fwd_ms = max_over_ranks(fwd_ms, world, dev)
+    dec_ms = max_over_ranks(dec_ms, world, dev)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -406,8 +417,8 @@ def run_ours(args):
                 hdlse.copy_(DLSE, non_blocking=True)
                 evs[i][2].record(stream)
             barrier()
-        e_f = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs))
-        e_d = max_over_ranks(sum(e[1].elapsed_time(e[2]) for e in evs))
+        e_f = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs), world, dev)
+        e_d = max_over_ranks(sum(e[1].elapsed_time(e[2]) for e in evs), world, dev)
         e2e = {"value": world * n_e2e * fc.flops() / (e_f * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "decode": {"value": world * n_e2e * dc.bytes() / (e_d * 1e-3) / 1e9, "unit": "GB/s"}}
