@@ -60,8 +60,8 @@ struct Layout {
     // barrier indices
     static constexpr int bQFull = 0, bQEmpty = 2, bEFull = 4, bEEmpty = 4 + kEntries;
     static constexpr int bSFull = 4 + 2 * kEntries, bPFull = bSFull + 2, bOFull = bSFull + 4, bOEmpty = bSFull + 6;
-    static constexpr int bStats = bSFull + 8, bDrain = bSFull + 10;
-    static constexpr int kNumBars = bDrain + 1;
+    static constexpr int bStats = bSFull + 8, bDrain = bSFull + 10, bIssued = bSFull + 12;
+    static constexpr int kNumBars = bIssued + 2;
     static constexpr int kStatsOff = kBarOff + ((kNumBars * 8 + 15) / 16) * 16;
     static constexpr int kMiscOff = kStatsOff + 2 * 2 * BM * 4;   // m[2][128], l[2][128]
     static constexpr int kPrefixOff = kMiscOff + 16;               // tmem base, abort flag
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars[L::bQEmpty + 1], 1);
         for (int i = 0; i < L::kEntries; ++i) {
             mbar_init(&bars[L::bEFull + i], 1);
-            mbar_init(&bars[L::bEEmpty + i], 1);
+            mbar_init(&bars[L::bEEmpty + i], 2);  // released by both MMA warps
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[L::bSFull + s], 1);
@@ -224,7 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[L::bOEmpty + s], 4);
             mbar_init(&bars[L::bStats + s], 4);
         }
-        mbar_init(&bars[L::bDrain], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[L::bDrain + s], 1);
+            mbar_init(&bars[L::bIssued + s], 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -336,23 +339,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(&bars[L::bQFull + s], qphase[s] ^ 1u, &dummy, 20000000ull);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
-        // The whole warp walks the schedule (descriptors and slots stay warp-uniform); lane 0
-        // issues every tcgen05 instruction. Per KV step n the tensor pipe receives
-        //   burst 0: PV0(n-1), S0(n)     burst 1: PV1(n-1), S1(n)
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------------ MMA issuers
+        // Warp 1 issues Q tile 0's products, warp 2 Q tile 1's. Per KV step n the tensor pipe
+        // receives
+        //   burst 0 (warp 1): PV0(n-1), S0(n)     burst 1 (warp 2): PV1(n-1), S1(n)
         // so it computes one tile's products while the other tile's softmax works; S_s(n) is
         // issued after PV_s(n-1) by the same thread, so its completion covers PV_s(n-1).
-        // Completion signals go out back to back after each burst: a commit briefly drains
-        // the tensor pipe, and consecutive commits share that drain.
+        // A token pair keeps the bursts in that alternating order: each warp passes the token
+        // as soon as its MMAs are issued, before its completion signals, so the other warp's
+        // waits and descriptor set-up overlap the commits. Both warps walk the same schedule;
+        // ring entry n is released once both have committed their reads of it (count 2).
+        // Within a warp, lane 0 issues every tcgen05 instruction while the whole warp keeps the
+        // descriptors and slots warp-uniform.
+        const int s = warp - 1;
         const uint32_t leader = lane == 0;
         constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0);
         constexpr uint32_t idO = idesc_bf16_f32(BM, D, 1);
+        const uint32_t colS = s ? kColS1 : kColS0;
+        const uint32_t colO = s ? kColO1 : kColO0;
         uint32_t stage = 0, phase = 0;
-        uint32_t ph = 0;  // phase bits: 0-1 Q full, 2-3 P full, 4-5 O empty (per Q tile)
-        const uint32_t q_base = smem_u32(smem + L::kQOff);
+        uint32_t qf = 0, pf = 0, oe = 0, burst = 0;
+        const uint32_t q_base = smem_u32(smem + L::kQOff) + s * L::kQBytes;
         const uint32_t kv_base = smem_u32(smem + L::kKVOff);
-        const uint64_t dq0 = smem_desc_sw128(q_base, 16, 1024), dq1 = smem_desc_sw128(q_base + L::kQBytes, 16, 1024);
+        const uint64_t dq = smem_desc_sw128(q_base, 16, 1024);
         const uint64_t dk0 = smem_desc_sw128(kv_base, 16, 1024);
         const uint64_t dv0 = smem_desc_sw128(kv_base, L::kChunkBytesKV, 1024);
         bool ok = true, any = false;
@@ -360,69 +370,67 @@ __global__ void __launch_bounds__(kThreads, 1)
             Tile t;
             get_tile(p, prefix, w, t);
             const int nmax = max(t.n[0], t.n[1]);
+            const int ns = s ? t.n[1] : t.n[0];
             if (nmax == 0) continue;
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-                if (!ok || t.n[s] == 0) continue;
-                ok = warp_wait(&bars[L::bQFull + s], (ph >> s) & 1u, abort_flag, wd);
-                ph ^= 1u << s;
+            if (ns > 0) {
+                if (!(ok = warp_wait(&bars[L::bQFull + s], qf, abort_flag, wd))) break;
+                qf ^= 1u;
+                any = true;
             }
-            if (!ok) break;
-            any = true;
             for (int n = 0; n <= nmax && ok; ++n) {
+                const bool do_pv = n >= 1 && n - 1 < ns, do_s = n < ns;
                 const uint32_t e_slot = stage, e_par = phase;
                 if (++stage == (uint32_t)L::kEntries) { stage = 0; phase ^= 1u; }
-                ATTN_TL_DECL(long long te = clock64());
+                ATTN_TL_DECL(long long tp = clock64());
                 if (!(ok = warp_wait(&bars[L::bEFull + e_slot], e_par, abort_flag, wd))) break;
-                ATTN_TL(1, 300, n, te, clock64());
-                const uint32_t ent_off = e_slot * L::kEntryBytes;
-                const uint64_t vd = dv0 + (uint64_t)((ent_off + L::kKVBytes) >> 4);
-                const uint64_t kd = dk0 + (uint64_t)(ent_off >> 4);
-#pragma unroll 1
-                for (int s = 0; s < 2; ++s) {
-                    const int ns = s ? t.n[1] : t.n[0];
-                    const bool do_pv = n >= 1 && n - 1 < ns, do_s = n < ns;
-                    const uint32_t colS = s ? kColS1 : kColS0;
-                    const uint32_t colO = s ? kColO1 : kColO0;
-                    ATTN_TL_DECL(long long tp = clock64());
-                    if (do_pv) {
-                        if (!(ok = warp_wait(&bars[L::bPFull + s], (ph >> (2 + s)) & 1u, abort_flag, wd))) break;
-                        ph ^= 4u << s;
-                        if (n - 1 == 0) {
-                            if (!(ok = warp_wait(&bars[L::bOEmpty + s], ((ph >> (4 + s)) & 1u) ^ 1u, abort_flag, wd))) break;
-                            ph ^= 16u << s;
-                        }
+                if (do_pv) {
+                    if (!(ok = warp_wait(&bars[L::bPFull + s], pf, abort_flag, wd))) break;
+                    pf ^= 1u;
+                    if (n - 1 == 0) {
+                        if (!(ok = warp_wait(&bars[L::bOEmpty + s], oe ^ 1u, abort_flag, wd))) break;
+                        oe ^= 1u;
                     }
-                    ATTN_TL(1, 100 + s, n, tp, clock64());
-                    tc_fence_after();
-                    if (do_pv) {
-                        const uint32_t acc0 = n - 1 > 0 ? 1u : 0u;
-#pragma unroll
-                        for (int k = 0; k < BN / 16; ++k)
-                            tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO,
-                                         k == 0 ? acc0 : 1u);
-                    }
-                    if (do_s) {
-                        const uint64_t qd = s ? dq1 : dq0;
-#pragma unroll
-                        for (int k = 0; k < D / 16; ++k) {
-                            const uint64_t off = (uint64_t)(((k >> 2) * L::kChunkBytesQ + (k & 3) * 32) >> 4);
-                            tc_mma_ss_by(leader, tmem + colS, qd + off, kd + off, idS, k > 0 ? 1u : 0u);
-                        }
-                        tc_commit_by(leader, &bars[L::bSFull + s]);
-                    }
-                    if (do_pv && n - 1 == ns - 1) tc_commit_by(leader, &bars[L::bOFull + s]);
-                    if (do_s && n == ns - 1) tc_commit_by(leader, &bars[L::bQEmpty + s]);
-                    if (s == 1) tc_commit_by(leader, &bars[L::bEEmpty + e_slot]);  // entry n read by both bursts
-                    ATTN_TL(1, 200 + s, n, clock64(), 0);
                 }
+                // token: burst 0 of step n follows burst 1 of step n-1; burst 1 follows burst 0
+                if (s == 0) {
+                    if (burst > 0 && !(ok = warp_wait(&bars[L::bIssued + 1], (burst - 1) & 1u, abort_flag, wd))) break;
+                } else {
+                    if (!(ok = warp_wait(&bars[L::bIssued + 0], burst & 1u, abort_flag, wd))) break;
+                }
+                ATTN_TL(s ? 4 : 1, 100 + s, n, tp, clock64());
+                tc_fence_after();
+                const uint32_t ent_off = e_slot * L::kEntryBytes;
+                if (do_pv) {
+                    const uint64_t vd = dv0 + (uint64_t)((ent_off + L::kKVBytes) >> 4);
+                    const uint32_t acc0 = n - 1 > 0 ? 1u : 0u;
+#pragma unroll
+                    for (int k = 0; k < BN / 16; ++k)
+                        tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO,
+                                     k == 0 ? acc0 : 1u);
+                }
+                if (do_s) {
+                    const uint64_t kd = dk0 + (uint64_t)(ent_off >> 4);
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint64_t off = (uint64_t)(((k >> 2) * L::kChunkBytesQ + (k & 3) * 32) >> 4);
+                        tc_mma_ss_by(leader, tmem + colS, dq + off, kd + off, idS, k > 0 ? 1u : 0u);
+                    }
+                }
+                __syncwarp();
+                if (leader) mbar_arrive(&bars[L::bIssued + s]);
+                if (do_s) tc_commit_by(leader, &bars[L::bSFull + s]);
+                if (do_pv && n - 1 == ns - 1) tc_commit_by(leader, &bars[L::bOFull + s]);
+                if (do_s && n == ns - 1) tc_commit_by(leader, &bars[L::bQEmpty + s]);
+                tc_commit_by(leader, &bars[L::bEEmpty + e_slot]);
+                ATTN_TL(s ? 4 : 1, 200 + s, n, clock64(), 0);
+                ++burst;
             }
         }
         if (any) {
-            // Wait until every issued MMA has completed before TMEM can be released.
-            tc_commit_by(leader, &bars[L::bDrain]);
+            // Wait until every MMA this warp issued has completed before TMEM can be released.
+            tc_commit_by(leader, &bars[L::bDrain + s]);
             int dummy = 0;
-            if (leader) mbar_wait(&bars[L::bDrain], 0, &dummy, 50000000ull);
+            if (leader) mbar_wait(&bars[L::bDrain + s], 0, &dummy, 50000000ull);
             __syncwarp();
         }
     }
@@ -475,13 +483,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < BN; ++c)
                         if (c >= lim) sv[c] = -INFINITY;
                 }
+                // row maximum: eight chains of three-input maxima
                 float mx[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx[i] = sv[i];
+                for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[i], sv[i + 8]);
 #pragma unroll
-                for (int c = 8; c < BN; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
-                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                for (int c = 16; c < BN; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx[i] = max3f(mx[i], sv[c + i], sv[c + 8 + i]);
+                const float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
                 const float m_cand = fmaxf(m, mt);
                 const bool need = (m_cand - m) * sl2 > p.rescale_thr;  // NaN (both -inf) is false
                 const bool warp_need = __any_sync(0xffffffffu, need);
@@ -505,12 +515,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++c_dec;
                 const float neg = (m == -INFINITY) ? 0.0f : -m * sl2;
+                // exponent arguments two at a time (packed FMA), exponentials, packed row sums
                 float sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
                 uint32_t pk[64];
 #pragma unroll
                 for (int c = 0; c < BN; c += 2) {
-                    const float x0 = fmaf(sv[c], sl2, neg);
-                    const float x1 = fmaf(sv[c + 1], sl2, neg);
+                    float x0, x1;
+                    ffma2(x0, x1, sv[c], sv[c + 1], sl2, sl2, neg, neg);
                     float p0, p1;
                     if (POLY_EVERY > 0 && (c % (POLY_EVERY > 0 ? POLY_EVERY : 1)) == POLY_EVERY - 2) {
                         p0 = ex2_mufu(x0);
@@ -519,7 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p0 = ex2_mufu(x0);
                         p1 = ex2_mufu(x1);
                     }
-                    sum[(c >> 1) & 7] += p0 + p1;
+                    const int a = ((c >> 1) & 3) * 2;
+                    fadd2(sum[a], sum[a + 1], sum[a], sum[a + 1], p0, p1);
                     pk[c >> 1] = pack_bf16x2(p0, p1);
                 }
                 tmem_st32(tS + 0, &pk[0]);
