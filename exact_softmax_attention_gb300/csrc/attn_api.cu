@@ -210,23 +210,34 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
     p.scale = scale;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     p.rescale_thr = (float)opt.rescale_threshold;
-    // scheduling section: largest multiple of G dividing Hq that is <= target heads
-    int target = opt.sec_heads > 0 ? opt.sec_heads : 8;
-    if (target < p.G) target = p.G;
-    int sec = p.G;
-    for (int c = p.G; c <= Hq && c <= target; c += p.G)
-        if (Hq % c == 0) sec = c;
-    p.sec_q = sec;
     p.status = ds->status;
     p.counters = opt.count ? ds->counters : nullptr;
     p.watchdog_ns = (unsigned long long)(opt.watchdog_ms * 1e6);
     int grid = ds->num_sms;
     if (!cu_seqlens) {
-        const long long tiles = (long long)B * Hq * cdiv(Nq, 256);
-        if (tiles > INT32_MAX) return ATTN_ERR_BAD_SHAPE;
+        const long long nblk = cdiv(Nq, 256);
+        const long long pairs = (long long)B * Hq;
+        const long long tiles = pairs * nblk;
+        if (tiles > INT32_MAX / 2) return ATTN_ERR_BAD_SHAPE;
         p.total_tiles = (int)tiles;
         if (tiles < grid) grid = (int)tiles;
+        // Section of (batch, head) pairs: all of them unless the tiles make 16 or more waves
+        // of the grid; then sections of at least 8 waves each, which keeps the heaviest-first
+        // order balanced within a section while fewer key/value heads share the L2.
+        long long sec = pairs;
+        if (opt.sec_heads > 0) sec = opt.sec_heads;
+        else if (nblk > 0 && tiles >= 16LL * grid) sec = cdiv(8LL * grid, nblk);
+        sec = ((sec + p.G - 1) / p.G) * p.G;
+        if (sec > pairs) sec = pairs;
+        p.sec_q = (int)sec;
     } else {
+        // packed: largest multiple of G dividing Hq that is <= the target heads per section
+        int target = opt.sec_heads > 0 ? opt.sec_heads : 8;
+        if (target < p.G) target = p.G;
+        int sec = p.G;
+        for (int c = p.G; c <= Hq && c <= target; c += p.G)
+            if (Hq % c == 0) sec = c;
+        p.sec_q = sec;
         p.total_tiles = 0;
     }
     if (grid <= 0) return ATTN_OK;

@@ -115,12 +115,18 @@ __device__ __forceinline__ bool packed_seq(const FwdParams& p, int b, int& first
     return ok;
 }
 
-// Map a work-tile index to its tile. Order inside a sequence: head sections of
-// sec_q query heads (whose key/value heads fit the L2 together), then query
-// blocks heaviest first under a causal mask, then the heads of the section (the
-// query heads of one key/value head are adjacent). Sequences are outermost.
+// Map a work-tile index to its tile (a work tile is two consecutive 128-row Q tiles of one
+// (sequence, query head)). The order puts the heaviest tiles first so that the snake walk
+// below balances the persistent CTAs (longest-processing-time first; under a causal mask a
+// tile's cost grows with its query block index).
+//   dense batches: sections of sec_q (batch, head) pairs, then query blocks, then the pairs
+//     of the section; sec_q is all pairs unless the problem spans many waves, where smaller
+//     sections keep the key/value heads being read together within the L2;
+//   packed sequences: sequences outermost, then sections of sec_q query heads, then query
+//     blocks, then the heads of the section.
+// The query heads of one key/value head are adjacent in both.
 __device__ __forceinline__ void get_tile(const FwdParams& p, const int* prefix, int w, Tile& t) {
-    int b, u, Lq, Lk, q0, k0;
+    int b, Lq, Lk, q0, k0, jj, h;
     if (p.cu_seqlens) {
         int lo = 0, hi = p.B;  // prefix[b] <= w < prefix[b+1]
         while (hi - lo > 1) {
@@ -128,29 +134,36 @@ __device__ __forceinline__ void get_tile(const FwdParams& p, const int* prefix, 
             if (prefix[mid] <= w) lo = mid; else hi = mid;
         }
         b = lo;
-        u = w - prefix[b];
+        const int u = w - prefix[b];
         int first, len;
         packed_seq(p, b, first, len);
         q0 = k0 = first;
         Lq = Lk = len;
+        const int nblk = cdiv(Lq, 2 * BM);
+        const int sec = p.sec_q;
+        const int per_sec = nblk * sec;
+        const int si = u / per_sec;
+        const int rem = u - si * per_sec;
+        jj = rem / sec;
+        h = si * sec + (rem - jj * sec);
     } else {
-        const int per_b = p.Hq * cdiv(p.Nq, 2 * BM);
-        b = w / per_b;
-        u = w - b * per_b;
         Lq = p.Nq;
         Lk = p.Nk;
+        const int nblk = cdiv(Lq, 2 * BM);
+        const int pairs = p.B * p.Hq;
+        const int sec = p.sec_q;
+        const int si = w / (sec * nblk);
+        const int rem = w - si * (sec * nblk);
+        const int len = min(sec, pairs - si * sec);  // the last section may be shorter
+        jj = rem / len;
+        const int pair = si * sec + (rem - jj * len);
+        b = pair / p.Hq;
+        h = pair - b * p.Hq;
         q0 = b * p.Nq;
         k0 = b * p.Nk;
     }
-    const int nblk = cdiv(Lq, 2 * BM);
-    const int sec = p.sec_q;
-    const int per_sec = nblk * sec;
-    const int si = u / per_sec;
-    const int rem = u - si * per_sec;
-    const int jj = rem / sec;
-    const int hh = rem - jj * sec;
-    const int j = p.causal ? (nblk - 1 - jj) : jj;
-    t.h = si * sec + hh;
+    const int j = p.causal ? (cdiv(Lq, 2 * BM) - 1 - jj) : jj;
+    t.h = h;
     t.kvh = t.h / p.G;
     t.q0 = q0;
     t.k0 = k0;
@@ -172,6 +185,14 @@ __device__ __forceinline__ void get_tile(const FwdParams& p, const int* prefix, 
         }
         t.n[s] = n;
     }
+}
+
+// The r-th work tile of this CTA: rounds of gridDim.x consecutive tiles, walked in
+// alternating direction (a snake), so that a CTA given one of the heaviest tiles of a round
+// is given one of the lightest of the next.
+__device__ __forceinline__ int snake_index(int r) {
+    const int c = (r & 1) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+    return r * (int)gridDim.x + c;
 }
 
 // Software 2^x on the FMA/ALU pipes ("FlashAttention-4: Blackwell algorithm-pipeline
@@ -284,7 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t stage = 0, phase = 0, qphase[2] = {0, 0};
         int issued = 0;
         bool ok = true;
-        for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
+            const int w = snake_index(r);
+            if (w >= total) continue;
             Tile t;
             get_tile(p, prefix, w, t);
             const int nmax = max(t.n[0], t.n[1]);
@@ -366,7 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dk0 = smem_desc_sw128(kv_base, 16, 1024);
         const uint64_t dv0 = smem_desc_sw128(kv_base, L::kChunkBytesKV, 1024);
         bool ok = true, any = false;
-        for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
+            const int w = snake_index(r);
+            if (w >= total) continue;
             Tile t;
             get_tile(p, prefix, w, t);
             const int nmax = max(t.n[0], t.n[1]);
@@ -447,7 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sf = 0, oe = 0;
         unsigned long long c_dec = 0, c_res = 0;
         bool ok = true;
-        for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
+            const int w = snake_index(r);
+            if (w >= total) continue;
             Tile t;
             get_tile(p, prefix, w, t);
             const int ns = s ? t.n[1] : t.n[0];
@@ -568,7 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         uint32_t of[2] = {0, 0}, sp[2] = {0, 0};
         bool ok = true;
-        for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
+            const int w = snake_index(r);
+            if (w >= total) continue;
             Tile t;
             get_tile(p, prefix, w, t);
             for (int s = 0; s < 2; ++s) {

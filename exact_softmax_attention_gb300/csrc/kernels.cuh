@@ -28,7 +28,7 @@ struct FwdParams {
     float scale;        // softmax scale applied to q.k
     float scale_log2;   // scale * log2(e)
     float rescale_thr;  // rescale O only when the row max grows by more than this (base-2 exponent units)
-    int sec_q;          // query heads per scheduling section (multiple of G, divides Hq)
+    int sec_q;          // scheduling section, a multiple of G: dense, (batch, head) pairs; packed, query heads (divides Hq)
     int total_tiles;    // dense: number of work tiles; varlen: ignored (computed on device)
     int* status;
     unsigned long long* counters;  // nullptr unless counting is enabled
