@@ -40,6 +40,7 @@ constexpr int BM = 128;  // rows per Q tile
 constexpr int BN = 128;  // keys per K/V tile
 constexpr int kThreads = 512;
 constexpr int kMaxVarlenB = 1024;
+constexpr int kMaxLevels = 2048;  // 256-row blocks per packed sequence for the level order
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
 constexpr uint32_t kTmemCols = 512;
 
@@ -64,8 +65,13 @@ struct Layout {
     static constexpr int kNumBars = bIssued + 2;
     static constexpr int kStatsOff = kBarOff + ((kNumBars * 8 + 15) / 16) * 16;
     static constexpr int kMiscOff = kStatsOff + 2 * 2 * BM * 4;   // m[2][128], l[2][128]
-    static constexpr int kPrefixOff = kMiscOff + 16;               // tmem base, abort flag
-    static constexpr int kBytes = kPrefixOff + (kMaxVarlenB + 1) * 4;
+    // misc: tmem base, abort flag, packed-order levels, packed work tiles
+    // packed-sequence work order (built once per CTA): pre, lvl, perm, nbs
+    static constexpr int kPreOff = kMiscOff + 16;
+    static constexpr int kLvlOff = kPreOff + ((kMaxVarlenB + 1) * 4 + 15) / 16 * 16;
+    static constexpr int kPermOff = kLvlOff + ((kMaxLevels + 2) * 4 + 15) / 16 * 16;
+    static constexpr int kNbOff = kPermOff + kMaxVarlenB * 4;
+    static constexpr int kBytes = kNbOff + kMaxVarlenB * 4;
     static constexpr int kAlloc = kBytes + 1024;                   // slack for 1024-byte alignment
 };
 
@@ -106,7 +112,7 @@ __device__ int g_timeline_n[5];
 
 // Packed sequence b: first token and length. Offsets outside [0, Nq] (total packed
 // query rows) or [0, Nk] (total key rows), or decreasing, make the sequence empty; the
-// prefix scan records that as a device error.
+// work-order build records that as a device error.
 __device__ __forceinline__ bool packed_seq(const FwdParams& p, int b, int& first, int& len) {
     const int a = __ldg(p.cu_seqlens + b), e = __ldg(p.cu_seqlens + b + 1);
     const bool ok = a >= 0 && e >= a && e <= p.Nq && e <= p.Nk;
@@ -115,37 +121,65 @@ __device__ __forceinline__ bool packed_seq(const FwdParams& p, int b, int& first
     return ok;
 }
 
+// Work order of packed sequences, built once per CTA in shared memory by build_packed_order.
+struct PackedOrder {
+    const int* pre;   // [B + 1] work tiles before the i-th sequence of perm (sequence-major order)
+    const int* lvl;   // lvl[j + 2] = work tiles at block levels above j (level order)
+    const int* perm;  // [B] sequences by 256-row block count, most first (stable)
+    int levels;       // > 0: level order over this many levels; 0: sequence-major order
+};
+
 // Map a work-tile index to its tile (a work tile is two consecutive 128-row Q tiles of one
 // (sequence, query head)). The order puts the heaviest tiles first so that the snake walk
 // below balances the persistent CTAs (longest-processing-time first; under a causal mask a
-// tile's cost grows with its query block index).
+// tile's cost grows with its query block index j, whatever the sequence).
 //   dense batches: sections of sec_q (batch, head) pairs, then query blocks, then the pairs
 //     of the section; sec_q is all pairs unless the problem spans many waves, where smaller
 //     sections keep the key/value heads being read together within the L2;
-//   packed sequences: sequences outermost, then sections of sec_q query heads, then query
-//     blocks, then the heads of the section.
-// The query heads of one key/value head are adjacent in both.
-__device__ __forceinline__ void get_tile(const FwdParams& p, const int* prefix, int w, Tile& t) {
-    int b, Lq, Lk, q0, k0, jj, h;
+//   packed sequences, causal: block levels j from the highest down, then the sequences that
+//     reach level j (longest first), then heads;
+//   packed sequences, no mask: sequences longest first, then sections of sec_q query heads,
+//     then query blocks, then the heads of the section.
+// The query heads of one key/value head are adjacent in all three.
+__device__ __forceinline__ void get_tile(const FwdParams& p, const PackedOrder& po, int w, Tile& t) {
+    int b, Lq, Lk, q0, k0, j, h;
     if (p.cu_seqlens) {
-        int lo = 0, hi = p.B;  // prefix[b] <= w < prefix[b+1]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (prefix[mid] <= w) lo = mid; else hi = mid;
+        int i;
+        if (po.levels > 0) {
+            int lo = 0, hi = po.levels - 1;  // smallest level j with lvl[j + 2] <= w
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (po.lvl[mid + 2] <= w) hi = mid; else lo = mid + 1;
+            }
+            j = lo;
+            const int k = w - po.lvl[j + 2];
+            i = k / p.Hq;
+            h = k - i * p.Hq;
+        } else {
+            int lo = 0, hi = p.B;  // pre[i] <= w < pre[i + 1]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (po.pre[mid] <= w) lo = mid; else hi = mid;
+            }
+            i = lo;
+            j = -1;
         }
-        b = lo;
-        const int u = w - prefix[b];
+        b = po.perm[i];
         int first, len;
         packed_seq(p, b, first, len);
         q0 = k0 = first;
         Lq = Lk = len;
-        const int nblk = cdiv(Lq, 2 * BM);
-        const int sec = p.sec_q;
-        const int per_sec = nblk * sec;
-        const int si = u / per_sec;
-        const int rem = u - si * per_sec;
-        jj = rem / sec;
-        h = si * sec + (rem - jj * sec);
+        if (j < 0) {
+            const int u = w - po.pre[i];
+            const int nblk = cdiv(Lq, 2 * BM);
+            const int sec = p.sec_q;
+            const int per_sec = nblk * sec;
+            const int si = u / per_sec;
+            const int rem = u - si * per_sec;
+            const int jj = rem / sec;
+            h = si * sec + (rem - jj * sec);
+            j = p.causal ? (nblk - 1 - jj) : jj;
+        }
     } else {
         Lq = p.Nq;
         Lk = p.Nk;
@@ -155,14 +189,14 @@ __device__ __forceinline__ void get_tile(const FwdParams& p, const int* prefix, 
         const int si = w / (sec * nblk);
         const int rem = w - si * (sec * nblk);
         const int len = min(sec, pairs - si * sec);  // the last section may be shorter
-        jj = rem / len;
+        const int jj = rem / len;
         const int pair = si * sec + (rem - jj * len);
         b = pair / p.Hq;
         h = pair - b * p.Hq;
         q0 = b * p.Nq;
         k0 = b * p.Nk;
+        j = p.causal ? (nblk - 1 - jj) : jj;
     }
-    const int j = p.causal ? (cdiv(Lq, 2 * BM) - 1 - jj) : jj;
     t.h = h;
     t.kvh = t.h / p.G;
     t.q0 = q0;
@@ -185,6 +219,97 @@ __device__ __forceinline__ void get_tile(const FwdParams& p, const int* prefix, 
         }
         t.n[s] = n;
     }
+}
+
+// Build the packed-sequence work order (one warp). Blocks per sequence nb = ceil(len / 256);
+// a counting sort by nb, stable so that every CTA derives the same order, gives perm.
+// Level order (causal, nb <= kMaxLevels): with c_j = #{sequences with nb > j}, level j holds
+// Hq * c_j tiles, and lvl[j + 2] = Hq * sum over levels above j of c. Returns the number of
+// levels (0 selects the sequence-major order) and the number of work tiles.
+__device__ void build_packed_order(const FwdParams& p, int* pre, int* lvl, int* perm, int* nbs, int lane,
+                                   int& levels, int& total) {
+    const int B = p.B;
+    int maxnb = 0;
+    for (int base = 0; base < B; base += 32) {
+        const int b = base + lane;
+        if (b < B) {
+            int first, len;
+            if (!packed_seq(p, b, first, len) && p.status && blockIdx.x == 0) atomicCAS(p.status, 0, kDevBadIndex);
+            nbs[b] = len > 0 ? cdiv(len, 2 * BM) : 0;
+            maxnb = max(maxnb, nbs[b]);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) maxnb = max(maxnb, __shfl_xor_sync(0xffffffffu, maxnb, o));
+    const bool sorted = maxnb <= kMaxLevels;
+    if (sorted) {
+        for (int v = lane; v <= maxnb + 1; v += 32) lvl[v] = 0;
+        __syncwarp();
+        for (int b = lane; b < B; b += 32) atomicAdd(&lvl[nbs[b]], 1);
+        __syncwarp();
+        // lvl[v] = #{nb > v}: exclusive suffix sums of the histogram, 32 values per pass from the top
+        int carry = 0;
+        for (int top = maxnb + 1; top >= 0; top -= 32) {
+            const int v = top - lane;
+            const int x = v >= 0 ? lvl[v] : 0;
+            int incl = x;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (v >= 0) lvl[v] = carry + incl - x;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+            __syncwarp();
+        }
+        // stable scatter; afterwards lvl[v] = #{nb >= v}
+        for (int base = 0; base < B; base += 32) {
+            const int b = base + lane;
+            const int v = b < B ? nbs[b] : -1;
+            const unsigned same = __match_any_sync(0xffffffffu, v);
+            const int rank = __popc(same & ((1u << lane) - 1u));
+            if (b < B) perm[lvl[v] + rank] = b;
+            __syncwarp();
+            if (b < B && rank == 0) lvl[v] += __popc(same);
+            __syncwarp();
+        }
+        // inclusive suffix sums times Hq: lvl[v] = Hq * sum_{u >= v} #{nb >= u}
+        carry = 0;
+        for (int top = maxnb + 1; top >= 0; top -= 32) {
+            const int v = top - lane;
+            const int x = v >= 0 ? lvl[v] : 0;
+            int incl = x;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (v >= 0) lvl[v] = p.Hq * (carry + incl);
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+            __syncwarp();
+        }
+    } else {
+        for (int b = lane; b < B; b += 32) perm[b] = b;
+        __syncwarp();
+    }
+    // sequence-major prefix over perm
+    int carry = 0;
+    for (int base = 0; base < B; base += 32) {
+        const int i = base + lane;
+        const int cnt = i < B ? p.Hq * nbs[perm[i]] : 0;
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (i < B) pre[i] = carry + incl - cnt;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) pre[B] = carry;
+    __syncwarp();
+    levels = (sorted && p.causal) ? maxnb : 0;
+    total = carry;
 }
 
 // The r-th work tile of this CTA: rounds of gridDim.x consecutive tiles, walked in
@@ -223,7 +348,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* st_l = st_m + 2 * BM;                                    // [2][128]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-    int* prefix = reinterpret_cast<int*>(smem + L::kPrefixOff);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -257,29 +381,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
-    // Work-tile prefix over packed sequences (warp 2, 32-wide scan).
-    int total = p.total_tiles;
-    if (p.cu_seqlens) {
-        if (warp == 2) {
-            int carry = 0;
-            for (int base = 0; base < p.B; base += 32) {
-                const int b = base + lane;
-                int cnt = 0;
-                if (b < p.B) {
-                    int first, len;
-                    if (!packed_seq(p, b, first, len) && p.status && blockIdx.x == 0) atomicCAS(p.status, 0, kDevBadIndex);
-                    cnt = len > 0 ? p.Hq * cdiv(len, 2 * BM) : 0;
-                }
-                int incl = cnt;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                if (b < p.B) prefix[b] = carry + incl - cnt;
-                carry += __shfl_sync(0xffffffffu, incl, 31);
-            }
-            if (lane == 0) prefix[p.B] = carry;
+    // Work order over packed sequences (warp 2).
+    int* misc = reinterpret_cast<int*>(smem + L::kMiscOff);
+    int* pre = reinterpret_cast<int*>(smem + L::kPreOff);
+    int* lvl = reinterpret_cast<int*>(smem + L::kLvlOff);
+    int* perm = reinterpret_cast<int*>(smem + L::kPermOff);
+    if (p.cu_seqlens && warp == 2) {
+        int levels, tiles;
+        build_packed_order(p, pre, lvl, perm, reinterpret_cast<int*>(smem + L::kNbOff), lane, levels, tiles);
+        if (lane == 0) {
+            misc[2] = levels;
+            misc[3] = tiles;
         }
     }
     if (warp == 1) {
@@ -289,7 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (p.cu_seqlens) total = prefix[p.B];
+    int total = p.total_tiles;
+    const PackedOrder po{pre, lvl, perm, p.cu_seqlens ? misc[2] : 0};
+    if (p.cu_seqlens) total = misc[3];
     const uint32_t tmem = *tmem_slot;
     const uint64_t wd = p.watchdog_ns;
 
@@ -309,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int w = snake_index(r);
             if (w >= total) continue;
             Tile t;
-            get_tile(p, prefix, w, t);
+            get_tile(p, po, w, t);
             const int nmax = max(t.n[0], t.n[1]);
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
@@ -393,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int w = snake_index(r);
             if (w >= total) continue;
             Tile t;
-            get_tile(p, prefix, w, t);
+            get_tile(p, po, w, t);
             const int nmax = max(t.n[0], t.n[1]);
             const int ns = s ? t.n[1] : t.n[0];
             if (nmax == 0) continue;
@@ -476,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int w = snake_index(r);
             if (w >= total) continue;
             Tile t;
-            get_tile(p, prefix, w, t);
+            get_tile(p, po, w, t);
             const int ns = s ? t.n[1] : t.n[0];
             if (ns == 0) continue;
             const int tile_row0 = t.r0 + s * BM;
@@ -599,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int w = snake_index(r);
             if (w >= total) continue;
             Tile t;
-            get_tile(p, prefix, w, t);
+            get_tile(p, po, w, t);
             for (int s = 0; s < 2; ++s) {
                 const int qrow = t.r0 + s * BM + row;
                 if (t.r0 + s * BM >= t.Lq) continue;

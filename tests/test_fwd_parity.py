@@ -79,6 +79,11 @@ SMALL = [
     case("sharp", 1, 4, 4, 1024, 1024, 128, True, 12, 4.0),         # large scores: many rescales
     case("varlen_small", 0, 4, 2, 0, 0, 128, True, 13, lens=[1, 129, 0, 256, 257, 5, 600]),
     case("varlen_d64_nc", 0, 2, 2, 0, 0, 64, False, 14, lens=[300, 17, 128]),
+    # more than 32 sequences (several passes of the work-order build), empties and equal lengths
+    case("varlen_many_causal", 0, 2, 1, 0, 0, 64, True, 16,
+         lens=[int(x) % 7 * 97 for x in synth.uniform_ints(75, 16, 0, 1 << 20)]),
+    case("varlen_many_nc", 0, 2, 2, 0, 0, 64, False, 17,
+         lens=[int(x) for x in synth.uniform_ints(40, 17, 0, 640)]),
 ]
 
 
