@@ -8,14 +8,17 @@
 // One persistent CTA per SM walks a list of work tiles (sequence, query head,
 // 256-row query block = two 128-row Q tiles). Warp roles (16 warps):
 //   warp 0       TMA producer: Q tiles once per work tile, then a ring of K/V tiles
-//   warp 1       MMA issuer: S = Q K^T and O += P V with tcgen05.mma, accumulators in
-//                tensor memory; owns the TMEM allocation
+//   warps 1-2    MMA issuers, one per Q tile: S = Q K^T and O += P V with tcgen05.mma,
+//                accumulators in tensor memory; warp 1 owns the TMEM allocation
 //   warps 4-7    softmax for Q tile 0, warps 8-11 softmax for Q tile 1: one thread per
 //                row reads S from TMEM, masks, takes the row max, decides whether to
 //                rescale O (warp-uniform, only when the max grew by more than the
 //                threshold), computes exponentials (MUFU ex2 and, optionally, a cubic
 //                polynomial on the FMA pipes for a fraction of columns), row sums, and
-//                writes P as bf16 into TMEM over S
+//                writes P as bf16 into TMEM over S in two stages (keys 0-95, then 96-127),
+//                each signalled at once, so that O += P V starts on the first three
+//                quarters while the last quarter is computed ("Low-precision FA4"
+//                section 2.1.1)
 //   warps 12-15  epilogue: O / l, LSE, bf16 store of finished rows
 // The GEMM issue order per KV step follows the two-tile ping-pong of
 // "Low-precision FA4" section 2.1.1 (S0 = Q0 K0, S1 = Q1 K0; then O0 += P0 V_n,
@@ -62,7 +65,8 @@ struct Layout {
     static constexpr int bQFull = 0, bQEmpty = 2, bEFull = 4, bEEmpty = 4 + kEntries;
     static constexpr int bSFull = 4 + 2 * kEntries, bPFull = bSFull + 2, bOFull = bSFull + 4, bOEmpty = bSFull + 6;
     static constexpr int bStats = bSFull + 8, bDrain = bSFull + 10, bIssued = bSFull + 12;
-    static constexpr int kNumBars = bIssued + 2;
+    static constexpr int bPRest = bSFull + 14;  // P stage 2 (keys 96-127); bPFull is stage 1
+    static constexpr int kNumBars = bPRest + 2;
     static constexpr int kStatsOff = kBarOff + ((kNumBars * 8 + 15) / 16) * 16;
     static constexpr int kMiscOff = kStatsOff + 2 * 2 * BM * 4;   // m[2][128], l[2][128]
     // misc: tmem base, abort flag, packed-order levels, packed work tiles
@@ -365,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[L::bSFull + s], 1);
             mbar_init(&bars[L::bPFull + s], 4);
+            mbar_init(&bars[L::bPRest + s], 4);
             mbar_init(&bars[L::bOFull + s], 1);
             mbar_init(&bars[L::bOEmpty + s], 4);
             mbar_init(&bars[L::bStats + s], 4);
@@ -407,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const uint64_t wd = p.watchdog_ns;
 
-    // Register split per warpgroup: producer/MMA 80, softmax 176 each, epilogue 72
-    // (sum 504 <= 4 x 128, the registers the CTA is launched with).
+    // Register split per warpgroup: producer/MMA 80, softmax 184 each, epilogue 64
+    // (sum 512 = 4 x 128, the registers the CTA is launched with).
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
     if (warp == 0) {
@@ -524,7 +529,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = warp_wait(&bars[L::bEFull + e_slot], e_par, abort_flag, wd))) break;
                 if (do_pv) {
                     if (!(ok = warp_wait(&bars[L::bPFull + s], pf, abort_flag, wd))) break;
-                    pf ^= 1u;
                     if (n - 1 == 0) {
                         if (!(ok = warp_wait(&bars[L::bOEmpty + s], oe ^ 1u, abort_flag, wd))) break;
                         oe ^= 1u;
@@ -543,9 +547,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t vd = dv0 + (uint64_t)((ent_off + L::kKVBytes) >> 4);
                     const uint32_t acc0 = n - 1 > 0 ? 1u : 0u;
 #pragma unroll
-                    for (int k = 0; k < BN / 16; ++k)
+                    for (int k = 0; k < 6; ++k)  // keys 0-95: P stage 1
                         tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO,
                                      k == 0 ? acc0 : 1u);
+                    if (!(ok = warp_wait(&bars[L::bPRest + s], pf, abort_flag, wd))) break;
+                    pf ^= 1u;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 6; k < BN / 16; ++k)  // keys 96-127: P stage 2
+                        tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO, 1u);
                 }
                 if (do_s) {
                     const uint64_t kd = dk0 + (uint64_t)(ent_off >> 4);
@@ -575,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     } else if (warp < 12) {
         // ------------------------------------------------------------------ softmax
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
         const int s = (warp - 4) >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
@@ -656,11 +666,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++c_dec;
                 const float neg = (m == -INFINITY) ? 0.0f : -m * sl2;
-                // exponent arguments two at a time (packed FMA), exponentials, packed row sums
+                // exponent arguments two at a time (packed FMA), exponentials, packed row sums;
+                // P goes out in two stages (keys 0-95, then 96-127)
                 float sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
                 uint32_t pk[64];
-#pragma unroll
-                for (int c = 0; c < BN; c += 2) {
+                auto exp_pair = [&](int c) {
                     float x0, x1;
                     ffma2(x0, x1, sv[c], sv[c + 1], sl2, sl2, neg, neg);
                     float p0, p1;
@@ -674,14 +684,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int a = ((c >> 1) & 3) * 2;
                     fadd2(sum[a], sum[a + 1], sum[a], sum[a + 1], p0, p1);
                     pk[c >> 1] = pack_bf16x2(p0, p1);
-                }
+                };
+#pragma unroll
+                for (int c = 0; c < 3 * BN / 4; c += 2) exp_pair(c);
                 tmem_st32(tS + 0, &pk[0]);
-                tmem_st32(tS + 32, &pk[32]);
-                l += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+                tmem_st16(tS + 32, &pk[32]);
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[L::bPFull + s]);
+#pragma unroll
+                for (int c = 3 * BN / 4; c < BN; c += 2) exp_pair(c);
+                tmem_st16(tS + 48, &pk[48]);
+                l += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[L::bPRest + s]);
                 if (quarter == 0) ATTN_TL(2 + s, n, ts0, ts1, clock64());
             }
             if (!ok) break;
@@ -703,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------------ epilogue
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
