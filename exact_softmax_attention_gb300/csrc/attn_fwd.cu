@@ -17,8 +17,9 @@
 //                polynomial on the FMA pipes for a fraction of columns), row sums, and
 //                writes P as bf16 into TMEM over S in two stages (keys 0-95, then 96-127),
 //                each signalled at once, so that O += P V starts on the first three
-//                quarters while the last quarter is computed ("Low-precision FA4"
-//                section 2.1.1)
+//                quarters while the last quarter is computed ("FlashAttention-4:
+//                Blackwell algorithm-pipeline co-design", section on warp roles and
+//                barriers; "FlashAttention4 精读", P staging)
 //   warps 12-15  epilogue: O / l, LSE, bf16 store of finished rows
 // The GEMM issue order per KV step follows the two-tile ping-pong of
 // "Low-precision FA4" section 2.1.1 (S0 = Q0 K0, S1 = Q1 K0; then O0 += P0 V_n,
