@@ -12,6 +12,12 @@ Contents
     (formula and online-softmax equivalence) and section 03 (LSE output); paged
     decode per "Faster, more flexible FA4 for LLM inference" (PR 1999/2104 page
     gathering, PR 1940 split-KV), with the page table resolved first.
+``attn_decode_paged_fp8`` / ``fp8_values``
+    Paged decode over 8-bit floating-point caches ("Faster, more flexible FA4
+    for LLM inference", PR 2109: e4m3 or e5m2 inputs). The codes are decoded
+    from the OCP 8-bit floating-point definitions and multiplied by one descale
+    factor per tensor (a reading: the pages fix no scaling scheme), then the
+    same three-pass definition runs in float64.
 ``online_attention``
     The streaming recurrence of "FlashAttention: not computing less, moving
     less", section 02 (running max m, sum l, unnormalised accumulator a,
@@ -29,7 +35,9 @@ Readings of the pages taken here (the pages are silent or garbled):
  * LSE is the natural log of the sum of exp of the *scaled* scores;
  * query head h uses key/value head h // (Hq // Hkv);
  * the rescale threshold "256" is a factor on the exponentials, i.e.
-   tau = log2(256) = 8 in the base-2 exponent domain.
+   tau = log2(256) = 8 in the base-2 exponent domain;
+ * an FP8 cache holds one descale factor per tensor: code c stands for
+   descale * fp8(c).
 
 Every function here is pinned by tests against values the pages print, closed
 forms, invariants and an independent library routine (see ``tests/test_oracle.py``).
@@ -76,6 +84,10 @@ def _load():
             lib.oracle_attn_fwd.restype = i
             lib.oracle_attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, d, i]
             lib.oracle_attn_decode_paged.restype = i
+            lib.oracle_attn_decode_paged_fp8.argtypes = [vp, vp, vp, i, d, d, vp, vp, i, vp, vp, i, i, i, i, i, d, i]
+            lib.oracle_attn_decode_paged_fp8.restype = i
+            lib.oracle_fp8_values.argtypes = [vp, vp, i64, i]
+            lib.oracle_fp8_values.restype = None
             lib.oracle_exp2_poly.argtypes = [ctypes.c_float]
             lib.oracle_exp2_poly.restype = ctypes.c_float
             lib.oracle_floor_magic.argtypes = [ctypes.c_float]
@@ -144,6 +156,37 @@ def attn_decode_paged(q, k_cache, v_cache, page_table, seqlens, page_size, B, Hq
                                           B, Hq, Hkv, d, max_pages, float(scale), n_threads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle_attn_decode_paged rejected its arguments (rc={rc})")
+    return o, lse
+
+
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
+
+
+def fp8_values(codes, fmt: str) -> np.ndarray:
+    """float64 values of FP8 codes (OCP e4m3 or e5m2), as decoded by the oracle."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_fp8_values(c.ctypes.data, out.ctypes.data, c.size, FP8_FORMATS[fmt])
+    return out
+
+
+def attn_decode_paged_fp8(q, k_cache, v_cache, fmt, k_descale, v_descale, page_table, seqlens, page_size, B, Hq,
+                          Hkv, d, max_pages, scale, n_threads=None):
+    """Single-query paged attention in float64 over FP8 caches: q bf16 [B, Hq, d]; caches
+    FP8 codes [pages, page_size, Hkv, d] standing for descale * fp8(code)."""
+    q = _u16(q, "q")
+    kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seqlens, dtype=np.int32)
+    o = np.zeros((B, Hq, d), dtype=np.float64)
+    lse = np.zeros((B, Hq), dtype=np.float64)
+    rc = _load().oracle_attn_decode_paged_fp8(q.ctypes.data, kc.ctypes.data, vc.ctypes.data, FP8_FORMATS[fmt],
+                                              float(k_descale), float(v_descale), pt.ctypes.data, sl.ctypes.data,
+                                              page_size, o.ctypes.data, lse.ctypes.data, B, Hq, Hkv, d, max_pages,
+                                              float(scale), n_threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_attn_decode_paged_fp8 rejected its arguments (rc={rc})")
     return o, lse
 
 

@@ -274,3 +274,138 @@ int oracle_attn_decode_paged(const uint16_t* q, const uint16_t* k_cache, const u
     run_threads(dec_worker, &J, n_threads < B ? n_threads : B);
     return J.status;
 }
+
+/* ------------------------------------------------------------------ FP8 key/value caches */
+
+/*
+ * 8-bit floating-point caches ("Faster, more flexible FA4 for LLM inference", PR 2109:
+ * inputs in 8-bit floating point with four or five exponent bits, e4m3 or e5m2). The
+ * pages fix no scaling scheme; the reading taken is one descale factor per tensor: the
+ * cached key with code c stands for k_descale * fp8(c), and likewise for values. fp8(c)
+ * follows the OCP 8-bit floating-point definitions:
+ *   fmt 0, e4m3: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is
+ *                subnormal, m/8 * 2^-6; S.1111.111 is NaN; no infinities (largest 448);
+ *   fmt 1, e5m2: sign, 5 exponent bits (bias 15), 2 mantissa bits; exponent 0 is
+ *                subnormal, m/4 * 2^-14; exponent 31 is infinity (m = 0) or NaN.
+ * The attention is the same three-pass definition, on these values in float64.
+ */
+double oracle_fp8_value(uint8_t c, int fmt) {
+    const int neg = c >> 7;
+    double v;
+    if (fmt == 0) {
+        const int e = (c >> 3) & 15, m = c & 7;
+        if (e == 15 && m == 7) return NAN;
+        v = e == 0 ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+    } else {
+        const int e = (c >> 2) & 31, m = c & 3;
+        if (e == 31) return m == 0 ? (neg ? -INFINITY : INFINITY) : NAN;
+        v = e == 0 ? ldexp(m / 4.0, -14) : ldexp(1.0 + m / 4.0, e - 15);
+    }
+    return neg ? -v : v;
+}
+
+void oracle_fp8_values(const uint8_t* c, double* out, int64_t n, int fmt) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_fp8_value(c[i], fmt);
+}
+
+/* One query row (float64) against n keys/values given as float64 rows of stride `stride`. */
+static void attend_row_f64(const double* qd, const double* k, const double* v, int64_t stride, int64_t n, int d,
+                           double scale, double* s, double* o, double* lse) {
+    if (n <= 0) {
+        for (int c = 0; c < d; ++c) o[c] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    for (int64_t j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c) acc += qd[c] * k[j * stride + c];
+        s[j] = scale * acc;
+    }
+    double m = s[0];
+    for (int64_t j = 1; j < n; ++j)
+        if (s[j] > m) m = s[j];
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j) l += exp(s[j] - m);
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        const double p = exp(s[j] - m) / l;
+        for (int c = 0; c < d; ++c) o[c] += p * v[j * stride + c];
+    }
+    *lse = m + log(l);
+}
+
+typedef struct {
+    const uint16_t* q;
+    const uint8_t *kc, *vc;
+    int fmt;
+    double k_descale, v_descale;
+    const int32_t *page_table, *seqlens;
+    int page_size, B, Hq, Hkv, d, max_pages;
+    double scale;
+    double *o, *lse;
+    int64_t next;
+    int status;
+} dec8_job_t;
+
+static void* dec8_worker(void* p) {
+    dec8_job_t* J = (dec8_job_t*)p;
+    const int d = J->d, Hkv = J->Hkv, G = J->Hq / J->Hkv;
+    for (;;) {
+        const int64_t b = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
+        if (b >= J->B) break;
+        const int64_t L = J->seqlens[b];
+        if (L < 0 || L > (int64_t)J->max_pages * J->page_size) {
+            __atomic_store_n(&J->status, -3, __ATOMIC_RELAXED);
+            continue;
+        }
+        /* gather and widen this sequence's cached rows, [L, Hkv, d] */
+        const size_t row_elems = (size_t)Hkv * d, n = (size_t)(L > 0 ? L : 1) * row_elems;
+        double* kb = (double*)malloc(sizeof(double) * n);
+        double* vb = (double*)malloc(sizeof(double) * n);
+        double* s = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        double* qd = (double*)malloc(sizeof(double) * (size_t)d);
+        if (!kb || !vb || !s || !qd) {
+            __atomic_store_n(&J->status, -2, __ATOMIC_RELAXED);
+            free(kb); free(vb); free(s); free(qd);
+            continue;
+        }
+        for (int64_t t = 0; t < L; ++t) {
+            const int64_t page = J->page_table[b * J->max_pages + t / J->page_size];
+            const size_t src = (size_t)(page * J->page_size + t % J->page_size) * row_elems;
+            for (size_t e = 0; e < row_elems; ++e) {
+                kb[(size_t)t * row_elems + e] = J->k_descale * oracle_fp8_value(J->kc[src + e], J->fmt);
+                vb[(size_t)t * row_elems + e] = J->v_descale * oracle_fp8_value(J->vc[src + e], J->fmt);
+            }
+        }
+        for (int h = 0; h < J->Hq; ++h) {
+            const int g = h / G;
+            for (int c = 0; c < d; ++c) qd[c] = bf16d(J->q[(b * J->Hq + h) * d + c]);
+            attend_row_f64(qd, kb + (size_t)g * d, vb + (size_t)g * d, (int64_t)row_elems, L, d, J->scale, s,
+                           J->o + (b * J->Hq + h) * d, J->lse + b * J->Hq + h);
+        }
+        free(kb); free(vb); free(s); free(qd);
+    }
+    return NULL;
+}
+
+/*
+ * Paged decode over FP8 caches. q: bf16 [B, Hq, d]; k_cache, v_cache: FP8 codes
+ * [num_pages, page_size, Hkv, d]; fmt 0 = e4m3, 1 = e5m2; the rest as for
+ * oracle_attn_decode_paged.
+ */
+int oracle_attn_decode_paged_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_cache, int fmt,
+                                 double k_descale, double v_descale, const int32_t* page_table,
+                                 const int32_t* seqlens, int page_size, double* o, double* lse, int B, int Hq,
+                                 int Hkv, int d, int max_pages, double scale, int n_threads) {
+    if (!q || !k_cache || !v_cache || !page_table || !seqlens || !o || !lse) return -1;
+    if (fmt != 0 && fmt != 1) return -1;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || page_size <= 0 || max_pages < 0) return -1;
+    dec8_job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.kc = k_cache; J.vc = v_cache; J.fmt = fmt; J.k_descale = k_descale; J.v_descale = v_descale;
+    J.page_table = page_table; J.seqlens = seqlens; J.page_size = page_size; J.B = B; J.Hq = Hq; J.Hkv = Hkv;
+    J.d = d; J.max_pages = max_pages; J.scale = scale; J.o = o; J.lse = lse;
+    if (B == 0) return 0;
+    run_threads(dec8_worker, &J, n_threads < B ? n_threads : B);
+    return J.status;
+}

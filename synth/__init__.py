@@ -114,3 +114,38 @@ def f32_to_bf16(x) -> np.ndarray:
 def bf16_to_f32(h: np.ndarray) -> np.ndarray:
     """Exact widening of bf16 bit patterns to float32."""
     return (np.asarray(h, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# ----------------------------------------------------------------------------- FP8 inputs
+# The OCP 8-bit floating-point formats, used to lay out 8-bit key/value caches:
+#   e4m3: 4 exponent bits (bias 7), 3 mantissa bits, no infinities, S.1111.111 is NaN
+#   e5m2: 5 exponent bits (bias 15), 2 mantissa bits, exponent 31 is infinity or NaN
+_FP8_FORMATS = {"e4m3": (3, 7), "e5m2": (2, 15)}
+FP8_MAX = {"e4m3": 448.0, "e5m2": 57344.0}
+
+
+def _fp8_finite_values(fmt: str) -> np.ndarray:
+    """Values of the non-negative finite codes 0, 1, 2, ... of ``fmt`` (ascending with the code)."""
+    m_bits, bias = _FP8_FORMATS[fmt]
+    codes = np.arange(128, dtype=np.int64)
+    e = codes >> m_bits
+    m = (codes & ((1 << m_bits) - 1)).astype(np.float64) / (1 << m_bits)
+    val = np.where(e == 0, m * 2.0 ** (1 - bias), (1.0 + m) * np.exp2((e - bias).astype(np.float64)))
+    n_finite = 127 if fmt == "e4m3" else 124
+    return val[:n_finite]
+
+
+def fp8_encode(x, fmt: str) -> np.ndarray:
+    """Round values to FP8 codes (uint8): nearest, ties to the even code, saturating at the
+    largest finite value. Only lays out inputs; nothing reads these values but the kernels
+    and the oracle, each through its own decoding."""
+    v = _fp8_finite_values(fmt)
+    xs = np.asarray(x, dtype=np.float64)
+    a = np.abs(xs).ravel()
+    i = np.clip(np.searchsorted(v, a), 1, len(v) - 1)  # v[i-1] < a <= v[i] inside the range
+    lo, hi = v[i - 1], v[i]
+    up = (a - lo > hi - a) | ((a - lo == hi - a) & (i % 2 == 0))
+    code = np.where(up, i, i - 1)
+    code = np.where(a >= v[-1], len(v) - 1, code)
+    sign = np.signbit(xs).ravel().astype(np.uint8) << 7
+    return (code.astype(np.uint8) | sign).reshape(xs.shape)

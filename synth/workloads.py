@@ -11,6 +11,8 @@ Recipes (inputs i.i.d. N(0,1) rounded to bf16 unless stated):
   varlen_gqa  8 packed sequences, lengths U[512, 4096], Hq=32, Hkv=8, d=128, causal
   decode      B=64, Hq=32, Hkv=8, d=128, lengths U[1024, 32768], page_size=16,
               physical pages placed by a seeded permutation of the pool
+  decode_fp8  the decode workload with e4m3 key/value caches: the same N(0,1) draws,
+              divided by a per-tensor descale (max |x| / 448) and rounded to e4m3
 Seeds are ``20261202 + index`` in that order; each tensor draws from its own sub-stream.
 """
 from __future__ import annotations
@@ -20,7 +22,7 @@ import math
 
 import numpy as np
 
-from . import normal_bf16, permutation, sub_seed, uniform_ints
+from . import FP8_MAX, bf16_to_f32, fp8_encode, normal_bf16, permutation, sub_seed, uniform_ints
 
 BASE_SEED = 20261202
 
@@ -98,6 +100,7 @@ class DecodeCase:
     scale: float
     seed: int
     extra_pages: int = 0  # unreferenced pool pages (for canary tests)
+    kv_fmt: str = "bf16"  # cache element format: "bf16", or FP8 "e4m3" / "e5m2"
 
     @property
     def pages_per_seq(self) -> np.ndarray:
@@ -127,6 +130,22 @@ class DecodeCase:
         vc = normal_bf16(shape, sub_seed(self.seed, _V))
         return q, kc, vc, self.page_table(), self.seqlens.copy()
 
+    def generate_fp8(self):
+        """(q, k_cache, v_cache (uint8 FP8 codes), page_table, seqlens, k_descale, v_descale).
+
+        The cache values are the bf16 case's draws divided by a per-tensor descale
+        (max |x| / largest finite FP8 value, as float32) and rounded to FP8, so that the
+        cached key with code c stands for k_descale * fp8(c)."""
+        q, kc, vc, pt, sl = self.generate()
+        out = []
+        for c in (kc, vc):
+            x = bf16_to_f32(c).astype(np.float64)
+            amax = float(np.abs(x).max()) if x.size else 0.0
+            ds = np.float32(amax / FP8_MAX[self.kv_fmt]) if amax > 0 else np.float32(1.0)
+            out.append((fp8_encode(x / float(ds), self.kv_fmt), float(ds)))
+        (kc8, kds), (vc8, vds) = out
+        return q, kc8, vc8, pt, sl, kds, vds
+
     def flops(self) -> int:
         return 4 * self.d * self.Hq * int(self.seqlens.astype(np.int64).sum())
 
@@ -134,7 +153,8 @@ class DecodeCase:
         """Algorithmic HBM bytes: every cached K and V row of every sequence once, q, o, lse,
         the page-table entries in use and seqlens. Split-KV workspace traffic is not counted."""
         L = self.seqlens.astype(np.int64)
-        kv = int(L.sum()) * self.Hkv * self.d * 2 * 2
+        elem = 2 if self.kv_fmt == "bf16" else 1
+        kv = int(L.sum()) * self.Hkv * self.d * elem * 2
         qo = 2 * self.B * self.Hq * self.d * 2
         lse = self.B * self.Hq * 4
         pt = int(self.pages_per_seq.sum()) * 4
@@ -173,6 +193,11 @@ def decode() -> DecodeCase:
     seed = BASE_SEED + 4
     lens = uniform_ints(64, sub_seed(seed, _LEN), 1024, 32768)
     return DecodeCase("decode", 64, 32, 8, 128, 16, lens, 32768 // 16, 1.0 / math.sqrt(128), seed)
+
+
+def decode_fp8() -> DecodeCase:
+    c = decode()
+    return dataclasses.replace(c, name="decode_fp8", kv_fmt="e4m3")
 
 
 def all_prefill():

@@ -348,6 +348,76 @@ def test_decode_ignores_unreferenced_nan_pages():
     assert np.isfinite(o).all() and np.isfinite(lse).all()
 
 
+# --------------------------------------------------------------- FP8 caches
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_codes_match_torch_float8(fmt):
+    """All 256 codes against PyTorch's float8 types (an independent decoder), plus values
+    the OCP definitions fix."""
+    codes = np.arange(256, dtype=np.uint8)
+    a = oracle.fp8_values(codes, fmt)
+    td = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+    b = torch.from_numpy(codes).view(td).double().numpy()
+    assert ((a == b) | (np.isnan(a) & np.isnan(b))).all()
+    spot = {"e4m3": {0x7E: 448.0, 0x01: 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0xB8: -1.0, 0x00: 0.0},
+            "e5m2": {0x7B: 57344.0, 0x7C: math.inf, 0xFC: -math.inf, 0x01: 2.0 ** -16, 0x3C: 1.0, 0x04: 2.0 ** -14}}
+    for c, v in spot[fmt].items():
+        assert oracle.fp8_values(np.array([c], dtype=np.uint8), fmt)[0] == v
+    assert np.isnan(a).sum() == (2 if fmt == "e4m3" else 6)
+
+
+def _small_fp8_decode(fmt, seed=31, extra_pages=0, page_size=16):
+    c = _small_decode(seed=seed, extra_pages=extra_pages, page_size=page_size)
+    return W.DecodeCase(c.name, c.B, c.Hq, c.Hkv, c.d, c.page_size, c.seqlens, c.max_pages, c.scale, c.seed,
+                        extra_pages=extra_pages, kv_fmt=fmt)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_decode_equals_bf16_decode_of_the_same_values(fmt):
+    """With a power-of-two descale every cached value is exact in bf16, so the FP8 oracle
+    must reproduce the (separately pinned) bf16 decode oracle on those values."""
+    c = _small_fp8_decode(fmt)
+    q, kc8, vc8, pt, sl, _, _ = c.generate_fp8()
+    kds, vds = 0.125, 4.0
+    kc = synth.f32_to_bf16(kds * oracle.fp8_values(kc8, fmt))
+    vc = synth.f32_to_bf16(vds * oracle.fp8_values(vc8, fmt))
+    assert (synth.bf16_to_f32(kc) == kds * oracle.fp8_values(kc8, fmt)).all()
+    o8, l8 = oracle.attn_decode_paged_fp8(q, kc8, vc8, fmt, kds, vds, pt, sl, c.page_size, c.B, c.Hq, c.Hkv, c.d,
+                                          c.max_pages, c.scale)
+    o, lse = oracle.attn_decode_paged(q, kc, vc, pt, sl, c.page_size, c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.scale)
+    np.testing.assert_allclose(o8, o, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(l8, lse, rtol=1e-13, atol=1e-15)
+
+
+def test_fp8_descales_act_as_score_scale_and_value_scale():
+    """k_descale multiplies every score, exactly like the softmax scale; v_descale
+    multiplies the output and leaves the log-sum-exp alone."""
+    c = _small_fp8_decode("e4m3", seed=44)
+    q, kc8, vc8, pt, sl, _, _ = c.generate_fp8()
+    args = (pt, sl, c.page_size, c.B, c.Hq, c.Hkv, c.d, c.max_pages)
+    o1, l1 = oracle.attn_decode_paged_fp8(q, kc8, vc8, "e4m3", 0.37, 1.0, *args, c.scale)
+    o2, l2 = oracle.attn_decode_paged_fp8(q, kc8, vc8, "e4m3", 1.0, 1.0, *args, c.scale * 0.37)
+    # the two groupings of the product round differently: float64 reassociation only
+    np.testing.assert_allclose(o1, o2, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=1e-10, atol=1e-12)
+    o3, l3 = oracle.attn_decode_paged_fp8(q, kc8, vc8, "e4m3", 0.37, 2.5, *args, c.scale)
+    np.testing.assert_allclose(o3, 2.5 * o1, rtol=1e-10, atol=1e-12)
+    np.testing.assert_array_equal(l3, l1)
+
+
+def test_fp8_decode_ignores_unreferenced_nan_pages():
+    c = _small_fp8_decode("e4m3", seed=9, extra_pages=6)
+    q, kc8, vc8, pt, sl, kds, vds = c.generate_fp8()
+    used = np.zeros(c.num_pages, dtype=bool)
+    for b in range(c.B):
+        used[pt[b, : int(c.pages_per_seq[b])]] = True
+    kc8[~used] = 0x7F  # NaN in e4m3
+    vc8[~used] = 0x7F
+    o, lse = oracle.attn_decode_paged_fp8(q, kc8, vc8, "e4m3", kds, vds, pt, sl, c.page_size, c.B, c.Hq, c.Hkv,
+                                          c.d, c.max_pages, c.scale)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+
+
 # ----------------------------------------------------------------- exp2 model
 
 def test_exp2_cubic_error_table():

@@ -1,5 +1,6 @@
 """The seeded input generator: published splitmix64 values, rounding, determinism, recipes."""
 import numpy as np
+import pytest
 
 import synth
 from synth import workloads as W
@@ -64,3 +65,24 @@ def test_exact_work_counts():
     d = W.decode()
     assert d.bytes() == (int(d.seqlens.astype(np.int64).sum()) * 8 * 128 * 4 + 2 * 64 * 32 * 128 * 2
                          + 64 * 32 * 4 + int(d.pages_per_seq.sum()) * 4 + 64 * 4)
+
+
+def test_fp8_encoder_rounds_like_torch_and_saturates():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    for fmt, td in (("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)):
+        mx = synth.FP8_MAX[fmt]
+        x = np.concatenate([rng.standard_normal(50000) * mx / 8, rng.standard_normal(1000) * 1e-4, [0.0, -0.0, mx, -mx]])
+        x = np.clip(x, -mx, mx)
+        ours = synth.fp8_encode(x, fmt)
+        ref = torch.from_numpy(x).to(td).view(torch.uint8).numpy()
+        np.testing.assert_array_equal(ours, ref)
+        big = synth.fp8_encode(np.array([10 * mx, -10 * mx]), fmt)  # saturates at the largest finite code
+        assert list(big) == ([0x7E, 0xFE] if fmt == "e4m3" else [0x7B, 0xFB])
+
+
+def test_fp8_decode_workload_halves_the_cache_bytes():
+    from synth import workloads as W
+    bf, f8 = W.decode(), W.decode_fp8()
+    L = int(bf.seqlens.astype(np.int64).sum())
+    assert bf.bytes() - f8.bytes() == L * bf.Hkv * bf.d * 2
