@@ -10,6 +10,9 @@ A step is one pass of the whole hot path over one batch of synthetic input:
 visible (query, key) pair and head); the decode leg's HBM GB/s is reported under
 ``decode``. Both legs are timed with CUDA events on the stream they launch on;
 inputs are larger than L2, so no flush is needed between steps.
+After the timed steps, attn_decode_paged_fp8 runs the same decode workload with
+e4m3 key/value caches for as many timed calls; its GB/s (algorithmic bytes of the
+8-bit caches) is reported under ``decode_fp8``, outside ``value``.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 With --gpus N > 1 the script runs under torch.distributed.run, one rank per GPU,
@@ -40,6 +43,7 @@ from synth import workloads as W  # noqa: E402
 METRIC = "attn fwd TFLOP/s (bf16 hd128 causal) & paged-decode HBM GB/s vs roofline"
 FWD_KERNEL = "attn_fwd_kernel"
 DEC_KERNEL = "decode_split_kernel"
+DEC8_KERNEL = "decode_split_fp8_kernel"
 
 
 def parse():
@@ -68,7 +72,8 @@ def peaks():
 
 
 KERNEL_SOURCES = {FWD_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"],
-                  DEC_KERNEL: ["attn_decode.cu", "ptx.cuh", "kernels.cuh"]}
+                  DEC_KERNEL: ["attn_decode.cu", "ptx.cuh", "kernels.cuh"],
+                  DEC8_KERNEL: ["attn_decode.cu", "ptx.cuh", "kernels.cuh"]}
 
 
 def source_sha(kernel: str) -> str:
@@ -341,6 +346,18 @@ def run_ours(args):
     _, max_splits = A.attn_decode_plan(dc.B, dc.Hkv, dc.max_pages, dc.page_size, 0)
     launches_per_step = 1 + (2 if max_splits > 1 else 1)
 
+    # FP8 (e4m3) key/value caches of the same decode workload: a leg of its own, timed after
+    # the step
+    dc8 = W.decode_fp8()
+    _, kc8, vc8, _, _, kds, vds = dc8.generate_fp8()
+    with torch.cuda.stream(stream):
+        KC8, VC8 = torch.from_numpy(kc8).to(dev), torch.from_numpy(vc8).to(dev)
+    stream.synchronize()
+
+    def dec8():
+        A.attn_decode_paged_fp8(DQ, KC8, VC8, PT, SL, dc8.page_size, DO, DLSE, s_handle, dc8.B, dc8.Hq, dc8.Hkv,
+                                dc8.d, dc8.max_pages, dc8.num_pages, dc8.scale, 0, dc8.kv_fmt, kds, vds)
+
     def barrier():
         if world > 1:
             import torch.distributed as dist
@@ -381,6 +398,21 @@ def run_ours(args):
     total_ms = max_over_ranks(total_ms, world, dev)
     fwd_ms = max_over_ranks(fwd_ms, world, dev)
     dec_ms = max_over_ranks(dec_ms, world, dev)
+
+    # FP8 decode leg: warm-up, then the same number of timed calls
+    for _ in range(args.warmup):
+        dec8()
+    barrier()
+    s8, e8 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s8.record(stream)
+    for _ in range(K_):
+        dec8()
+    e8.record(stream)
+    barrier()
+    st = A.attn_get_device_status(s_handle)
+    if st != 0:
+        raise RuntimeError(f"device status after the FP8 decode leg: {A.status_string(st)}")
+    dec8_ms = max_over_ranks(s8.elapsed_time(e8), world, dev)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -440,6 +472,7 @@ def run_ours(args):
     dvalue = world * K_ * dc.bytes() / (dec_ms * 1e-3) / 1e9
     tr_f = ncu_traffic(FWD_KERNEL)
     tr_d = ncu_traffic(DEC_KERNEL)
+    d8_ach = dc8.bytes() / (dec8_ms / K_ * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K_, "warmup": args.warmup,
         "ms_per_step": total_ms / K_, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -454,6 +487,13 @@ def run_ours(args):
         "decode": {"value": dvalue, "unit": "GB/s", "ms_per_step": dec_ms / K_,
                    "roofline": {"bound": "hbm", "achieved": d_ach, "peak": hbm, "unit": "GB/s", "frac": d_ach / hbm,
                                 "traffic": tr_d, "kernel": DEC_KERNEL, "peak_source": f"{src} copy"}},
+        "decode_fp8": {"value": world * K_ * dc8.bytes() / (dec8_ms * 1e-3) / 1e9, "unit": "GB/s",
+                       "ms_per_call": dec8_ms / K_, "calls": K_, "gpu_launches": K_ * (launches_per_step - 1),
+                       "workload": "paged decode as above with e4m3 key/value caches (per-tensor descales)",
+                       "bytes_per_call": dc8.bytes(), "speedup_vs_bf16_decode": (dec_ms / K_) / (dec8_ms / K_),
+                       "roofline": {"bound": "hbm", "achieved": d8_ach, "peak": hbm, "unit": "GB/s",
+                                    "frac": d8_ach / hbm, "traffic": ncu_traffic(DEC8_KERNEL), "kernel": DEC8_KERNEL,
+                                    "peak_source": f"{src} copy"}},
         "prefill_ms_per_step": fwd_ms / K_,
         "gpu_launches": K_ * launches_per_step,
         "clocks": clk.summary(),

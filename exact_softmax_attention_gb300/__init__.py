@@ -29,8 +29,12 @@ ATTN_ERR_DEVICE_BAD_INDEX = -7
 ATTN_ERR_BAD_ARG = -8
 ATTN_ERR_SCRATCH_TOO_SMALL = -9
 
+ATTN_FP8_E4M3 = 0
+ATTN_FP8_E5M2 = 1
+FP8_FORMATS = {"e4m3": ATTN_FP8_E4M3, "e5m2": ATTN_FP8_E5M2}
+
 #: every symbol the header declares
-EXPORTS = ("attn_fwd", "attn_decode_paged", "attn_decode_paged_noalloc", "attn_decode_plan", "attn_status_string", "attn_get_device_status",
+EXPORTS = ("attn_fwd", "attn_decode_paged", "attn_decode_paged_fp8", "attn_decode_paged_noalloc", "attn_decode_plan", "attn_status_string", "attn_get_device_status",
            "attn_set_option", "attn_get_option", "attn_read_counters", "attn_debug_exp2", "attn_debug_watchdog",
            "attn_version")
 
@@ -51,6 +55,9 @@ lib.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i
 lib.attn_fwd.restype = _i
 lib.attn_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i]
 lib.attn_decode_paged.restype = _i
+lib.attn_decode_paged_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _f,
+                                       _f]
+lib.attn_decode_paged_fp8.restype = _i
 lib.attn_decode_paged_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i]
 lib.attn_decode_paged_noalloc.restype = _i
 lib.attn_decode_plan.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]
@@ -120,6 +127,19 @@ def attn_decode_paged(q, k_cache, v_cache, page_table, seqlens, page_size, o, ls
                                int(page_size), _ptr(o), _ptr(lse), _stream(stream), int(B), int(Hq), int(Hkv), int(d),
                                int(max_pages_per_seq), int(num_pages), float(scale), int(num_splits))
     return _check(rc, "attn_decode_paged", raise_on_error)
+
+
+def attn_decode_paged_fp8(q, k_cache, v_cache, page_table, seqlens, page_size, o, lse, stream, B, Hq, Hkv, d,
+                          max_pages_per_seq, num_pages, scale, num_splits=0, kv_format="e4m3", k_descale=1.0,
+                          v_descale=1.0, raise_on_error=True):
+    """Paged decode over FP8 key/value caches; see ``attn_decode_paged_fp8`` in include/attn.h.
+    ``kv_format`` is "e4m3" or "e5m2" (or the ATTN_FP8_* code)."""
+    fmt = FP8_FORMATS[kv_format] if isinstance(kv_format, str) else int(kv_format)
+    rc = lib.attn_decode_paged_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(seqlens),
+                                   int(page_size), _ptr(o), _ptr(lse), _stream(stream), int(B), int(Hq), int(Hkv),
+                                   int(d), int(max_pages_per_seq), int(num_pages), float(scale), int(num_splits), fmt,
+                                   float(k_descale), float(v_descale))
+    return _check(rc, "attn_decode_paged_fp8", raise_on_error)
 
 
 def attn_decode_paged_noalloc(q, k_cache, v_cache, page_table, seqlens, page_size, o, lse, stream, B, Hq, Hkv, d,

@@ -6,6 +6,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <float.h>
 #include <math.h>
 #include <mutex>
 #include <string.h>
@@ -280,9 +281,12 @@ attn_status_t attn_decode_plan(int B, int Hkv, int max_pages_per_seq, int page_s
     return ATTN_OK;
 }
 
-attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* page_table,
-                                const int* seqlens, int page_size, void* o, float* lse, void* stream, int B, int Hq,
-                                int Hkv, int d, int max_pages_per_seq, int num_pages, float scale, int num_splits) {
+// Shared body of the paged decode entry points. kv_format < 0: bf16 caches; 0 / 1: FP8
+// e4m3 / e5m2 caches with the given descales.
+static attn_status_t decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* page_table,
+                                  const int* seqlens, int page_size, void* o, float* lse, void* stream, int B, int Hq,
+                                  int Hkv, int d, int max_pages_per_seq, int num_pages, float scale, int num_splits,
+                                  int kv_format, float k_descale, float v_descale) {
     if (!q || !k_cache || !v_cache || !page_table || !seqlens || !o || !lse) return ATTN_ERR_NULL_PTR;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq / Hkv > 16 || (d != 64 && d != 128) || page_size <= 0 ||
         max_pages_per_seq <= 0 || num_pages <= 0 || num_splits < 0 || B > 65535 || Hkv > 65535)
@@ -317,9 +321,11 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
     p.num_pages = num_pages;
     p.chunk = chunk;
     p.max_splits = max_splits;
-    p.scale = scale;
-    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    const double score_scale = kv_format < 0 ? (double)scale : (double)scale * (double)k_descale;
+    p.scale = (float)score_scale;
+    p.scale_log2 = (float)(score_scale * 1.4426950408889634);
     p.rescale_thr = (float)opt.rescale_threshold;
+    p.v_descale = kv_format < 0 ? 1.0f : v_descale;
     p.status = ds->status;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     void* ws = nullptr;
@@ -345,9 +351,28 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
         p.ws_o = reinterpret_cast<float*>(ws);
         p.ws_lse = p.ws_o + n_o;
     }
-    const cudaError_t e = attn::launch_attn_decode(p, d, s);
+    const cudaError_t e = kv_format < 0 ? attn::launch_attn_decode(p, d, s) : attn::launch_attn_decode_fp8(p, d, kv_format, s);
     if (ws) cudaFreeAsync(ws, s);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* page_table,
+                                const int* seqlens, int page_size, void* o, float* lse, void* stream, int B, int Hq,
+                                int Hkv, int d, int max_pages_per_seq, int num_pages, float scale, int num_splits) {
+    return decode_paged(q, k_cache, v_cache, page_table, seqlens, page_size, o, lse, stream, B, Hq, Hkv, d,
+                        max_pages_per_seq, num_pages, scale, num_splits, -1, 1.0f, 1.0f);
+}
+
+attn_status_t attn_decode_paged_fp8(const void* q, const void* k_cache, const void* v_cache, const int* page_table,
+                                    const int* seqlens, int page_size, void* o, float* lse, void* stream, int B,
+                                    int Hq, int Hkv, int d, int max_pages_per_seq, int num_pages, float scale,
+                                    int num_splits, int kv_format, float k_descale, float v_descale) {
+    if (kv_format != ATTN_FP8_E4M3 && kv_format != ATTN_FP8_E5M2) return ATTN_ERR_BAD_ARG;
+    if (!isfinite(k_descale) || !isfinite(v_descale)) return ATTN_ERR_BAD_ARG;
+    const double score_scale_log2 = (double)scale * (double)k_descale * 1.4426950408889634;
+    if (!(fabs(score_scale_log2) <= (double)FLT_MAX)) return ATTN_ERR_BAD_ARG;  // the kernels use it as a float
+    return decode_paged(q, k_cache, v_cache, page_table, seqlens, page_size, o, lse, stream, B, Hq, Hkv, d,
+                        max_pages_per_seq, num_pages, scale, num_splits, kv_format, k_descale, v_descale);
 }
 
 attn_status_t attn_get_device_status(void* stream) {

@@ -46,6 +46,81 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
     return (uint32_t)(r * (D * 2) + ((c ^ (r & 7)) << 4));
 }
 
+// Merge the 4 warps' partial results of a split kernel (max-shifted LSE weighting) and
+// store: directly as bf16 o / lse when the sequence has one split, else as an fp32 partial
+// for the combine kernel. PERM_D: the accumulator rows follow the FP8 kernel's permuted d
+// order (row 16 mt + i of O^T holds d = (D/8) i + 2 mt, row 16 mt + i + 8 holds the next d);
+// otherwise row r holds d = r. out_scale multiplies the output (the value descale).
+template <int D, int GN, bool PERM_D>
+__device__ __forceinline__ void merge_and_store(const DecodeParams& p, uint8_t* smem, float (&oacc)[GN / 8][D / 16][4],
+                                                float m0, float m1, float l0, float l1, int split, int nsplit, int kvh,
+                                                int b, float out_scale) {
+    constexpr int NH = GN / 8;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g0 = lane >> 2;
+    const float sl2 = p.scale_log2;
+    // row sums over the quad
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    __syncthreads();  // every warp is done with its ring: reuse shared memory for the merge
+
+    // ---- merge the 4 warps: sm_o[w][head][d], sm_m[w][head], sm_l[w][head]
+    float* sm_o = reinterpret_cast<float*>(smem);
+    float* sm_m = sm_o + kWarps * GN * D;
+    float* sm_l = sm_m + kWarps * GN;
+    if ((lane & 3) == 0) {
+        sm_m[warp * GN + g0] = m0;
+        sm_l[warp * GN + g0] = l0;
+        if (GN == 16) {
+            sm_m[warp * GN + g0 + 8] = m1;
+            sm_l[warp * GN + g0 + 8] = l1;
+        }
+    }
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            const int hd = nh * 8 + 2 * (lane & 3);
+            const int dr0 = PERM_D ? (D / 8) * g0 + 2 * mt : mt * 16 + g0;
+            const int dr1 = PERM_D ? dr0 + 1 : dr0 + 8;
+            float* base = sm_o + (long long)warp * GN * D;
+            base[hd * D + dr0] = oacc[nh][mt][0];
+            base[(hd + 1) * D + dr0] = oacc[nh][mt][1];
+            base[hd * D + dr1] = oacc[nh][mt][2];
+            base[(hd + 1) * D + dr1] = oacc[nh][mt][3];
+        }
+    __syncthreads();
+
+    const bool direct = nsplit == 1;
+    for (int idx = threadIdx.x; idx < p.G * D; idx += blockDim.x) {
+        const int hh = idx / D, d = idx - hh * D;
+        float mm = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, sm_m[w * GN + hh]);
+        float ll = 0.0f, acc = 0.0f;
+        if (mm != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float sw = ex2_mufu((sm_m[w * GN + hh] - mm) * sl2);
+                ll += sw * sm_l[w * GN + hh];
+                acc += sw * sm_o[(w * GN + hh) * D + d];
+            }
+        }
+        const float o = ll > 0.0f ? acc / ll * out_scale : 0.0f;
+        const float lse = ll > 0.0f ? mm * p.scale + logf(ll) : -INFINITY;
+        const long long bh = (long long)b * p.Hq + kvh * p.G + hh;
+        if (direct) {
+            p.o[bh * D + d] = __float2bfloat16(o);
+            if (d == 0) p.lse[bh] = lse;
+        } else {
+            p.ws_o[(bh * p.max_splits + split) * D + d] = o;
+            if (d == 0) p.ws_lse[bh * p.max_splits + split] = lse;
+        }
+    }
+}
+
 template <int D, int GN, int NST>
 __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeParams p) {
     using L = DecLayout<D>;
@@ -249,65 +324,285 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeP
         }
     }
     cp_async_wait<0>();
-    // row sums over the quad
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    __syncthreads();  // every warp is done with its ring: reuse shared memory for the merge
+    merge_and_store<D, GN, false>(p, smem, oacc, m0, m1, l0, l1, split, nsplit, kvh, b, 1.0f);
+}
 
-    // ---- merge the 4 warps: sm_o[w][head][d], sm_m[w][head], sm_l[w][head]
-    float* sm_o = reinterpret_cast<float*>(smem);
-    float* sm_m = sm_o + kWarps * GN * D;
-    float* sm_l = sm_m + kWarps * GN;
-    if ((lane & 3) == 0) {
-        sm_m[warp * GN + g0] = m0;
-        sm_l[warp * GN + g0] = l0;
-        if (GN == 16) {
-            sm_m[warp * GN + g0 + 8] = m1;
-            sm_l[warp * GN + g0 + 8] = l1;
-        }
+// ---------------------------------------------------------------------------- FP8 caches
+// "Faster, more flexible FA4 for LLM inference", PR 2109: key/value caches in 8-bit floating
+// point, e4m3 or e5m2. Key code c stands for k_descale * fp8(c) and value code c for
+// v_descale * fp8(c) (one factor per tensor). The split kernel keeps the structure of the
+// bf16 one (per-warp cp.async rings of 16 tokens, GQA heads as MMA rows, online softmax,
+// warp merge) with three changes:
+//  - the products are f16 m16n8k16 MMAs. One cvt turns two cached codes into the f16 pair
+//    an operand register holds, exactly (every e4m3 and e5m2 value is an f16 value); the
+//    query is converted from bf16 to f16 once (exact for |q| in [2^-14, 65504]), and the
+//    probabilities are rounded to f16 instead of bf16;
+//  - the order of d inside Q K^T is permuted, identically in Q and K, and so is the order of
+//    d among the value rows (undone when the output is stored), so that the bytes of each
+//    lane's operands are contiguous in shared memory: one 16-byte load feeds several MMAs,
+//    without ldmatrix;
+//  - k_descale is folded into the softmax scale by the host; v_descale scales the output.
+
+// Byte offset of 16-byte chunk c of row r inside a [16 x D] byte warp-stage tile.
+template <int D>
+__device__ __forceinline__ uint32_t swz8(int r, int c) {
+    constexpr int kChunks = D / 16;
+    return (uint32_t)(r * D + ((c ^ (r & (kChunks - 1))) << 4));
+}
+
+// Two FP8 codes (low byte first) to an f16 pair (low half first).
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t two_codes) {
+    const uint16_t v = (uint16_t)two_codes;
+    uint32_t d;
+    if (FMT == 0)
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(v));
+    else
+        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(d) : "h"(v));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+    return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void lds128(uint32_t addr, uint32_t* w) {
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void lds64(uint32_t addr, uint32_t* w) {
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(addr) : "memory");
+}
+
+template <int D, int GN, int NST, int FMT>
+__global__ void __launch_bounds__(kWarps * 32) decode_split_fp8_kernel(const DecodeParams p) {
+    constexpr int kTile = kGroup * D;   // bytes of one K or V warp-stage tile
+    constexpr int kChunks = D / 16;     // 16-byte chunks per cache row
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long max_len = (long long)p.max_pages * p.page_size;
+
+    int len = __ldg(p.seqlens + b);
+    if (len < 0 || len > max_len) {
+        if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevBadIndex);
+        len = len < 0 ? 0 : (int)max_len;
     }
+    const int nsplit = cdiv(len, p.chunk);
+    const int t_begin = split * p.chunk;
+    if (len == 0) {
+        if (split == 0) {
+            for (int i = threadIdx.x; i < p.G * D; i += blockDim.x) {
+                const int h = kvh * p.G + i / D;
+                p.o[((long long)b * p.Hq + h) * D + (i % D)] = __float2bfloat16(0.0f);
+            }
+            if (threadIdx.x < p.G) p.lse[(long long)b * p.Hq + kvh * p.G + threadIdx.x] = -INFINITY;
+        }
+        return;
+    }
+    if (t_begin >= len) return;
+    const int t_end = min(len, t_begin + p.chunk);
+
+    // ---- query fragments (f16), rows = query heads of this kv head. Permuted d: column
+    // 2 qd + e of k-step kk is d = (D/4) qd + 4 kk + e, column 2 qd + 8 + e is that + 2.
+    const int g0 = lane >> 2, qd = lane & 3;
+    const int h0 = kvh * p.G + g0, h1 = kvh * p.G + g0 + 8;
+    const bool v0 = g0 < p.G, v1 = (GN == 16) && (g0 + 8 < p.G);
+    const uint32_t* q0p = reinterpret_cast<const uint32_t*>(p.q + ((long long)b * p.Hq + h0) * D);
+    const uint32_t* q1p = reinterpret_cast<const uint32_t*>(p.q + ((long long)b * p.Hq + h1) * D);
+    uint32_t aq[D / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const int c = (D / 8) * qd + 2 * kk;  // u32 index of d = (D/4) qd + 4 kk
+        aq[kk][0] = v0 ? bf16x2_to_f16x2(__ldg(q0p + c)) : 0u;
+        aq[kk][1] = v1 ? bf16x2_to_f16x2(__ldg(q1p + c)) : 0u;
+        aq[kk][2] = v0 ? bf16x2_to_f16x2(__ldg(q0p + c + 1)) : 0u;
+        aq[kk][3] = v1 ? bf16x2_to_f16x2(__ldg(q1p + c + 1)) : 0u;
+    }
+
+    // ---- per-warp ring of NST stages x (K tile, V tile), 16 rows of D bytes each
+    uint8_t* ring = smem + warp * NST * 2 * kTile;
+    const uint32_t ring_s = smem_u32(ring);
+    const long long row_stride = (long long)p.Hkv * D;  // bytes between consecutive cache rows
+    const uint8_t* kc = reinterpret_cast<const uint8_t*>(p.k_cache);
+    const uint8_t* vc = reinterpret_cast<const uint8_t*>(p.v_cache);
+    const int* pt = p.page_table + (long long)b * p.max_pages;
+    constexpr int kRowsPerIter = 32 / kChunks;
+    constexpr int kIters = kGroup / kRowsPerIter;
+    const int my_chunk = lane % kChunks;
+    const int my_row0 = lane / kChunks;
+    const int n_groups_total = cdiv(t_end - t_begin, kGroup);
+    const int my_groups = n_groups_total > warp ? cdiv(n_groups_total - warp, kWarps) : 0;
+
+    auto issue = [&](int i) {
+        const int slot = i % NST;
+        const int g = t_begin + kGroup * (warp + kWarps * i);
+        const int tok = g + (lane & 15);
+        long long off = 0;
+        int ok = 0;
+        if (tok < t_end) {
+            const int pg = __ldg(pt + tok / p.page_size);
+            if (pg >= 0 && pg < p.num_pages) {
+                off = ((long long)pg * p.page_size + (tok % p.page_size)) * row_stride + (long long)kvh * D;
+                ok = 1;
+            } else {
+                atomicCAS(p.status, 0, kDevBadIndex);
+            }
+        }
+        const uint32_t kdst = ring_s + slot * 2 * kTile;
+        const uint32_t vdst = kdst + kTile;
+#pragma unroll
+        for (int it = 0; it < kIters; ++it) {
+            const int r = it * kRowsPerIter + my_row0;
+            const long long ro = __shfl_sync(0xffffffffu, off, r);
+            const int rok = __shfl_sync(0xffffffffu, ok, r);
+            cp_async16(kdst + swz8<D>(r, my_chunk), rok ? kc + ro + my_chunk * 16 : kc, rok ? 16u : 0u);
+            cp_async16(vdst + swz8<D>(r, my_chunk), rok ? vc + ro + my_chunk * 16 : vc, rok ? 16u : 0u);
+        }
+    };
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+    constexpr int NH = GN / 8;
+    float oacc[NH][D / 16][4];
 #pragma unroll
     for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-            const int hd = nh * 8 + 2 * (lane & 3);
-            const int dr = mt * 16 + (lane >> 2);
-            float* base = sm_o + (long long)warp * GN * D;
-            base[hd * D + dr] = oacc[nh][mt][0];
-            base[(hd + 1) * D + dr] = oacc[nh][mt][1];
-            base[hd * D + dr + 8] = oacc[nh][mt][2];
-            base[(hd + 1) * D + dr + 8] = oacc[nh][mt][3];
-        }
-    __syncthreads();
+        for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) oacc[nh][mt][e] = 0.0f;
+    const float sl2 = p.scale_log2;
 
-    const bool direct = nsplit == 1;
-    for (int idx = threadIdx.x; idx < p.G * D; idx += blockDim.x) {
-        const int hh = idx / D, d = idx - hh * D;
-        float mm = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, sm_m[w * GN + hh]);
-        float ll = 0.0f, acc = 0.0f;
-        if (mm != -INFINITY) {
+    for (int i = 0; i < NST - 1; ++i) {
+        if (i < my_groups) issue(i);
+        cp_async_commit();
+    }
+    for (int i = 0; i < my_groups; ++i) {
+        cp_async_wait<NST - 2>();
+        __syncwarp();
+        if (i + NST - 1 < my_groups) issue(i + NST - 1);
+        cp_async_commit();
+
+        const int slot = i % NST;
+        const uint32_t kt = ring_s + slot * 2 * kTile;
+        const uint32_t vt = kt + kTile;
+        const int g = t_begin + kGroup * (warp + kWarps * i);
+
+        // K operand bytes: tokens g0 and g0 + 8, bytes [(D/4) qd, (D/4) qd + D/4) of the row
+        uint32_t kw[2][D / 16];
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float sw = ex2_mufu((sm_m[w * GN + hh] - mm) * sl2);
-                ll += sw * sm_l[w * GN + hh];
-                acc += sw * sm_o[(w * GN + hh) * D + d];
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int j = 0; j < D / 64; ++j) lds128(kt + swz8<D>(g0 + 8 * nt, (D / 64) * qd + j), &kw[nt][4 * j]);
+        // S = Q K^T : rows = heads, columns = 16 tokens (two n8 tiles)
+        float sc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            mma_f16_16816(sc[0], aq[kk], fp8x2_to_f16x2<FMT>(kw[0][kk]), fp8x2_to_f16x2<FMT>(kw[0][kk] >> 16));
+            mma_f16_16816(sc[1], aq[kk], fp8x2_to_f16x2<FMT>(kw[1][kk]), fp8x2_to_f16x2<FMT>(kw[1][kk] >> 16));
+        }
+        const int tk = g + 2 * qd;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (tk + nt * 8 + (e & 1) >= t_end) sc[nt][e] = -INFINITY;
+
+        // online softmax per head row (row0 = head g0, row1 = head g0 + 8)
+        float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+        float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mc0 = fmaxf(m0, mx0), mc1 = fmaxf(m1, mx1);
+        const bool need = ((mc0 - m0) * sl2 > p.rescale_thr) || (GN == 16 && (mc1 - m1) * sl2 > p.rescale_thr);
+        if (__any_sync(0xffffffffu, need)) {
+            const float a0 = (m0 == -INFINITY) ? 0.0f : ex2_mufu((m0 - mc0) * sl2);
+            const float a1 = (m1 == -INFINITY) ? 0.0f : ex2_mufu((m1 - mc1) * sl2);
+            l0 *= a0;
+            l1 *= a1;
+            m0 = mc0;
+            m1 = mc1;
+            const int src = qd * 8;  // lane holding head 2 qd: lane = 4 * head
+            const float c00 = __shfl_sync(0xffffffffu, a0, src);
+            const float c01 = __shfl_sync(0xffffffffu, a0, src + 4);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                oacc[0][mt][0] *= c00;
+                oacc[0][mt][1] *= c01;
+                oacc[0][mt][2] *= c00;
+                oacc[0][mt][3] *= c01;
+            }
+            if (GN == 16) {
+                const float c10 = __shfl_sync(0xffffffffu, a1, src);
+                const float c11 = __shfl_sync(0xffffffffu, a1, src + 4);
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    oacc[NH - 1][mt][0] *= c10;
+                    oacc[NH - 1][mt][1] *= c11;
+                    oacc[NH - 1][mt][2] *= c10;
+                    oacc[NH - 1][mt][3] *= c11;
+                }
             }
         }
-        const float o = ll > 0.0f ? acc / ll : 0.0f;
-        const float lse = ll > 0.0f ? mm * p.scale + logf(ll) : -INFINITY;
-        const long long bh = (long long)b * p.Hq + kvh * p.G + hh;
-        if (direct) {
-            p.o[bh * D + d] = __float2bfloat16(o);
-            if (d == 0) p.lse[bh] = lse;
-        } else {
-            p.ws_o[(bh * p.max_splits + split) * D + d] = o;
-            if (d == 0) p.ws_lse[bh * p.max_splits + split] = lse;
+        const float n0 = (m0 == -INFINITY) ? 0.0f : -m0 * sl2;
+        const float n1 = (m1 == -INFINITY) ? 0.0f : -m1 * sl2;
+        float pr[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            pr[nt][0] = ex2_mufu(fmaf(sc[nt][0], sl2, n0));
+            pr[nt][1] = ex2_mufu(fmaf(sc[nt][1], sl2, n0));
+            pr[nt][2] = ex2_mufu(fmaf(sc[nt][2], sl2, n1));
+            pr[nt][3] = ex2_mufu(fmaf(sc[nt][3], sl2, n1));
+        }
+        l0 += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+        l1 += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+        const uint32_t pb0 = pack_f16x2(pr[0][0], pr[0][1]);
+        const uint32_t pb1 = pack_f16x2(pr[1][0], pr[1][1]);
+        const uint32_t pb2 = pack_f16x2(pr[0][2], pr[0][3]);
+        const uint32_t pb3 = pack_f16x2(pr[1][2], pr[1][3]);
+
+        // V operand bytes: tokens 2qd, 2qd+1, 2qd+8, 2qd+9; bytes [(D/8) g0, (D/8) g0 + D/8).
+        // Row 16 mt + g0 of V^T is d = (D/8) g0 + 2 mt, row 16 mt + g0 + 8 is d + 1.
+        uint32_t vw[4][D / 32];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int tok = 2 * qd + (t & 1) + 8 * (t >> 1);
+            if (D == 128)
+                lds128(vt + swz8<D>(tok, g0), vw[t]);
+            else
+                lds64(vt + swz8<D>(tok, g0 >> 1) + (g0 & 1) * 8, vw[t]);
+        }
+        // O^T += V^T P^T : rows = permuted d (16 per m-tile), k = 16 tokens
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;  // bytes 2j and 2j+1 of both tokens
+            const uint32_t lo = __byte_perm(vw[0][mt >> 1], vw[1][mt >> 1], sel);
+            const uint32_t hi = __byte_perm(vw[2][mt >> 1], vw[3][mt >> 1], sel);
+            const uint32_t a[4] = {fp8x2_to_f16x2<FMT>(lo), fp8x2_to_f16x2<FMT>(lo >> 16), fp8x2_to_f16x2<FMT>(hi),
+                                   fp8x2_to_f16x2<FMT>(hi >> 16)};
+            mma_f16_16816(oacc[0][mt], a, pb0, pb1);
+            if (GN == 16) mma_f16_16816(oacc[NH - 1][mt], a, pb2, pb3);
         }
     }
+    cp_async_wait<0>();
+    merge_and_store<D, GN, true>(p, smem, oacc, m0, m1, l0, l1, split, nsplit, kvh, b, p.v_descale);
 }
 
 // One warp per (sequence, query head): LSE = log sum_s exp(lse_s) (max-shifted, warp
@@ -387,7 +682,46 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
     return e;
 }
 
+template <int D, int GN, int NST, int FMT>
+cudaError_t launch_fp8_t(const DecodeParams& p, cudaStream_t stream) {
+    constexpr int ring = kWarps * NST * 2 * kGroup * D;
+    constexpr int merge = (kWarps * GN * D + 2 * kWarps * GN) * 4;
+    constexpr int bytes = ring > merge ? ring : merge;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(decode_split_fp8_kernel<D, GN, NST, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 bytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const dim3 grid(p.max_splits, p.Hkv, p.B);
+    decode_split_fp8_kernel<D, GN, NST, FMT><<<grid, kWarps * 32, bytes, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (p.max_splits > 1) {
+        const long long rows = (long long)p.B * p.Hq;
+        decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+template <int FMT>
+cudaError_t launch_fp8_fmt(const DecodeParams& p, int d, cudaStream_t stream) {
+    constexpr int NST = 3;  // 48 KB of rings: 4 CTAs per SM (deeper rings measured slower)
+    if (d == 128)
+        return p.G <= 8 ? launch_fp8_t<128, 8, NST, FMT>(p, stream) : launch_fp8_t<128, 16, NST, FMT>(p, stream);
+    return p.G <= 8 ? launch_fp8_t<64, 8, NST, FMT>(p, stream) : launch_fp8_t<64, 16, NST, FMT>(p, stream);
+}
+
 }  // namespace
+
+cudaError_t launch_attn_decode_fp8(const DecodeParams& p, int d, int fmt, cudaStream_t stream) {
+    return fmt == 0 ? launch_fp8_fmt<0>(p, d, stream) : launch_fp8_fmt<1>(p, d, stream);
+}
 
 cudaError_t launch_attn_decode(const DecodeParams& p, int d, cudaStream_t stream) {
     constexpr int NST = 3;

@@ -58,10 +58,14 @@ struct DecodeParams {
     int chunk;       // tokens per split (multiple of 64)
     int max_splits;  // splits per sequence the workspace holds
     float scale, scale_log2, rescale_thr;
+    float v_descale;  // FP8 caches: value descale applied to the output (bf16 caches: unused)
     int* status;
 };
 
 cudaError_t launch_attn_decode(const DecodeParams& p, int d, cudaStream_t stream);
+// FP8 caches (k_cache / v_cache hold 8-bit codes); fmt 0 = e4m3, 1 = e5m2. p.scale and
+// p.scale_log2 already include the key descale.
+cudaError_t launch_attn_decode_fp8(const DecodeParams& p, int d, int fmt, cudaStream_t stream);
 
 // Status word and SM count of the current device (checks that it is an sm_103 GPU);
 // returns an attn_status_t code.

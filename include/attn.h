@@ -114,6 +114,30 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
                                 int Hkv, int d, int max_pages_per_seq, int num_pages, float scale, int num_splits);
 
 /*
+ * attn_decode_paged over key/value caches in 8-bit floating point ("Faster, more flexible
+ * FA4 for LLM inference", PR 2109: e4m3 or e5m2 inputs; half the cache bytes of bf16).
+ *
+ * k_cache, v_cache  device, 8-bit codes [num_pages, page_size, Hkv, d] in the OCP FP8
+ *                   format kv_format: ATTN_FP8_E4M3 (4 exponent bits, bias 7, largest 448,
+ *                   no infinities) or ATTN_FP8_E5M2 (5 exponent bits, bias 15).
+ * k_descale, v_descale  one factor per tensor: key code c stands for k_descale * fp8(c),
+ *                   value code c for v_descale * fp8(c). Finite; otherwise
+ *                   ATTN_ERR_BAD_ARG. An unknown kv_format is ATTN_ERR_BAD_ARG.
+ * Everything else (q in bf16, page table, seqlens, o, lse, sizes, num_splits, workspace,
+ * alignment, errors) is as for attn_decode_paged.
+ * Arithmetic: the products run on the tensor cores in f16 with fp32 accumulation. Every
+ * FP8 value is exact in f16; q is converted from bf16 to f16, which is exact for
+ * |q| in [2^-14, 65504] (smaller magnitudes lose low bits, larger ones overflow), and the
+ * probabilities are rounded to f16 before the P V product.
+ */
+#define ATTN_FP8_E4M3 0
+#define ATTN_FP8_E5M2 1
+attn_status_t attn_decode_paged_fp8(const void* q, const void* k_cache, const void* v_cache, const int* page_table,
+                                    const int* seqlens, int page_size, void* o, float* lse, void* stream, int B,
+                                    int Hq, int Hkv, int d, int max_pages_per_seq, int num_pages, float scale,
+                                    int num_splits, int kv_format, float k_descale, float v_descale);
+
+/*
  * attn_decode_paged without any memory allocation. The pages have no counterpart to this
  * call; it exists for callers that cannot allocate device memory when they run decode:
  * a serving engine that has already given nearly all of the GPU's memory to its own

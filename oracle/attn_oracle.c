@@ -350,6 +350,11 @@ typedef struct {
 static void* dec8_worker(void* p) {
     dec8_job_t* J = (dec8_job_t*)p;
     const int d = J->d, Hkv = J->Hkv, G = J->Hq / J->Hkv;
+    double ktab[256], vtab[256]; /* descale * fp8(c) for every code c */
+    for (int c = 0; c < 256; ++c) {
+        ktab[c] = J->k_descale * oracle_fp8_value((uint8_t)c, J->fmt);
+        vtab[c] = J->v_descale * oracle_fp8_value((uint8_t)c, J->fmt);
+    }
     for (;;) {
         const int64_t b = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
         if (b >= J->B) break;
@@ -373,8 +378,8 @@ static void* dec8_worker(void* p) {
             const int64_t page = J->page_table[b * J->max_pages + t / J->page_size];
             const size_t src = (size_t)(page * J->page_size + t % J->page_size) * row_elems;
             for (size_t e = 0; e < row_elems; ++e) {
-                kb[(size_t)t * row_elems + e] = J->k_descale * oracle_fp8_value(J->kc[src + e], J->fmt);
-                vb[(size_t)t * row_elems + e] = J->v_descale * oracle_fp8_value(J->vc[src + e], J->fmt);
+                kb[(size_t)t * row_elems + e] = ktab[J->kc[src + e]];
+                vb[(size_t)t * row_elems + e] = vtab[J->vc[src + e]];
             }
         }
         for (int h = 0; h < J->Hq; ++h) {

@@ -79,6 +79,31 @@ def test_decode_host_validation(lib):
     assert _dec(lib, B=0) == A.ATTN_OK
 
 
+def _dec8(lib, fmt=0, kds=0.5, vds=2.0, **kw):
+    f = lib.attn_decode_paged_fp8
+    vp = ctypes.c_void_p
+    f.argtypes = ([vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp] + [ctypes.c_int] * 6 +
+                  [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_float])
+    a = dict(q=16, kc=16, vc=16, pt=16, sl=16, ps=16, o=16, lse=16, B=1, Hq=8, Hkv=2, d=128, mp=4, npg=4,
+             scale=0.1, ns=0)
+    a.update(kw)
+    return f(a["q"], a["kc"], a["vc"], a["pt"], a["sl"], a["ps"], a["o"], a["lse"], None, a["B"], a["Hq"], a["Hkv"],
+             a["d"], a["mp"], a["npg"], a["scale"], a["ns"], fmt, kds, vds)
+
+
+def test_fp8_decode_host_validation(lib):
+    import exact_softmax_attention_gb300 as A
+    assert _dec8(lib, fmt=2) == A.ATTN_ERR_BAD_ARG
+    assert _dec8(lib, fmt=-1) == A.ATTN_ERR_BAD_ARG
+    assert _dec8(lib, kds=float("inf")) == A.ATTN_ERR_BAD_ARG
+    assert _dec8(lib, vds=float("nan")) == A.ATTN_ERR_BAD_ARG
+    assert _dec8(lib, kds=1e30, scale=1e30) == A.ATTN_ERR_BAD_ARG  # score scale overflows
+    assert _dec8(lib, pt=None) == A.ATTN_ERR_NULL_PTR
+    assert _dec8(lib, d=96) == A.ATTN_ERR_BAD_SHAPE
+    assert _dec8(lib, vc=0x1008) == A.ATTN_ERR_ALIGN
+    assert _dec8(lib, fmt=1, B=0) == A.ATTN_OK
+
+
 @pytest.mark.parametrize("B,Hkv,mp,ps,ns", [(64, 8, 2048, 16, 0), (1, 1, 1, 1, 0), (3, 2, 10, 7, 4),
                                             (64, 8, 2048, 16, 5), (8, 1, 100, 1, 1)])
 def test_decode_plan(B, Hkv, mp, ps, ns):

@@ -1,0 +1,137 @@
+"""attn_decode_paged_fp8 (8-bit floating-point key/value caches) on the GPU against the float64
+CPU oracle, which decodes the codes from the OCP FP8 definitions and applies the descales."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import TOL_LSE, TOL_O, compare, ensure_built, to_dev
+from synth import workloads as W
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def A():
+    ensure_built()
+    import exact_softmax_attention_gb300 as mod
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return mod
+
+
+def run(A, c, q, kc8, vc8, pt, sl, kds, vds, num_splits=0):
+    o = torch.full((c.B, c.Hq, c.d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((c.B, c.Hq), float("nan"), dtype=torch.float32, device=DEV)
+    A.attn_decode_paged_fp8(to_dev(q, DEV), torch.from_numpy(kc8).to(DEV), torch.from_numpy(vc8).to(DEV),
+                            torch.from_numpy(pt).to(DEV), torch.from_numpy(sl).to(DEV), c.page_size, o, lse, None,
+                            c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.num_pages, c.scale, num_splits, c.kv_fmt, kds, vds)
+    assert A.attn_get_device_status() == 0
+    return o, lse
+
+
+def reference(c, q, kc8, vc8, pt, sl, kds, vds, rows=None):
+    if rows is None:
+        rows = np.arange(c.B)
+    return oracle.attn_decode_paged_fp8(q[rows], kc8, vc8, c.kv_fmt, kds, vds, pt[rows], sl[rows], c.page_size,
+                                        len(rows), c.Hq, c.Hkv, c.d, c.max_pages, c.scale)
+
+
+def fcase(name, B, Hq, Hkv, d, page_size, lo, hi, seed, fmt, extra=0, lens=None):
+    if lens is None:
+        lens = synth.uniform_ints(B, seed, lo, hi)
+    lens = np.asarray(lens, dtype=np.int32)
+    max_pages = int((max(int(lens.max()), 1) + page_size - 1) // page_size) + 2
+    return W.DecodeCase(name, len(lens), Hq, Hkv, d, page_size, lens, max_pages, 1.0 / math.sqrt(d), seed,
+                        extra_pages=extra, kv_fmt=fmt)
+
+
+CASES = [
+    (fcase("e4m3_p16_g4", 9, 32, 8, 128, 16, 1, 3000, 21, "e4m3"), 0),
+    (fcase("e5m2_p16_g4", 9, 32, 8, 128, 16, 1, 3000, 22, "e5m2"), 0),
+    (fcase("e4m3_split3", 5, 8, 2, 128, 16, 500, 2500, 23, "e4m3"), 3),
+    (fcase("e4m3_p1", 4, 8, 2, 128, 1, 1, 700, 24, "e4m3"), 0),
+    (fcase("e5m2_p7_d64", 6, 12, 3, 64, 7, 1, 1500, 25, "e5m2"), 0),
+    (fcase("e4m3_d64_g16", 3, 16, 1, 64, 16, 100, 5000, 26, "e4m3"), 0),
+    (fcase("e4m3_mqa_g16", 3, 16, 1, 128, 16, 100, 5000, 27, "e4m3"), 0),
+    (fcase("e4m3_g12", 3, 24, 2, 128, 32, 100, 2000, 28, "e4m3"), 2),
+    (fcase("e5m2_g1", 4, 4, 4, 64, 16, 1, 900, 29, "e5m2"), 0),
+    (fcase("e4m3_edges", 0, 8, 2, 128, 16, 0, 0, 30, "e4m3", lens=[0, 1, 15, 16, 17, 63, 64, 65, 1024, 1025]), 0),
+]
+
+
+@pytest.mark.parametrize("c,ns", CASES, ids=[c.name for c, _ in CASES])
+def test_fp8_decode_cases(A, c, ns):
+    q, kc8, vc8, pt, sl, kds, vds = c.generate_fp8()
+    o, lse = run(A, c, q, kc8, vc8, pt, sl, kds, vds, ns)
+    ro, rl = reference(c, q, kc8, vc8, pt, sl, kds, vds)
+    do, dl = compare(o, lse, ro, rl)
+    assert do <= TOL_O and dl <= TOL_LSE, f"{c.name}: max|dO|={do:.3e} max|dLSE|={dl:.3e}"
+
+
+def test_fp8_descales_are_applied(A):
+    """Scaling the descales changes the GPU result exactly as it changes the oracle's."""
+    c = fcase("descale", 4, 8, 2, 128, 16, 200, 3000, 31, "e4m3")
+    q, kc8, vc8, pt, sl, _, _ = c.generate_fp8()
+    for kds, vds in ((0.004, 0.01), (0.02, 3.0)):
+        o, lse = run(A, c, q, kc8, vc8, pt, sl, kds, vds)
+        ro, rl = reference(c, q, kc8, vc8, pt, sl, kds, vds)
+        do, dl = compare(o, lse, ro, rl)
+        # the output is stored in bf16: its rounding grows with |O|, so the bound scales with it
+        tol = TOL_O * max(1.0, float(np.abs(ro).max()))
+        assert do <= tol and dl <= TOL_LSE, f"descales {kds},{vds}: {do:.3e} {dl:.3e}"
+
+
+def test_fp8_nan_pages_never_read(A):
+    c = fcase("canary", 6, 8, 2, 128, 16, 1, 2000, 32, "e4m3", extra=12)
+    q, kc8, vc8, pt, sl, kds, vds = c.generate_fp8()
+    used = np.zeros(c.num_pages, dtype=bool)
+    for b in range(c.B):
+        used[pt[b, : int(c.pages_per_seq[b])]] = True
+    kc8[~used] = 0x7F  # NaN codes
+    vc8[~used] = 0x7F
+    o, lse = run(A, c, q, kc8, vc8, pt, sl, kds, vds)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    ro, rl = reference(c, q, kc8, vc8, pt, sl, kds, vds)
+    do, dl = compare(o, lse, ro, rl)
+    assert do <= TOL_O and dl <= TOL_LSE
+
+
+def test_fp8_split_count_does_not_change_result(A):
+    c = fcase("splits", 4, 8, 2, 128, 16, 3000, 6000, 33, "e5m2")
+    q, kc8, vc8, pt, sl, kds, vds = c.generate_fp8()
+    outs = [run(A, c, q, kc8, vc8, pt, sl, kds, vds, ns) for ns in (1, 2, 5, 0)]
+    for o, lse in outs[1:]:
+        assert (o.float() - outs[0][0].float()).abs().max().item() <= 2e-2
+        assert (lse - outs[0][1]).abs().max().item() <= 2e-3
+
+
+def test_fp8_decode_workload_sampled(A):
+    """The full e4m3 decode workload (64 sequences, lengths up to 32768) on the GPU, compared
+    with the oracle on 8 sequences including the longest."""
+    c = W.decode_fp8()
+    q, kc8, vc8, pt, sl, kds, vds = c.generate_fp8()
+    o, lse = run(A, c, q, kc8, vc8, pt, sl, kds, vds)
+    rows = np.unique(np.concatenate([[int(np.argmax(sl)), int(np.argmin(sl))], np.arange(0, c.B, 10)]))
+    ro, rl = reference(c, q, kc8, vc8, pt, sl, kds, vds, rows)
+    do, dl = compare(o[torch.from_numpy(rows).to(DEV)], lse[torch.from_numpy(rows).to(DEV)], ro, rl)
+    assert do <= TOL_O and dl <= TOL_LSE, f"max|dO|={do:.3e} max|dLSE|={dl:.3e}"
+
+
+def test_fp8_rejects_unknown_format_and_bad_descales(A):
+    c = fcase("bad", 2, 8, 2, 128, 16, 10, 20, 34, "e4m3")
+    q, kc8, vc8, pt, sl, kds, vds = c.generate_fp8()
+    for fmt, k_, v_ in ((2, kds, vds), (0, float("inf"), vds), (1, kds, float("nan"))):
+        o = torch.full((c.B, c.Hq, c.d), float("nan"), dtype=torch.bfloat16, device=DEV)
+        lse = torch.full((c.B, c.Hq), float("nan"), dtype=torch.float32, device=DEV)
+        rc = A.attn_decode_paged_fp8(to_dev(q, DEV), torch.from_numpy(kc8).to(DEV), torch.from_numpy(vc8).to(DEV),
+                                     torch.from_numpy(pt).to(DEV), torch.from_numpy(sl).to(DEV), c.page_size, o, lse,
+                                     None, c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.num_pages, c.scale, 0, fmt, k_, v_,
+                                     raise_on_error=False)
+        assert rc == A.ATTN_ERR_BAD_ARG
+        torch.cuda.synchronize()
+        assert torch.isnan(o.float()).all()
