@@ -18,6 +18,10 @@ Contents
     from the OCP 8-bit floating-point definitions and multiplied by one descale
     factor per tensor (a reading: the pages fix no scaling scheme), then the
     same three-pass definition runs in float64.
+``attn_fwd_f64`` / ``attn_fwd_fp8``
+    The forward definition on float64 inputs; ``attn_fwd_fp8`` decodes 8-bit
+    floating-point Q/K/V codes (PR 2109 of the same page) and applies one descale
+    per tensor before it.
 ``online_attention``
     The streaming recurrence of "FlashAttention: not computing less, moving
     less", section 02 (running max m, sum l, unnormalised accumulator a,
@@ -86,6 +90,8 @@ def _load():
             lib.oracle_attn_decode_paged.restype = i
             lib.oracle_attn_decode_paged_fp8.argtypes = [vp, vp, vp, i, d, d, vp, vp, i, vp, vp, i, i, i, i, i, d, i]
             lib.oracle_attn_decode_paged_fp8.restype = i
+            lib.oracle_attn_fwd_f64.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, d, i, vp, vp, i64, i]
+            lib.oracle_attn_fwd_f64.restype = i
             lib.oracle_fp8_values.argtypes = [vp, vp, i64, i]
             lib.oracle_fp8_values.restype = None
             lib.oracle_exp2_poly.argtypes = [ctypes.c_float]
@@ -141,6 +147,38 @@ def attn_fwd(q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens=None, row
     if rc != 0:
         raise ValueError(f"oracle_attn_fwd rejected its arguments (rc={rc})")
     return o, lse
+
+
+def attn_fwd_f64(q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens=None, rows=None, n_threads=None):
+    """attn_fwd on float64 inputs (same layouts, masks and ``rows`` as ``attn_fwd``)."""
+    q, k, v = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v))
+    cu = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    T = int(cu[-1]) if cu is not None else B * Nq
+    if rows is None:
+        o = np.zeros((T, Hq, d), dtype=np.float64)
+        lse = np.zeros((T, Hq), dtype=np.float64)
+        rp, nr = None, 0
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        o = np.zeros((len(rows), d), dtype=np.float64)
+        lse = np.zeros((len(rows),), dtype=np.float64)
+        rp, nr = rows.ctypes.data, len(rows)
+    rc = _load().oracle_attn_fwd_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data, o.ctypes.data, lse.ctypes.data,
+                                     B, Hq, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                                     None if cu is None else cu.ctypes.data, rp, nr, n_threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_attn_fwd_f64 rejected its arguments (rc={rc})")
+    return o, lse
+
+
+def attn_fwd_fp8(q, k, v, fmt, q_descale, k_descale, v_descale, B, Hq, Hkv, Nq, Nk, d, scale, causal,
+                 cu_seqlens=None, rows=None, n_threads=None):
+    """attn_fwd on 8-bit floating-point Q/K/V codes (uint8, OCP e4m3 or e5m2), each tensor
+    standing for its descale times the decoded values."""
+    qf = q_descale * fp8_values(q, fmt)
+    kf = k_descale * fp8_values(k, fmt)
+    vf = v_descale * fp8_values(v, fmt)
+    return attn_fwd_f64(qf, kf, vf, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens, rows, n_threads)
 
 
 def attn_decode_paged(q, k_cache, v_cache, page_table, seqlens, page_size, B, Hq, Hkv, d, max_pages, scale,

@@ -77,10 +77,14 @@ static void attend_row(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
     *lse = m + log(l);
 }
 
+static void attend_row_f64(const double* qd, const double* k, const double* v, int64_t stride, int64_t n, int d,
+                           double scale, double* s, double* o, double* lse);
+
 /* ------------------------------------------------------------------ forward */
 
 typedef struct {
     const uint16_t *q, *k, *v;
+    const double *qf, *kf, *vf; /* float64 inputs (oracle_attn_fwd_f64) */
     double *o, *lse;
     int B, Hq, Hkv, Nq, Nk, d, causal;
     double scale;
@@ -412,5 +416,78 @@ int oracle_attn_decode_paged_fp8(const uint16_t* q, const uint8_t* k_cache, cons
     J.d = d; J.max_pages = max_pages; J.scale = scale; J.o = o; J.lse = lse;
     if (B == 0) return 0;
     run_threads(dec8_worker, &J, n_threads < B ? n_threads : B);
+    return J.status;
+}
+
+
+/* ------------------------------------------------------------------ forward, float64 inputs */
+
+/*
+ * The forward definition on float64 inputs, for inputs that are not bf16: 8-bit
+ * floating-point Q/K/V ("Faster, more flexible FA4 for LLM inference", PR 2109) are
+ * decoded and multiplied by their descales by the caller, then passed here. Same
+ * layouts, masks and rows as oracle_attn_fwd.
+ */
+static void* fwd_f64_worker(void* p) {
+    fwd_job_t* J = (fwd_job_t*)p;
+    const int d = J->d;
+    const int G = J->Hq / J->Hkv;
+    const int64_t total_tokens = J->cu ? J->cu[J->B] : (int64_t)J->B * J->Nq;
+    const int64_t n_items = J->rows ? J->n_rows : total_tokens * J->Hq;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(J->max_keys > 0 ? J->max_keys : 1));
+    if (!s) {
+        __atomic_store_n(&J->status, -2, __ATOMIC_RELAXED);
+        return NULL;
+    }
+    for (;;) {
+        const int64_t it = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
+        if (it >= n_items) break;
+        const int64_t row = J->rows ? J->rows[it] : it;
+        const int64_t t = row / J->Hq;
+        const int h = (int)(row % J->Hq);
+        int64_t i, nq, nk, k0;
+        if (row < 0 || locate(J, t, &i, &nq, &nk, &k0) != 0) {
+            __atomic_store_n(&J->status, -3, __ATOMIC_RELAXED);
+            continue;
+        }
+        int64_t n_vis = nk;
+        if (J->causal) {
+            const int64_t last = i + (nk - nq);
+            n_vis = last + 1 < nk ? last + 1 : nk;
+        }
+        if (n_vis < 0) n_vis = 0;
+        const int g = h / G;
+        const int64_t kv_stride = (int64_t)J->Hkv * d;
+        attend_row_f64(J->qf + (t * J->Hq + h) * d, J->kf + k0 * kv_stride + (int64_t)g * d,
+                       J->vf + k0 * kv_stride + (int64_t)g * d, kv_stride, n_vis, d, J->scale, s, J->o + it * d,
+                       J->lse + it);
+    }
+    free(s);
+    return NULL;
+}
+
+int oracle_attn_fwd_f64(const double* q, const double* k, const double* v, double* o, double* lse, int B, int Hq,
+                        int Hkv, int Nq, int Nk, int d, double scale, int causal, const int32_t* cu_seqlens,
+                        const int64_t* rows, int64_t n_rows, int n_threads) {
+    if (!q || !k || !v || !o || !lse || B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0) return -1;
+    fwd_job_t J;
+    memset(&J, 0, sizeof J);
+    J.qf = q; J.kf = k; J.vf = v; J.o = o; J.lse = lse;
+    J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.Nq = Nq; J.Nk = Nk; J.d = d; J.causal = causal;
+    J.scale = scale; J.cu = cu_seqlens; J.rows = rows; J.n_rows = n_rows;
+    if (cu_seqlens) {
+        int64_t mx = 0;
+        for (int b = 0; b < B; ++b) {
+            const int64_t L = (int64_t)cu_seqlens[b + 1] - cu_seqlens[b];
+            if (L < 0) return -1;
+            if (L > mx) mx = L;
+        }
+        J.max_keys = mx;
+    } else {
+        if (Nq < 0 || Nk < 0) return -1;
+        J.max_keys = Nk;
+    }
+    if (B == 0) return 0;
+    run_threads(fwd_f64_worker, &J, n_threads);
     return J.status;
 }

@@ -53,6 +53,19 @@ class PrefillCase:
     def total_k(self) -> int:
         return int(self.cu_seqlens[-1]) if self.cu_seqlens is not None else self.B * self.Nk
 
+    def generate_fp8(self, fmt: str = "e4m3"):
+        """(q, k, v as FP8 codes (uint8), q_descale, k_descale, v_descale): the bf16 case's
+        draws divided by a per-tensor descale (max |x| / largest finite FP8 value, float32)
+        and rounded to FP8."""
+        out = []
+        for c in self.generate():
+            x = bf16_to_f32(c).astype(np.float64)
+            amax = float(np.abs(x).max()) if x.size else 0.0
+            ds = np.float32(amax / FP8_MAX[fmt]) if amax > 0 else np.float32(1.0)
+            out.append((fp8_encode(x / float(ds), fmt), float(ds)))
+        (q8, qd), (k8, kd), (v8, vd) = out
+        return q8, k8, v8, qd, kd, vd
+
     def generate(self):
         """(q [Tq, Hq, d], k [Tk, Hkv, d], v [Tk, Hkv, d]) as bf16 bit patterns (uint16)."""
         q = normal_bf16((self.total_q, self.Hq, self.d), sub_seed(self.seed, _Q), self.q_mult)

@@ -418,6 +418,56 @@ def test_fp8_decode_ignores_unreferenced_nan_pages():
     assert np.isfinite(o).all() and np.isfinite(lse).all()
 
 
+def test_fwd_f64_equals_bf16_forward_on_the_same_values():
+    """The float64-input forward reproduces the (separately pinned) bf16 forward exactly on
+    bf16 values: dense causal with Nq < Nk, packed sequences, and a row subset."""
+    c = W.PrefillCase("f64", 2, 4, 2, 70, 90, 32, 0.2, True, 5)
+    q, k, v = c.generate()
+    f = synth.bf16_to_f32
+    o1, l1 = oracle.attn_fwd(q, k, v, c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d, c.scale, True)
+    o2, l2 = oracle.attn_fwd_f64(f(q), f(k), f(v), c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d, c.scale, True)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    cu = np.array([0, 33, 33, 120], dtype=np.int32)
+    pc = W.PrefillCase("f64p", 3, 4, 1, 0, 0, 16, 0.25, True, 6, cu_seqlens=cu)
+    q, k, v = pc.generate()
+    rows = np.array([0, 5, 33 * 4 + 3, 119 * 4 + 2], dtype=np.int64)
+    for r in (None, rows):
+        o1, l1 = oracle.attn_fwd(q, k, v, 3, 4, 1, 120, 120, 16, 0.25, True, cu, r)
+        o2, l2 = oracle.attn_fwd_f64(f(q), f(k), f(v), 3, 4, 1, 120, 120, 16, 0.25, True, cu, r)
+        np.testing.assert_array_equal(o1, o2)
+        np.testing.assert_array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_forward_equals_bf16_forward_of_the_same_values(fmt):
+    """With power-of-two descales every FP8 value times its descale is exact in bf16, so the
+    FP8 forward must equal the bf16 forward oracle on those values."""
+    c = W.PrefillCase("fp8f", 1, 4, 2, 96, 96, 32, 0.18, True, 7)
+    q8, k8, v8, _, _, _ = c.generate_fp8(fmt)
+    qs, ks, vs = 0.25, 0.0625, 2.0
+    qb, kb, vb = (synth.f32_to_bf16(s_ * oracle.fp8_values(a, fmt)) for s_, a in ((qs, q8), (ks, k8), (vs, v8)))
+    assert (synth.bf16_to_f32(kb) == ks * oracle.fp8_values(k8, fmt)).all()
+    o8, l8 = oracle.attn_fwd_fp8(q8, k8, v8, fmt, qs, ks, vs, c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d, c.scale, True)
+    o, lse = oracle.attn_fwd(qb, kb, vb, c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d, c.scale, True)
+    np.testing.assert_array_equal(o8, o)
+    np.testing.assert_array_equal(l8, lse)
+
+
+def test_fp8_forward_descales_act_as_scales():
+    """q and k descales multiply every score like the softmax scale; the v descale multiplies O."""
+    c = W.PrefillCase("fp8d", 1, 2, 2, 64, 64, 32, 0.2, False, 8)
+    q8, k8, v8, _, _, _ = c.generate_fp8("e4m3")
+    a = (c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d)
+    o1, l1 = oracle.attn_fwd_fp8(q8, k8, v8, "e4m3", 0.3, 0.05, 1.0, *a, c.scale, False)
+    o2, l2 = oracle.attn_fwd_fp8(q8, k8, v8, "e4m3", 1.0, 1.0, 1.0, *a, c.scale * 0.3 * 0.05, False)
+    np.testing.assert_allclose(o1, o2, rtol=1e-10, atol=1e-12)  # reassociation only
+    np.testing.assert_allclose(l1, l2, rtol=1e-10, atol=1e-12)
+    o3, l3 = oracle.attn_fwd_fp8(q8, k8, v8, "e4m3", 0.3, 0.05, 7.0, *a, c.scale, False)
+    np.testing.assert_allclose(o3, 7.0 * o1, rtol=1e-12, atol=1e-14)
+    np.testing.assert_array_equal(l3, l1)
+
+
 # ----------------------------------------------------------------- exp2 model
 
 def test_exp2_cubic_error_table():
