@@ -84,15 +84,16 @@ attn_status_t encode_fn() {
     return ATTN_OK;
 }
 
-// 3-D map over a [rows, heads, d] bf16 tensor; box = 64 elements of d x 1 head x 128 rows,
-// 128-byte swizzle (the K-major / MN-major canonical layout the MMAs read), zero fill
-// outside [0, rows).
-attn_status_t make_map(CUtensorMap* m, const void* base, long long rows, int heads, int d) {
+// 3-D map over a [rows, heads, d] tensor of bf16 (elem 2) or 8-bit codes (elem 1); box =
+// 128 bytes of d x 1 head x 128 rows, 128-byte swizzle (the K-major / MN-major canonical
+// layout the MMAs read), zero fill outside [0, rows).
+attn_status_t make_map(CUtensorMap* m, const void* base, long long rows, int heads, int d, int elem = 2) {
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
-    cuuint32_t box[3] = {64, 1, 128};
+    cuuint64_t strides[2] = {(cuuint64_t)d * elem, (cuuint64_t)heads * d * elem};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / elem), 1, 128};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = g_encode(m, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                          const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
@@ -170,11 +171,15 @@ attn_status_t attn_get_option(const char* name, double* value) {
     return ATTN_OK;
 }
 
-attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                       int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens, void* stream) {
+// Shared body of the forward entry points. fp8 < 0: bf16 Q/K/V; 0 / 1: e4m3 / e5m2 codes
+// with per-tensor descales (d = 128 only).
+static attn_status_t fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                         int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens, void* stream, int fp8,
+                         float q_descale, float k_descale, float v_descale) {
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL_PTR;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq < 0 || Nk < 0 || (d != 64 && d != 128))
         return ATTN_ERR_BAD_SHAPE;
+    if (fp8 >= 0 && d != 128) return ATTN_ERR_BAD_SHAPE;
     if (causal != 0 && causal != 1) return ATTN_ERR_BAD_SHAPE;
     if (!isfinite(scale)) return ATTN_ERR_BAD_SHAPE;
     if (Hq > 65535 || Hkv > 65535) return ATTN_ERR_BAD_SHAPE;
@@ -192,8 +197,9 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
     if (st != ATTN_OK) return st;
     if ((st = encode_fn()) != ATTN_OK) return st;
     FwdTmaps tm;
-    if (make_map(&tm.q, q, Tq, Hq, d) != ATTN_OK || make_map(&tm.k, k, Tk, Hkv, d) != ATTN_OK ||
-        make_map(&tm.v, v, Tk, Hkv, d) != ATTN_OK)
+    const int elem = fp8 >= 0 ? 1 : 2;
+    if (make_map(&tm.q, q, Tq, Hq, d, elem) != ATTN_OK || make_map(&tm.k, k, Tk, Hkv, d, elem) != ATTN_OK ||
+        make_map(&tm.v, v, Tk, Hkv, d, elem) != ATTN_OK)
         return ATTN_ERR_CUDA;
     const Options opt = options();
     FwdParams p;
@@ -208,8 +214,10 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
     p.Nq = Nq;
     p.Nk = Nk;
     p.causal = causal;
-    p.scale = scale;
-    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    const double score_scale = fp8 < 0 ? (double)scale : (double)scale * (double)q_descale * (double)k_descale;
+    p.scale = (float)score_scale;
+    p.scale_log2 = (float)(score_scale * 1.4426950408889634);
+    p.out_scale = fp8 < 0 ? 1.0f : v_descale;
     p.rescale_thr = (float)opt.rescale_threshold;
     p.status = ds->status;
     p.counters = opt.count ? ds->counters : nullptr;
@@ -242,8 +250,26 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
         p.total_tiles = 0;
     }
     if (grid <= 0) return ATTN_OK;
-    const cudaError_t e = attn::launch_attn_fwd(tm, p, d, opt.exp_poly, grid, reinterpret_cast<cudaStream_t>(stream));
+    const cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = fp8 < 0 ? attn::launch_attn_fwd(tm, p, d, opt.exp_poly, grid, st_)
+                                  : attn::launch_attn_fwd_fp8(tm, p, d, fp8, grid, st_);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                       int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens, void* stream) {
+    return fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens, stream, -1, 1.0f, 1.0f, 1.0f);
+}
+
+attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                           int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens, void* stream,
+                           int fp8_format, float q_descale, float k_descale, float v_descale) {
+    if (fp8_format != ATTN_FP8_E4M3 && fp8_format != ATTN_FP8_E5M2) return ATTN_ERR_BAD_ARG;
+    if (!isfinite(q_descale) || !isfinite(k_descale) || !isfinite(v_descale)) return ATTN_ERR_BAD_ARG;
+    const double score_scale_log2 = (double)scale * (double)q_descale * (double)k_descale * 1.4426950408889634;
+    if (!(fabs(score_scale_log2) <= (double)FLT_MAX)) return ATTN_ERR_BAD_ARG;  // the kernel uses it as a float
+    return fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens, stream, fp8_format, q_descale,
+               k_descale, v_descale);
 }
 
 attn_status_t attn_decode_plan(int B, int Hkv, int max_pages_per_seq, int page_size, int num_splits, int num_sms,

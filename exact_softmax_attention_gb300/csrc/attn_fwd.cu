@@ -48,16 +48,24 @@ constexpr int kMaxLevels = 2048;  // 256-row blocks per packed sequence for the 
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
 constexpr uint32_t kTmemCols = 512;
 
-template <int D>
+template <int D, int F8 = 0>
 struct Layout {
-    static constexpr int kQBytes = BM * D * 2;
-    static constexpr int kKVBytes = BN * D * 2;
+    // F8 != 0: Q, K and V arrive as 8-bit floating-point codes (1 = e4m3, 2 = e5m2); V is
+    // widened to f16 in shared memory before the P V product.
+    static constexpr int kElem = F8 ? 1 : 2;             // bytes per loaded Q/K/V element
+    static constexpr int kQBytes = BM * D * kElem;
+    static constexpr int kKBytes = BN * D * kElem;       // K tile as loaded
+    static constexpr int kV8Bytes = F8 ? BN * D : 0;     // 8-bit V tile as loaded
+    static constexpr int kVBytes = BN * D * 2;           // 16-bit V tile read by the MMA
     // Ring entry n holds what burst n reads: K tile n (for S = Q K_n^T) and V tile n-1
-    // (for O += P_{n-1} V_{n-1}).
-    static constexpr int kEntryBytes = 2 * kKVBytes;
+    // (for O += P_{n-1} V_{n-1}); with 8-bit inputs also the 8-bit V tile it is widened from.
+    static constexpr int kV8Off = kKBytes;
+    static constexpr int kVOff = kKBytes + kV8Bytes;
+    static constexpr int kEntryBytes = kKBytes + kV8Bytes + kVBytes;
     static constexpr int kEntries = (D == 128) ? 2 : 4;
-    static constexpr int kChunks = D / 64;                // 128-byte swizzle chunks along d
-    static constexpr int kChunkBytesQ = BM * 128;         // one [128 rows x 64 d] chunk
+    static constexpr int kChunks = D * kElem / 128;      // 128-byte swizzle chunks per Q/K row
+    static constexpr int kVChunks = D / 64;              // 128-byte chunks per 16-bit V row
+    static constexpr int kChunkBytesQ = BM * 128;        // one [128 rows x 128 bytes] chunk
     static constexpr int kChunkBytesKV = BN * 128;
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = 2 * kQBytes;
@@ -67,7 +75,10 @@ struct Layout {
     static constexpr int bSFull = 4 + 2 * kEntries, bPFull = bSFull + 2, bOFull = bSFull + 4, bOEmpty = bSFull + 6;
     static constexpr int bStats = bSFull + 8, bDrain = bSFull + 10, bIssued = bSFull + 12;
     static constexpr int bPRest = bSFull + 14;  // P stage 2 (keys 96-127); bPFull is stage 1
-    static constexpr int kNumBars = bPRest + 2;
+    // 8-bit inputs: [kEntries] the entry's 8-bit V tile has landed / has been widened. Only
+    // entries that carry V advance them.
+    static constexpr int bV8Full = bSFull + 16, bVConv = bV8Full + (F8 ? kEntries : 0);
+    static constexpr int kNumBars = bVConv + (F8 ? kEntries : 0);
     static constexpr int kStatsOff = kBarOff + ((kNumBars * 8 + 15) / 16) * 16;
     static constexpr int kMiscOff = kStatsOff + 2 * 2 * BM * 4;   // m[2][128], l[2][128]
     // misc: tmem base, abort flag, packed-order levels, packed work tiles
@@ -124,6 +135,86 @@ __device__ __forceinline__ bool packed_seq(const FwdParams& p, int b, int& first
     first = ok ? a : 0;
     len = ok ? e - a : 0;
     return ok;
+}
+
+// ------------------------------------------------------------------ 8-bit inputs
+// Instruction descriptor of kind::f8f6f4 with fp32 accumulation; fmt 0 = e4m3, 1 = e5m2
+// for both A and B ([7,10) A format, [10,13) B format), both K-major.
+__host__ __device__ constexpr uint32_t idesc_f8_f32(uint32_t M, uint32_t N, uint32_t fmt) {
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Instruction descriptor of kind::f16 with f16 A and B (format 0) and fp32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, uint32_t b_mn_major) {
+    return (1u << 4) | (b_mn_major << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma_ss_f8_by(uint32_t issue, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 e, %5, 0;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two 8-bit codes (low byte first) to an f16 pair (low half first); exact for every code.
+template <int F8>
+__device__ __forceinline__ uint32_t f8x2_to_f16x2(uint32_t two_codes) {
+    const uint16_t v = (uint16_t)two_codes;
+    uint32_t d;
+    if (F8 == 1)
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(v));
+    else
+        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(d) : "h"(v));
+    return d;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Widen row r of the 8-bit V tile at v8 ([BN keys x D bytes], rows of 128 bytes in the TMA's
+// 128-byte swizzle: 16-byte unit u of row r at r*128 + ((u ^ (r & 7)) << 4)) into the 16-bit
+// V tile at v16, in the layout a TMA load of 16-bit V would have produced: D/64 chunks of
+// [BN rows x 128 bytes], unit u of row r of chunk c at c*BN*128 + r*128 + ((u ^ (r & 7)) << 4).
+template <int D, int F8>
+__device__ __forceinline__ void widen_v_rows(uint32_t v8, uint32_t v16, int r) {
+    static_assert(D == 128, "8-bit inputs: one 128-byte row per key");
+    {
+        const uint32_t sw = (uint32_t)(r & 7);
+#pragma unroll 2
+        for (int u = 0; u < 8; ++u) {  // 16 codes: d = 16u .. 16u + 15
+            uint32_t w[4];
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                         : "r"(v8 + r * 128 + ((u ^ sw) << 4))
+                         : "memory");
+            uint32_t h[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                h[2 * i] = f8x2_to_f16x2<F8>(w[i]);
+                h[2 * i + 1] = f8x2_to_f16x2<F8>(w[i] >> 16);
+            }
+            const int c = u >> 2;                 // 64-column chunk
+            const uint32_t u0 = (uint32_t)((u & 3) * 2);  // first 16-byte unit of these 16 values
+            const uint32_t base = v16 + c * (BN * 128) + r * 128;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(base + ((u0 ^ sw) << 4)), "r"(h[0]), "r"(h[1]),
+                         "r"(h[2]), "r"(h[3])
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(base + (((u0 + 1) ^ sw) << 4)), "r"(h[4]),
+                         "r"(h[5]), "r"(h[6]), "r"(h[7])
+                         : "memory");
+        }
+    }
 }
 
 // Work order of packed sequences, built once per CTA in shared memory by build_packed_order.
@@ -341,11 +432,11 @@ __device__ __forceinline__ float ex2_poly(float x) {
     return __uint_as_float(__float_as_uint(q) + (__float_as_uint(t) << 23));
 }
 
-template <int D, int POLY_EVERY>
+template <int D, int POLY_EVERY, int F8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using L = Layout<D>;
+    using L = Layout<D, F8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
@@ -366,6 +457,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < L::kEntries; ++i) {
             mbar_init(&bars[L::bEFull + i], 1);
             mbar_init(&bars[L::bEEmpty + i], 2);  // released by both MMA warps
+            if (F8) {
+                mbar_init(&bars[L::bV8Full + i], 1);
+                mbar_init(&bars[L::bVConv + i], 4);  // the four widening (epilogue) warps
+            }
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[L::bSFull + s], 1);
@@ -413,10 +508,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const uint64_t wd = p.watchdog_ns;
 
-    // Register split per warpgroup: producer/MMA 80, softmax 184 each, epilogue 64
-    // (sum 512 = 4 x 128, the registers the CTA is launched with).
+    // Register split per warpgroup: producer/MMA 80, softmax 184 each, epilogue 64; with 8-bit
+    // inputs 72, 184, 184, 72 (the epilogue warps also widen V). Either sums to 512 = 4 x 128,
+    // the registers the CTA is launched with.
     if (warp < 4) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
+        if constexpr (F8 != 0)
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
+        else
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
         // The whole warp walks the schedule so that addresses and coordinates stay
@@ -431,6 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             Tile t;
             get_tile(p, po, w, t);
             const int nmax = max(t.n[0], t.n[1]);
+            if (nmax == 0) continue;  // no visible key in the block: the other roles skip it too
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
                 if (!ok || t.n[s] == 0) continue;
@@ -441,27 +541,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx_by(leader, &bars[L::bQFull + s], L::kQBytes);
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_3d_by(leader, dst + c * L::kChunkBytesQ, &tmQ, &bars[L::bQFull + s], c * 64, t.h,
-                                   t.q0 + t.r0 + s * BM);
+                    tma_load_3d_by(leader, dst + c * L::kChunkBytesQ, &tmQ, &bars[L::bQFull + s],
+                                   c * (128 / L::kElem), t.h, t.q0 + t.r0 + s * BM);
                 ATTN_TL(0, 10 + s, w, tq, clock64());
             }
             for (int e = 0; e <= nmax && ok; ++e) {
                 ATTN_TL_DECL(long long tw = clock64());
                 if (!(ok = warp_wait(&bars[L::bEEmpty + stage], phase ^ 1u, abort_flag, wd))) break;
                 uint8_t* ent = smem + L::kKVOff + stage * L::kEntryBytes;
-                const uint32_t bytes = (e < nmax ? (uint32_t)L::kKVBytes : 0u) + (e >= 1 ? (uint32_t)L::kKVBytes : 0u);
+                const uint32_t bytes = (e < nmax ? (uint32_t)L::kKBytes : 0u) + (!F8 && e >= 1 ? (uint32_t)L::kVBytes : 0u);
                 mbar_arrive_expect_tx_by(leader, &bars[L::bEFull + stage], bytes);
                 if (e < nmax) {
 #pragma unroll
                     for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d_by(leader, ent + c * L::kChunkBytesKV, &tmK, &bars[L::bEFull + stage], c * 64, t.kvh,
-                                       t.k0 + e * BN);
+                        tma_load_3d_by(leader, ent + c * L::kChunkBytesKV, &tmK, &bars[L::bEFull + stage],
+                                       c * (128 / L::kElem), t.kvh, t.k0 + e * BN);
                 }
-                if (e >= 1) {
+                if (e >= 1) {  // 16-bit V tile, or the 8-bit tile it is widened from (own barrier)
+                    constexpr int kBoxes = F8 ? L::kChunks : L::kVChunks;
+                    uint64_t* vbar = &bars[(F8 ? L::bV8Full : L::bEFull) + stage];
+                    if (F8) mbar_arrive_expect_tx_by(leader, vbar, L::kV8Bytes);
 #pragma unroll
-                    for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d_by(leader, ent + L::kKVBytes + c * L::kChunkBytesKV, &tmV, &bars[L::bEFull + stage],
-                                       c * 64, t.kvh, t.k0 + (e - 1) * BN);
+                    for (int c = 0; c < kBoxes; ++c)
+                        tma_load_3d_by(leader, ent + (F8 ? L::kV8Off : L::kVOff) + c * L::kChunkBytesKV, &tmV, vbar,
+                                       c * (128 / L::kElem), t.kvh, t.k0 + (e - 1) * BN);
                 }
                 ATTN_TL(0, 0, e, tw, clock64());
                 ++issued;
@@ -497,12 +600,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // descriptors and slots warp-uniform.
         const int s = warp - 1;
         const uint32_t leader = lane == 0;
-        constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0);
-        constexpr uint32_t idO = idesc_bf16_f32(BM, D, 1);
+        constexpr uint32_t idS = F8 ? idesc_f8_f32(BM, BN, F8 - 1) : idesc_bf16_f32(BM, BN, 0);
+        constexpr uint32_t idO = F8 ? idesc_f16_f32(BM, D, 1) : idesc_bf16_f32(BM, D, 1);
         const uint32_t colS = s ? kColS1 : kColS0;
         const uint32_t colO = s ? kColO1 : kColO0;
         uint32_t stage = 0, phase = 0;
         uint32_t qf = 0, pf = 0, oe = 0, burst = 0;
+        uint32_t vcv = 0;  // 8-bit inputs: phase bit per ring slot of the V-widened barrier
         const uint32_t q_base = smem_u32(smem + L::kQOff) + s * L::kQBytes;
         const uint32_t kv_base = smem_u32(smem + L::kKVOff);
         const uint64_t dq = smem_desc_sw128(q_base, 16, 1024);
@@ -535,6 +639,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         oe ^= 1u;
                     }
                 }
+                if (F8 && n >= 1) {  // every entry that carries V: wait until it has been widened
+                    if (!(ok = warp_wait(&bars[L::bVConv + e_slot], (vcv >> e_slot) & 1u, abort_flag, wd))) break;
+                    vcv ^= 1u << e_slot;
+                }
                 // token: burst 0 of step n follows burst 1 of step n-1; burst 1 follows burst 0
                 if (s == 0) {
                     if (burst > 0 && !(ok = warp_wait(&bars[L::bIssued + 1], (burst - 1) & 1u, abort_flag, wd))) break;
@@ -545,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t ent_off = e_slot * L::kEntryBytes;
                 if (do_pv) {
-                    const uint64_t vd = dv0 + (uint64_t)((ent_off + L::kKVBytes) >> 4);
+                    const uint64_t vd = dv0 + (uint64_t)((ent_off + L::kVOff) >> 4);
                     const uint32_t acc0 = n - 1 > 0 ? 1u : 0u;
 #pragma unroll
                     for (int k = 0; k < 6; ++k)  // keys 0-95: P stage 1
@@ -559,11 +667,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO, 1u);
                 }
                 if (do_s) {
+                    // K steps of 32 bytes (16 bf16 or 32 8-bit elements), 4 per 128-byte chunk
                     const uint64_t kd = dk0 + (uint64_t)(ent_off >> 4);
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
+                    for (int k = 0; k < D * L::kElem / 32; ++k) {
                         const uint64_t off = (uint64_t)(((k >> 2) * L::kChunkBytesQ + (k & 3) * 32) >> 4);
-                        tc_mma_ss_by(leader, tmem + colS, dq + off, kd + off, idS, k > 0 ? 1u : 0u);
+                        if (F8)
+                            tc_mma_ss_f8_by(leader, tmem + colS, dq + off, kd + off, idS, k > 0 ? 1u : 0u);
+                        else
+                            tc_mma_ss_by(leader, tmem + colS, dq + off, kd + off, idS, k > 0 ? 1u : 0u);
                     }
                 }
                 __syncwarp();
@@ -684,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int a = ((c >> 1) & 3) * 2;
                     fadd2(sum[a], sum[a + 1], sum[a], sum[a + 1], p0, p1);
-                    pk[c >> 1] = pack_bf16x2(p0, p1);
+                    pk[c >> 1] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
                 };
 #pragma unroll
                 for (int c = 0; c < 3 * BN / 4; c += 2) exp_pair(c);
@@ -723,17 +835,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------------ epilogue
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
+        if constexpr (F8 != 0)
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");  // also widens the 8-bit V tiles
+        else
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         uint32_t of[2] = {0, 0}, sp[2] = {0, 0};
+        uint32_t stage = 0, v8ph = 0;  // 8-bit inputs: ring slot and per-slot phase bits of bV8Full
         bool ok = true;
         for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
             const int w = snake_index(r);
             if (w >= total) continue;
             Tile t;
             get_tile(p, po, w, t);
+            if constexpr (F8 != 0) {
+                // Widen this tile's 8-bit V tiles first (rows 32*quarter .. +31 of each), in ring
+                // order. The MMA warps wait for them (bVConv) before each P V product and only
+                // then release the entry, so the 8-bit tile is never overwritten while read here.
+                const int nmax = max(t.n[0], t.n[1]);
+                for (int e = 0; e <= nmax && nmax > 0 && ok; ++e) {
+                    const uint32_t e_slot = stage;
+                    if (++stage == (uint32_t)L::kEntries) stage = 0;
+                    if (e == 0) continue;
+                    if (!(ok = warp_wait(&bars[L::bV8Full + e_slot], (v8ph >> e_slot) & 1u, abort_flag, wd))) break;
+                    v8ph ^= 1u << e_slot;
+                    const uint32_t ent = smem_u32(smem + L::kKVOff) + e_slot * L::kEntryBytes;
+                    widen_v_rows<D, F8>(ent + L::kV8Off, ent + L::kVOff, quarter * 32 + lane);
+                    fence_proxy_async_smem();  // make the generic-proxy stores visible to the MMA
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[L::bVConv + e_slot]);
+                }
+                if (!ok) break;
+            }
             for (int s = 0; s < 2; ++s) {
                 const int qrow = t.r0 + s * BM + row;
                 if (t.r0 + s * BM >= t.Lq) continue;
@@ -756,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const float m = st_m[s * BM + row];
                 const float l = st_l[s * BM + row];
-                const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+                const float inv = l > 0.0f ? p.out_scale / l : 0.0f;
                 const uint32_t tO = tmem + lane_off + (s ? kColO1 : kColO0);
 #pragma unroll 1
                 for (int c = 0; c < D; c += 32) {
@@ -794,19 +929,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, int POLY>
+template <int D, int POLY, int F8>
 cudaError_t launch_t(const FwdTmaps& tm, const FwdParams& p, int grid, cudaStream_t stream) {
-    using L = Layout<D>;
+    using L = Layout<D, F8>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(attn_fwd_kernel<D, POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+        e = cudaFuncSetAttribute(attn_fwd_kernel<D, POLY, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    attn_fwd_kernel<D, POLY><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.k, tm.v, p);
+    attn_fwd_kernel<D, POLY, F8><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.k, tm.v, p);
     return cudaGetLastError();
 }
 
@@ -817,9 +952,15 @@ int fwd_max_varlen_batch() { return kMaxVarlenB; }
 cudaError_t launch_attn_fwd(const FwdTmaps& tm, const FwdParams& p, int d, int exp_poly, int grid,
                             cudaStream_t stream) {
     if (d == 128) {
-        return exp_poly ? launch_t<128, 8>(tm, p, grid, stream) : launch_t<128, 0>(tm, p, grid, stream);
+        return exp_poly ? launch_t<128, 8, 0>(tm, p, grid, stream) : launch_t<128, 0, 0>(tm, p, grid, stream);
     }
-    return exp_poly ? launch_t<64, 8>(tm, p, grid, stream) : launch_t<64, 0>(tm, p, grid, stream);
+    return exp_poly ? launch_t<64, 8, 0>(tm, p, grid, stream) : launch_t<64, 0, 0>(tm, p, grid, stream);
+}
+
+cudaError_t launch_attn_fwd_fp8(const FwdTmaps& tm, const FwdParams& p, int d, int fmt, int grid,
+                                cudaStream_t stream) {
+    if (d != 128) return cudaErrorInvalidValue;
+    return fmt == 0 ? launch_t<128, 0, 1>(tm, p, grid, stream) : launch_t<128, 0, 2>(tm, p, grid, stream);
 }
 
 // ------------------------------------------------------------------------------ diagnostics

@@ -28,6 +28,7 @@ struct FwdParams {
     float scale;        // softmax scale applied to q.k
     float scale_log2;   // scale * log2(e)
     float rescale_thr;  // rescale O only when the row max grows by more than this (base-2 exponent units)
+    float out_scale;    // multiplies O at the end (8-bit inputs: the value descale; else 1)
     int sec_q;          // scheduling section, a multiple of G: dense, (batch, head) pairs; packed, query heads (divides Hq)
     int total_tiles;    // dense: number of work tiles; varlen: ignored (computed on device)
     int* status;
@@ -42,6 +43,10 @@ struct FwdTmaps {
 // Launch the forward kernel for head dim d in {64, 128}; exp_poly selects the MUFU/polynomial split.
 cudaError_t launch_attn_fwd(const FwdTmaps& tm, const FwdParams& p, int d, int exp_poly, int grid,
                             cudaStream_t stream);
+// 8-bit Q/K/V codes (fmt 0 = e4m3, 1 = e5m2), d = 128; p.scale already includes the q and k
+// descales and p.out_scale is the v descale.
+cudaError_t launch_attn_fwd_fp8(const FwdTmaps& tm, const FwdParams& p, int d, int fmt, int grid,
+                                cudaStream_t stream);
 int fwd_max_varlen_batch();
 
 struct DecodeParams {

@@ -48,6 +48,10 @@ typedef int attn_status_t;
 #define ATTN_ERR_BAD_ARG (-8)           /* an unknown option name or an invalid value */
 #define ATTN_ERR_SCRATCH_TOO_SMALL (-9) /* attn_decode_paged_noalloc: sizes exceed its fixed scratch */
 
+/* 8-bit floating-point formats (OCP FP8) of attn_fwd_fp8 and attn_decode_paged_fp8 */
+#define ATTN_FP8_E4M3 0 /* 4 exponent bits (bias 7), 3 mantissa bits, largest 448, no infinities */
+#define ATTN_FP8_E5M2 1 /* 5 exponent bits (bias 15), 2 mantissa bits, largest 57344 */
+
 /*
  * Forward attention ("FlashAttention: not computing less, moving less", section 01
  * formula O = softmax(QK^T / sqrt(d)) V with a general scale; section 02 online-softmax
@@ -80,6 +84,26 @@ typedef int attn_status_t;
  */
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                        int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens, void* stream);
+
+/*
+ * attn_fwd on Q/K/V given in 8-bit floating point ("Faster, more flexible FA4 for LLM
+ * inference", PR 2109: e4m3 or e5m2 inputs).
+ *
+ * q, k, v     device, 8-bit codes in the layouts of attn_fwd, OCP FP8 format fp8_format
+ *             (ATTN_FP8_E4M3 or ATTN_FP8_E5M2, defined below); each tensor stands for its
+ *             descale times the decoded values (one factor per tensor, finite)
+ * o, lse      bf16 [T, Hq, d] and fp32 [T, Hq] as for attn_fwd
+ * d           128 only (other values: ATTN_ERR_BAD_SHAPE)
+ * Everything else (masks, packed sequences, GQA, alignment, errors) is as for attn_fwd.
+ * An unknown format, a non-finite descale or a score scale that overflows a float is
+ * ATTN_ERR_BAD_ARG.
+ * Arithmetic: S = Q K^T on the tensor cores in 8-bit floating point with fp32 accumulation
+ * (products of 8-bit values are exact); the softmax as for attn_fwd; P rounded to f16; V
+ * widened exactly to f16 in shared memory; O += P V in f16 with fp32 accumulation.
+ */
+attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                           int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens, void* stream,
+                           int fp8_format, float q_descale, float k_descale, float v_descale);
 
 /*
  * Paged-KV decode ("Faster, more flexible FA4 for LLM inference": PR 1999/2104 arbitrary
@@ -130,8 +154,6 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
  * |q| in [2^-14, 65504] (smaller magnitudes lose low bits, larger ones overflow), and the
  * probabilities are rounded to f16 before the P V product.
  */
-#define ATTN_FP8_E4M3 0
-#define ATTN_FP8_E5M2 1
 attn_status_t attn_decode_paged_fp8(const void* q, const void* k_cache, const void* v_cache, const int* page_table,
                                     const int* seqlens, int page_size, void* o, float* lse, void* stream, int B,
                                     int Hq, int Hkv, int d, int max_pages_per_seq, int num_pages, float scale,
