@@ -12,7 +12,8 @@ visible (query, key) pair and head); the decode leg's HBM GB/s is reported under
 inputs are larger than L2, so no flush is needed between steps.
 After the timed steps, attn_decode_paged_fp8 runs the same decode workload with
 e4m3 key/value caches for as many timed calls; its GB/s (algorithmic bytes of the
-8-bit caches) is reported under ``decode_fp8``, outside ``value``.
+8-bit caches) is reported under ``decode_fp8``, outside ``value``. Likewise
+attn_fwd_fp8 on the long causal prefill with e4m3 Q/K/V, under ``prefill_fp8``.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 With --gpus N > 1 the script runs under torch.distributed.run, one rank per GPU,
@@ -44,6 +45,7 @@ METRIC = "attn fwd TFLOP/s (bf16 hd128 causal) & paged-decode HBM GB/s vs roofli
 FWD_KERNEL = "attn_fwd_kernel"
 DEC_KERNEL = "decode_split_kernel"
 DEC8_KERNEL = "decode_split_fp8_kernel"
+FWD8_KERNEL = "attn_fwd_kernel<128, 0, 1>"
 
 
 def parse():
@@ -73,7 +75,8 @@ def peaks():
 
 KERNEL_SOURCES = {FWD_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"],
                   DEC_KERNEL: ["attn_decode.cu", "ptx.cuh", "kernels.cuh"],
-                  DEC8_KERNEL: ["attn_decode.cu", "ptx.cuh", "kernels.cuh"]}
+                  DEC8_KERNEL: ["attn_decode.cu", "ptx.cuh", "kernels.cuh"],
+                  FWD8_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"]}
 
 
 def source_sha(kernel: str) -> str:
@@ -354,6 +357,16 @@ def run_ours(args):
         KC8, VC8 = torch.from_numpy(kc8).to(dev), torch.from_numpy(vc8).to(dev)
     stream.synchronize()
 
+    # FP8 (e4m3) Q/K/V of the same long causal prefill: a leg of its own, timed after the step
+    q8, k8, v8, qds, kds8, vds8 = fc.generate_fp8("e4m3")
+    with torch.cuda.stream(stream):
+        Q8, K8, V8 = (torch.from_numpy(a).to(dev) for a in (q8, k8, v8))
+    stream.synchronize()
+
+    def fwd8():
+        A.attn_fwd_fp8(Q8, K8, V8, O, LSE, fc.B, fc.Hq, fc.Hkv, fc.Nq, fc.Nk, fc.d, fc.scale, fc.causal, None,
+                       s_handle, "e4m3", qds, kds8, vds8)
+
     def dec8():
         A.attn_decode_paged_fp8(DQ, KC8, VC8, PT, SL, dc8.page_size, DO, DLSE, s_handle, dc8.B, dc8.Hq, dc8.Hkv,
                                 dc8.d, dc8.max_pages, dc8.num_pages, dc8.scale, 0, dc8.kv_fmt, kds, vds)
@@ -413,6 +426,21 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device status after the FP8 decode leg: {A.status_string(st)}")
     dec8_ms = max_over_ranks(s8.elapsed_time(e8), world, dev)
+
+    # FP8 forward leg
+    for _ in range(args.warmup):
+        fwd8()
+    barrier()
+    sf8, ef8 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sf8.record(stream)
+    for _ in range(K_):
+        fwd8()
+    ef8.record(stream)
+    barrier()
+    st = A.attn_get_device_status(s_handle)
+    if st != 0:
+        raise RuntimeError(f"device status after the FP8 forward leg: {A.status_string(st)}")
+    fwd8_ms = max_over_ranks(sf8.elapsed_time(ef8), world, dev)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -494,6 +522,16 @@ def run_ours(args):
                        "roofline": {"bound": "hbm", "achieved": d8_ach, "peak": hbm, "unit": "GB/s",
                                     "frac": d8_ach / hbm, "traffic": ncu_traffic(DEC8_KERNEL), "kernel": DEC8_KERNEL,
                                     "peak_source": f"{src} copy"}},
+        "prefill_fp8": {"value": world * K_ * fc.flops() / (fwd8_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                        "ms_per_call": fwd8_ms / K_, "calls": K_, "gpu_launches": K_,
+                        "workload": "long causal prefill as above with e4m3 Q/K/V (per-tensor descales)",
+                        "speedup_vs_bf16_prefill": (fwd_ms / K_) / (fwd8_ms / K_),
+                        "roofline": {"bound": "tensor", "achieved": fc.flops() / (fwd8_ms / K_ * 1e-3) / 1e12,
+                                     "peak": bf16 * 4.0 / 3.0, "unit": "TFLOP/s",
+                                     "frac": fc.flops() / (fwd8_ms / K_ * 1e-3) / 1e12 / (bf16 * 4.0 / 3.0),
+                                     "traffic": ncu_traffic(FWD8_KERNEL), "kernel": FWD8_KERNEL,
+                                     "peak_source": f"{src} bf16 burst x 4/3 (half the FLOPs in fp8 at 2x, half in "
+                                                    "f16 at 1x)"}},
         "prefill_ms_per_step": fwd_ms / K_,
         "gpu_launches": K_ * launches_per_step,
         "clocks": clk.summary(),
