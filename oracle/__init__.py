@@ -19,7 +19,9 @@ Contents
     factor per tensor (a reading: the pages fix no scaling scheme), then the
     same three-pass definition runs in float64.
 ``attn_fwd_f64`` / ``attn_fwd_fp8``
-    The forward definition on float64 inputs; ``attn_fwd_fp8`` decodes 8-bit
+    The forward definition on float64 inputs, also with values (and outputs)
+    narrower than queries and keys, e.g. head dims (192, 128) ("FlashAttention-4:
+    Blackwell algorithm-pipeline co-design", performance section); ``attn_fwd_fp8`` decodes 8-bit
     floating-point Q/K/V codes (PR 2109 of the same page) and applies one descale
     per tensor before it.
 ``online_attention``
@@ -90,7 +92,7 @@ def _load():
             lib.oracle_attn_decode_paged.restype = i
             lib.oracle_attn_decode_paged_fp8.argtypes = [vp, vp, vp, i, d, d, vp, vp, i, vp, vp, i, i, i, i, i, d, i]
             lib.oracle_attn_decode_paged_fp8.restype = i
-            lib.oracle_attn_fwd_f64.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, d, i, vp, vp, i64, i]
+            lib.oracle_attn_fwd_f64.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, d, i, vp, vp, i64, i]
             lib.oracle_attn_fwd_f64.restype = i
             lib.oracle_fp8_values.argtypes = [vp, vp, i64, i]
             lib.oracle_fp8_values.restype = None
@@ -149,22 +151,24 @@ def attn_fwd(q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens=None, row
     return o, lse
 
 
-def attn_fwd_f64(q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens=None, rows=None, n_threads=None):
-    """attn_fwd on float64 inputs (same layouts, masks and ``rows`` as ``attn_fwd``)."""
+def attn_fwd_f64(q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens=None, rows=None, n_threads=None, dv=None):
+    """attn_fwd on float64 inputs (same layouts, masks and ``rows`` as ``attn_fwd``). ``dv``
+    (default ``d``) is the value / output width: q, k are d wide, v and o dv wide."""
+    dv = d if dv is None else dv
     q, k, v = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v))
     cu = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, dtype=np.int32)
     T = int(cu[-1]) if cu is not None else B * Nq
     if rows is None:
-        o = np.zeros((T, Hq, d), dtype=np.float64)
+        o = np.zeros((T, Hq, dv), dtype=np.float64)
         lse = np.zeros((T, Hq), dtype=np.float64)
         rp, nr = None, 0
     else:
         rows = np.ascontiguousarray(rows, dtype=np.int64)
-        o = np.zeros((len(rows), d), dtype=np.float64)
+        o = np.zeros((len(rows), dv), dtype=np.float64)
         lse = np.zeros((len(rows),), dtype=np.float64)
         rp, nr = rows.ctypes.data, len(rows)
     rc = _load().oracle_attn_fwd_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data, o.ctypes.data, lse.ctypes.data,
-                                     B, Hq, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                                     B, Hq, Hkv, Nq, Nk, d, dv, float(scale), int(bool(causal)),
                                      None if cu is None else cu.ctypes.data, rp, nr, n_threads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle_attn_fwd_f64 rejected its arguments (rc={rc})")

@@ -77,8 +77,8 @@ static void attend_row(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
     *lse = m + log(l);
 }
 
-static void attend_row_f64(const double* qd, const double* k, const double* v, int64_t stride, int64_t n, int d,
-                           double scale, double* s, double* o, double* lse);
+static void attend_row_f64(const double* qd, const double* k, const double* v, int64_t kstride, int64_t vstride,
+                           int64_t n, int d, int dv, double scale, double* s, double* o, double* lse);
 
 /* ------------------------------------------------------------------ forward */
 
@@ -87,6 +87,7 @@ typedef struct {
     const double *qf, *kf, *vf; /* float64 inputs (oracle_attn_fwd_f64) */
     double *o, *lse;
     int B, Hq, Hkv, Nq, Nk, d, causal;
+    int dv; /* value / output width (oracle_attn_fwd_f64); d for the others */
     double scale;
     const int32_t* cu; /* host cu_seqlens or NULL */
     const int64_t* rows;  /* optional (token * Hq + head) list */
@@ -312,17 +313,18 @@ void oracle_fp8_values(const uint8_t* c, double* out, int64_t n, int fmt) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_fp8_value(c[i], fmt);
 }
 
-/* One query row (float64) against n keys/values given as float64 rows of stride `stride`. */
-static void attend_row_f64(const double* qd, const double* k, const double* v, int64_t stride, int64_t n, int d,
-                           double scale, double* s, double* o, double* lse) {
+/* One query row (float64, d wide) against n keys (d wide, row stride kstride) and values
+ * (dv wide, row stride vstride) given as float64 rows; o is dv wide. */
+static void attend_row_f64(const double* qd, const double* k, const double* v, int64_t kstride, int64_t vstride,
+                           int64_t n, int d, int dv, double scale, double* s, double* o, double* lse) {
     if (n <= 0) {
-        for (int c = 0; c < d; ++c) o[c] = 0.0;
+        for (int c = 0; c < dv; ++c) o[c] = 0.0;
         *lse = -INFINITY;
         return;
     }
     for (int64_t j = 0; j < n; ++j) {
         double acc = 0.0;
-        for (int c = 0; c < d; ++c) acc += qd[c] * k[j * stride + c];
+        for (int c = 0; c < d; ++c) acc += qd[c] * k[j * kstride + c];
         s[j] = scale * acc;
     }
     double m = s[0];
@@ -330,10 +332,10 @@ static void attend_row_f64(const double* qd, const double* k, const double* v, i
         if (s[j] > m) m = s[j];
     double l = 0.0;
     for (int64_t j = 0; j < n; ++j) l += exp(s[j] - m);
-    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (int c = 0; c < dv; ++c) o[c] = 0.0;
     for (int64_t j = 0; j < n; ++j) {
         const double p = exp(s[j] - m) / l;
-        for (int c = 0; c < d; ++c) o[c] += p * v[j * stride + c];
+        for (int c = 0; c < dv; ++c) o[c] += p * v[j * vstride + c];
     }
     *lse = m + log(l);
 }
@@ -389,8 +391,8 @@ static void* dec8_worker(void* p) {
         for (int h = 0; h < J->Hq; ++h) {
             const int g = h / G;
             for (int c = 0; c < d; ++c) qd[c] = bf16d(J->q[(b * J->Hq + h) * d + c]);
-            attend_row_f64(qd, kb + (size_t)g * d, vb + (size_t)g * d, (int64_t)row_elems, L, d, J->scale, s,
-                           J->o + (b * J->Hq + h) * d, J->lse + b * J->Hq + h);
+            attend_row_f64(qd, kb + (size_t)g * d, vb + (size_t)g * d, (int64_t)row_elems, (int64_t)row_elems, L, d, d,
+                           J->scale, s, J->o + (b * J->Hq + h) * d, J->lse + b * J->Hq + h);
         }
         free(kb); free(vb); free(s); free(qd);
     }
@@ -426,7 +428,10 @@ int oracle_attn_decode_paged_fp8(const uint16_t* q, const uint8_t* k_cache, cons
  * The forward definition on float64 inputs, for inputs that are not bf16: 8-bit
  * floating-point Q/K/V ("Faster, more flexible FA4 for LLM inference", PR 2109) are
  * decoded and multiplied by their descales by the caller, then passed here. Same
- * layouts, masks and rows as oracle_attn_fwd.
+ * layouts, masks and rows as oracle_attn_fwd, except that values (and so outputs) may be
+ * dv wide while queries and keys are d wide: head dims (d, dv) such as DeepSeek-V3's
+ * (192, 128) ("FlashAttention-4: Blackwell algorithm-pipeline co-design", performance
+ * section). The definition is unchanged: scores use d, the weighted sum runs over dv.
  */
 static void* fwd_f64_worker(void* p) {
     fwd_job_t* J = (fwd_job_t*)p;
@@ -457,23 +462,24 @@ static void* fwd_f64_worker(void* p) {
         }
         if (n_vis < 0) n_vis = 0;
         const int g = h / G;
-        const int64_t kv_stride = (int64_t)J->Hkv * d;
-        attend_row_f64(J->qf + (t * J->Hq + h) * d, J->kf + k0 * kv_stride + (int64_t)g * d,
-                       J->vf + k0 * kv_stride + (int64_t)g * d, kv_stride, n_vis, d, J->scale, s, J->o + it * d,
-                       J->lse + it);
+        const int dv = J->dv;
+        const int64_t k_stride = (int64_t)J->Hkv * d, v_stride = (int64_t)J->Hkv * dv;
+        attend_row_f64(J->qf + (t * J->Hq + h) * d, J->kf + k0 * k_stride + (int64_t)g * d,
+                       J->vf + k0 * v_stride + (int64_t)g * dv, k_stride, v_stride, n_vis, d, dv, J->scale, s,
+                       J->o + it * dv, J->lse + it);
     }
     free(s);
     return NULL;
 }
 
 int oracle_attn_fwd_f64(const double* q, const double* k, const double* v, double* o, double* lse, int B, int Hq,
-                        int Hkv, int Nq, int Nk, int d, double scale, int causal, const int32_t* cu_seqlens,
+                        int Hkv, int Nq, int Nk, int d, int dv, double scale, int causal, const int32_t* cu_seqlens,
                         const int64_t* rows, int64_t n_rows, int n_threads) {
-    if (!q || !k || !v || !o || !lse || B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0) return -1;
+    if (!q || !k || !v || !o || !lse || B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || dv <= 0) return -1;
     fwd_job_t J;
     memset(&J, 0, sizeof J);
     J.qf = q; J.kf = k; J.vf = v; J.o = o; J.lse = lse;
-    J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.Nq = Nq; J.Nk = Nk; J.d = d; J.causal = causal;
+    J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.Nq = Nq; J.Nk = Nk; J.d = d; J.dv = dv; J.causal = causal;
     J.scale = scale; J.cu = cu_seqlens; J.rows = rows; J.n_rows = n_rows;
     if (cu_seqlens) {
         int64_t mx = 0;

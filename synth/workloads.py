@@ -44,6 +44,11 @@ class PrefillCase:
     seed: int
     q_mult: float = 1.0
     cu_seqlens: np.ndarray | None = None  # int32 [B+1] for packed sequences
+    dv: int | None = None  # value / output width when it differs from d (e.g. d = 192, dv = 128)
+
+    @property
+    def d_v(self) -> int:
+        return self.d if self.dv is None else self.dv
 
     @property
     def total_q(self) -> int:
@@ -70,7 +75,7 @@ class PrefillCase:
         """(q [Tq, Hq, d], k [Tk, Hkv, d], v [Tk, Hkv, d]) as bf16 bit patterns (uint16)."""
         q = normal_bf16((self.total_q, self.Hq, self.d), sub_seed(self.seed, _Q), self.q_mult)
         k = normal_bf16((self.total_k, self.Hkv, self.d), sub_seed(self.seed, _K))
-        v = normal_bf16((self.total_k, self.Hkv, self.d), sub_seed(self.seed, _V))
+        v = normal_bf16((self.total_k, self.Hkv, self.d_v), sub_seed(self.seed, _V))
         return q, k, v
 
     def seq_lens(self):
@@ -91,12 +96,12 @@ class PrefillCase:
         return total
 
     def flops(self) -> int:
-        """Algorithmic FLOPs: two products (QK^T and PV) of 2*d each per visible pair and query head."""
-        return 4 * self.d * self.Hq * self.visible_pairs()
+        """Algorithmic FLOPs per visible pair and query head: 2*d for QK^T and 2*dv for PV."""
+        return 2 * (self.d + self.d_v) * self.Hq * self.visible_pairs()
 
     def bytes(self) -> int:
         """Algorithmic HBM bytes: read q, k, v once and write o (bf16) and lse (fp32) once."""
-        return (2 * self.total_q * self.Hq * self.d * 2 + 2 * self.total_k * self.Hkv * self.d * 2
+        return ((self.total_q * self.Hq * (self.d + self.d_v) + self.total_k * self.Hkv * (self.d + self.d_v)) * 2
                 + 4 * self.total_q * self.Hq)
 
 

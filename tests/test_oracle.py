@@ -439,6 +439,33 @@ def test_fwd_f64_equals_bf16_forward_on_the_same_values():
         np.testing.assert_array_equal(l1, l2)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_narrow_values_match_torch_sdpa_float64(causal):
+    """Head dims (d, dv) = (48, 32): PyTorch's float64 SDPA accepts values narrower than keys."""
+    c = W.PrefillCase("dv", 1, 4, 2, 40, 57, 48, 0.15, causal, 9, dv=32)
+    q, k, v = c.generate()
+    f = lambda a: synth.bf16_to_f32(a).astype(np.float64)
+    o, lse = oracle.attn_fwd_f64(f(q), f(k), f(v), c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d, c.scale, causal, dv=32)
+    o_ref, lse_ref = _torch_reference(q, k, v, c.scale, causal, c.Nq, c.Nk, c.Hq // c.Hkv)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_value_columns_are_independent():
+    """Splitting V by columns splits O by columns: the weights depend on Q and K only."""
+    c = W.PrefillCase("split", 2, 2, 1, 33, 33, 24, 0.3, True, 10, dv=40)
+    q, k, v = c.generate()
+    f = lambda a: synth.bf16_to_f32(a).astype(np.float64)
+    args = (c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d, c.scale, True)
+    o, lse = oracle.attn_fwd_f64(f(q), f(k), f(v), *args, dv=40)
+    oa, la = oracle.attn_fwd_f64(f(q), f(k), f(v)[..., :16], *args, dv=16)
+    ob, lb = oracle.attn_fwd_f64(f(q), f(k), f(v)[..., 16:], *args, dv=24)
+    np.testing.assert_array_equal(o[..., :16], oa)
+    np.testing.assert_array_equal(o[..., 16:], ob)
+    np.testing.assert_array_equal(lse, la)
+    np.testing.assert_array_equal(lse, lb)
+
+
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 def test_fp8_forward_equals_bf16_forward_of_the_same_values(fmt):
     """With power-of-two descales every FP8 value times its descale is exact in bf16, so the
