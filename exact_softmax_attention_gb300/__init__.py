@@ -34,7 +34,7 @@ ATTN_FP8_E5M2 = 1
 FP8_FORMATS = {"e4m3": ATTN_FP8_E4M3, "e5m2": ATTN_FP8_E5M2}
 
 #: every symbol the header declares
-EXPORTS = ("attn_fwd", "attn_fwd_fp8", "attn_decode_paged", "attn_decode_paged_fp8", "attn_decode_paged_noalloc", "attn_decode_plan", "attn_status_string", "attn_get_device_status",
+EXPORTS = ("attn_fwd", "attn_fwd_hd", "attn_fwd_fp8", "attn_decode_paged", "attn_decode_paged_fp8", "attn_decode_paged_noalloc", "attn_decode_plan", "attn_status_string", "attn_get_device_status",
            "attn_set_option", "attn_get_option", "attn_read_counters", "attn_debug_exp2", "attn_debug_watchdog",
            "attn_version")
 
@@ -53,6 +53,8 @@ lib = ctypes.CDLL(LIB_PATH)
 _vp, _i, _f, _d = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double
 lib.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]
 lib.attn_fwd.restype = _i
+lib.attn_fwd_hd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]
+lib.attn_fwd_hd.restype = _i
 lib.attn_fwd_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _i, _f, _f, _f]
 lib.attn_fwd_fp8.restype = _i
 lib.attn_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i]
@@ -120,6 +122,15 @@ def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens=N
     rc = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq), int(Hkv), int(Nq), int(Nk),
                       int(d), float(scale), int(causal), _ptr(cu_seqlens), _stream(stream))
     return _check(rc, "attn_fwd", raise_on_error)
+
+
+def attn_fwd_hd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, dv, scale, causal, cu_seqlens=None, stream=None,
+                raise_on_error=True):
+    """Forward with values narrower than queries and keys, (d, dv) = (192, 128); see
+    ``attn_fwd_hd`` in include/attn.h."""
+    rc = lib.attn_fwd_hd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq), int(Hkv), int(Nq), int(Nk),
+                         int(d), int(dv), float(scale), int(causal), _ptr(cu_seqlens), _stream(stream))
+    return _check(rc, "attn_fwd_hd", raise_on_error)
 
 
 def attn_fwd_fp8(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens=None, stream=None,

@@ -87,10 +87,11 @@ attn_status_t encode_fn() {
 // 3-D map over a [rows, heads, d] tensor of bf16 (elem 2) or 8-bit codes (elem 1); box =
 // 128 bytes of d x 1 head x 128 rows, 128-byte swizzle (the K-major / MN-major canonical
 // layout the MMAs read), zero fill outside [0, rows).
-attn_status_t make_map(CUtensorMap* m, const void* base, long long rows, int heads, int d, int elem = 2) {
+attn_status_t make_map(CUtensorMap* m, const void* base, long long rows, int heads, int d, int elem = 2,
+                       int box_rows = 128) {
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
     cuuint64_t strides[2] = {(cuuint64_t)d * elem, (cuuint64_t)heads * d * elem};
-    cuuint32_t box[3] = {(cuuint32_t)(128 / elem), 1, 128};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / elem), 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
                           const_cast<void*>(base), dims, strides, box, estr,
@@ -172,18 +173,19 @@ attn_status_t attn_get_option(const char* name, double* value) {
 }
 
 // Shared body of the forward entry points. fp8 < 0: bf16 Q/K/V; 0 / 1: e4m3 / e5m2 codes
-// with per-tensor descales (d = 128 only).
+// with per-tensor descales (d = 128 only). dv: value / output width (= d, or 128 with d = 192).
 static attn_status_t fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                          int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens, void* stream, int fp8,
-                         float q_descale, float k_descale, float v_descale) {
+                         float q_descale, float k_descale, float v_descale, int dv = -1) {
+    if (dv < 0) dv = d;
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL_PTR;
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq < 0 || Nk < 0 || (d != 64 && d != 128))
-        return ATTN_ERR_BAD_SHAPE;
+    const bool shape_ok = (d == dv && (d == 64 || d == 128)) || (d == 192 && dv == 128);
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq < 0 || Nk < 0 || !shape_ok) return ATTN_ERR_BAD_SHAPE;
     if (fp8 >= 0 && d != 128) return ATTN_ERR_BAD_SHAPE;
     if (causal != 0 && causal != 1) return ATTN_ERR_BAD_SHAPE;
     if (!isfinite(scale)) return ATTN_ERR_BAD_SHAPE;
     if (Hq > 65535 || Hkv > 65535) return ATTN_ERR_BAD_SHAPE;
-    if (cu_seqlens && B > attn::fwd_max_varlen_batch()) return ATTN_ERR_BAD_SHAPE;
+    if (cu_seqlens && B > attn::fwd_max_varlen_batch(d)) return ATTN_ERR_BAD_SHAPE;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
         (cu_seqlens && !aligned(cu_seqlens, 4)))
         return ATTN_ERR_ALIGN;
@@ -198,8 +200,9 @@ static attn_status_t fwd(const void* q, const void* k, const void* v, void* o, f
     if ((st = encode_fn()) != ATTN_OK) return st;
     FwdTmaps tm;
     const int elem = fp8 >= 0 ? 1 : 2;
-    if (make_map(&tm.q, q, Tq, Hq, d, elem) != ATTN_OK || make_map(&tm.k, k, Tk, Hkv, d, elem) != ATTN_OK ||
-        make_map(&tm.v, v, Tk, Hkv, d, elem) != ATTN_OK)
+    const int kv_rows = d > 128 ? 96 : 128;  // keys per K/V tile of the kernel instantiation
+    if (make_map(&tm.q, q, Tq, Hq, d, elem) != ATTN_OK || make_map(&tm.k, k, Tk, Hkv, d, elem, kv_rows) != ATTN_OK ||
+        make_map(&tm.v, v, Tk, Hkv, dv, elem, kv_rows) != ATTN_OK)
         return ATTN_ERR_CUDA;
     const Options opt = options();
     FwdParams p;
@@ -251,14 +254,20 @@ static attn_status_t fwd(const void* q, const void* k, const void* v, void* o, f
     }
     if (grid <= 0) return ATTN_OK;
     const cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = fp8 < 0 ? attn::launch_attn_fwd(tm, p, d, opt.exp_poly, grid, st_)
-                                  : attn::launch_attn_fwd_fp8(tm, p, d, fp8, grid, st_);
+    const cudaError_t e = fp8 >= 0  ? attn::launch_attn_fwd_fp8(tm, p, d, fp8, grid, st_)
+                          : d != dv ? attn::launch_attn_fwd_hd(tm, p, d, dv, grid, st_)
+                                    : attn::launch_attn_fwd(tm, p, d, opt.exp_poly, grid, st_);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                        int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens, void* stream) {
     return fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens, stream, -1, 1.0f, 1.0f, 1.0f);
+}
+
+attn_status_t attn_fwd_hd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                          int Nq, int Nk, int d, int dv, float scale, int causal, const int* cu_seqlens, void* stream) {
+    return fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens, stream, -1, 1.0f, 1.0f, 1.0f, dv);
 }
 
 attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,

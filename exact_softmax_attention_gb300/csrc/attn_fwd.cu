@@ -42,31 +42,36 @@ namespace {
 
 constexpr int BM = 128;  // rows per Q tile
 constexpr int BN = 128;  // keys per K/V tile
+constexpr int kBNWide = 96;  // keys per K/V tile when Q/K rows are 192 wide (shared-memory bound)
 constexpr int kThreads = 512;
 constexpr int kMaxVarlenB = 1024;
 constexpr int kMaxLevels = 2048;  // 256-row blocks per packed sequence for the level order
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
 constexpr uint32_t kTmemCols = 512;
 
-template <int D, int F8 = 0>
+// D: width of queries and keys; DV: width of values and outputs; BNT: keys per K/V tile.
+template <int D, int F8 = 0, int DV = D, int BNT = BN>
 struct Layout {
     // F8 != 0: Q, K and V arrive as 8-bit floating-point codes (1 = e4m3, 2 = e5m2); V is
     // widened to f16 in shared memory before the P V product.
     static constexpr int kElem = F8 ? 1 : 2;             // bytes per loaded Q/K/V element
     static constexpr int kQBytes = BM * D * kElem;
-    static constexpr int kKBytes = BN * D * kElem;       // K tile as loaded
-    static constexpr int kV8Bytes = F8 ? BN * D : 0;     // 8-bit V tile as loaded
-    static constexpr int kVBytes = BN * D * 2;           // 16-bit V tile read by the MMA
+    static constexpr int kKBytes = BNT * D * kElem;      // K tile as loaded
+    static constexpr int kV8Bytes = F8 ? BNT * DV : 0;   // 8-bit V tile as loaded
+    static constexpr int kVBytes = BNT * DV * 2;         // 16-bit V tile read by the MMA
     // Ring entry n holds what burst n reads: K tile n (for S = Q K_n^T) and V tile n-1
     // (for O += P_{n-1} V_{n-1}); with 8-bit inputs also the 8-bit V tile it is widened from.
     static constexpr int kV8Off = kKBytes;
     static constexpr int kVOff = kKBytes + kV8Bytes;
     static constexpr int kEntryBytes = kKBytes + kV8Bytes + kVBytes;
-    static constexpr int kEntries = (D == 128) ? 2 : 4;
+    static constexpr int kEntries = (D == 64) ? 4 : 2;
     static constexpr int kChunks = D * kElem / 128;      // 128-byte swizzle chunks per Q/K row
-    static constexpr int kVChunks = D / 64;              // 128-byte chunks per 16-bit V row
-    static constexpr int kChunkBytesQ = BM * 128;        // one [128 rows x 128 bytes] chunk
-    static constexpr int kChunkBytesKV = BN * 128;
+    static constexpr int kVChunks = DV / 64;             // 128-byte chunks per 16-bit V row
+    static constexpr int kChunkBytesQ = BM * 128;        // one [BM rows x 128 bytes] chunk
+    static constexpr int kChunkBytesKV = BNT * 128;      // one [BNT rows x 128 bytes] chunk
+    // packed-sequence order tables: smaller where Q/K tiles leave less shared memory
+    static constexpr int kMaxB = D > 128 ? 256 : kMaxVarlenB;
+    static constexpr int kMaxLv = D > 128 ? 512 : kMaxLevels;
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = 2 * kQBytes;
     static constexpr int kBarOff = kKVOff + kEntries * kEntryBytes;
@@ -84,10 +89,10 @@ struct Layout {
     // misc: tmem base, abort flag, packed-order levels, packed work tiles
     // packed-sequence work order (built once per CTA): pre, lvl, perm, nbs
     static constexpr int kPreOff = kMiscOff + 16;
-    static constexpr int kLvlOff = kPreOff + ((kMaxVarlenB + 1) * 4 + 15) / 16 * 16;
-    static constexpr int kPermOff = kLvlOff + ((kMaxLevels + 2) * 4 + 15) / 16 * 16;
-    static constexpr int kNbOff = kPermOff + kMaxVarlenB * 4;
-    static constexpr int kBytes = kNbOff + kMaxVarlenB * 4;
+    static constexpr int kLvlOff = kPreOff + ((kMaxB + 1) * 4 + 15) / 16 * 16;
+    static constexpr int kPermOff = kLvlOff + ((kMaxLv + 2) * 4 + 15) / 16 * 16;
+    static constexpr int kNbOff = kPermOff + kMaxB * 4;
+    static constexpr int kBytes = kNbOff + kMaxB * 4;
     static constexpr int kAlloc = kBytes + 1024;                   // slack for 1024-byte alignment
 };
 
@@ -182,6 +187,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Store packed P columns [C0, C1) (two 16-bit probabilities per column) to TMEM at tS.
+template <int C0, int C1>
+__device__ __forceinline__ void store_p_cols(uint32_t tS, const uint32_t* pk) {
+    static_assert((C1 - C0) % 16 == 0, "whole 16-column stores");
+    if constexpr (C1 - C0 >= 32) {
+        tmem_st32(tS + C0, pk + C0);
+        store_p_cols<C0 + 32, C1>(tS, pk);
+    } else if constexpr (C1 - C0 >= 16) {
+        tmem_st16(tS + C0, pk + C0);
+        store_p_cols<C0 + 16, C1>(tS, pk);
+    }
+}
+
 // Widen row r of the 8-bit V tile at v8 ([BN keys x D bytes], rows of 128 bytes in the TMA's
 // 128-byte swizzle: 16-byte unit u of row r at r*128 + ((u ^ (r & 7)) << 4)) into the 16-bit
 // V tile at v16, in the layout a TMA load of 16-bit V would have produced: D/64 chunks of
@@ -237,6 +255,7 @@ struct PackedOrder {
 //   packed sequences, no mask: sequences longest first, then sections of sec_q query heads,
 //     then query blocks, then the heads of the section.
 // The query heads of one key/value head are adjacent in all three.
+template <int BNT>
 __device__ __forceinline__ void get_tile(const FwdParams& p, const PackedOrder& po, int w, Tile& t) {
     int b, Lq, Lk, q0, k0, j, h;
     if (p.cu_seqlens) {
@@ -308,9 +327,9 @@ __device__ __forceinline__ void get_tile(const FwdParams& p, const PackedOrder& 
             if (p.causal) {
                 const int rl = min(r + BM - 1, Lq - 1);
                 const int kmax = min(Lk, rl + (Lk - Lq) + 1);
-                n = kmax > 0 ? cdiv(kmax, BN) : 0;
+                n = kmax > 0 ? cdiv(kmax, BNT) : 0;
             } else {
-                n = cdiv(Lk, BN);
+                n = cdiv(Lk, BNT);
             }
         }
         t.n[s] = n;
@@ -319,11 +338,11 @@ __device__ __forceinline__ void get_tile(const FwdParams& p, const PackedOrder& 
 
 // Build the packed-sequence work order (one warp). Blocks per sequence nb = ceil(len / 256);
 // a counting sort by nb, stable so that every CTA derives the same order, gives perm.
-// Level order (causal, nb <= kMaxLevels): with c_j = #{sequences with nb > j}, level j holds
+// Level order (causal, nb <= max_levels): with c_j = #{sequences with nb > j}, level j holds
 // Hq * c_j tiles, and lvl[j + 2] = Hq * sum over levels above j of c. Returns the number of
 // levels (0 selects the sequence-major order) and the number of work tiles.
 __device__ void build_packed_order(const FwdParams& p, int* pre, int* lvl, int* perm, int* nbs, int lane,
-                                   int& levels, int& total) {
+                                   int max_levels, int& levels, int& total) {
     const int B = p.B;
     int maxnb = 0;
     for (int base = 0; base < B; base += 32) {
@@ -337,7 +356,7 @@ __device__ void build_packed_order(const FwdParams& p, int* pre, int* lvl, int* 
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) maxnb = max(maxnb, __shfl_xor_sync(0xffffffffu, maxnb, o));
-    const bool sorted = maxnb <= kMaxLevels;
+    const bool sorted = maxnb <= max_levels;
     if (sorted) {
         for (int v = lane; v <= maxnb + 1; v += 32) lvl[v] = 0;
         __syncwarp();
@@ -432,11 +451,14 @@ __device__ __forceinline__ float ex2_poly(float x) {
     return __uint_as_float(__float_as_uint(q) + (__float_as_uint(t) << 23));
 }
 
-template <int D, int POLY_EVERY, int F8>
+template <int D, int POLY_EVERY, int F8, int DV, int BNT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using L = Layout<D, F8>;
+    using L = Layout<D, F8, DV, BNT>;
+    constexpr int BN = BNT;  // keys per K/V tile (shadows the default)
+    static_assert(BN % 32 == 0 && BN <= 128 && DV <= 128 && DV % 64 == 0 && D % 64 == 0, "tile shape");
+    static_assert(L::kAlloc <= 232448, "shared memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
@@ -489,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* perm = reinterpret_cast<int*>(smem + L::kPermOff);
     if (p.cu_seqlens && warp == 2) {
         int levels, tiles;
-        build_packed_order(p, pre, lvl, perm, reinterpret_cast<int*>(smem + L::kNbOff), lane, levels, tiles);
+        build_packed_order(p, pre, lvl, perm, reinterpret_cast<int*>(smem + L::kNbOff), lane, L::kMaxLv, levels, tiles);
         if (lane == 0) {
             misc[2] = levels;
             misc[3] = tiles;
@@ -528,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int w = snake_index(r);
             if (w >= total) continue;
             Tile t;
-            get_tile(p, po, w, t);
+            get_tile<BN>(p, po, w, t);
             const int nmax = max(t.n[0], t.n[1]);
             if (nmax == 0) continue;  // no visible key in the block: the other roles skip it too
 #pragma unroll
@@ -601,7 +623,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = warp - 1;
         const uint32_t leader = lane == 0;
         constexpr uint32_t idS = F8 ? idesc_f8_f32(BM, BN, F8 - 1) : idesc_bf16_f32(BM, BN, 0);
-        constexpr uint32_t idO = F8 ? idesc_f16_f32(BM, D, 1) : idesc_bf16_f32(BM, D, 1);
+        constexpr uint32_t idO = F8 ? idesc_f16_f32(BM, DV, 1) : idesc_bf16_f32(BM, DV, 1);
+        constexpr int kPA = (3 * BN / 4) / 16;  // P stage 1: k-steps (16 keys each) 0 .. kPA-1
         const uint32_t colS = s ? kColS1 : kColS0;
         const uint32_t colO = s ? kColO1 : kColO0;
         uint32_t stage = 0, phase = 0;
@@ -617,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int w = snake_index(r);
             if (w >= total) continue;
             Tile t;
-            get_tile(p, po, w, t);
+            get_tile<BN>(p, po, w, t);
             const int nmax = max(t.n[0], t.n[1]);
             const int ns = s ? t.n[1] : t.n[0];
             if (nmax == 0) continue;
@@ -656,14 +679,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t vd = dv0 + (uint64_t)((ent_off + L::kVOff) >> 4);
                     const uint32_t acc0 = n - 1 > 0 ? 1u : 0u;
 #pragma unroll
-                    for (int k = 0; k < 6; ++k)  // keys 0-95: P stage 1
+                    for (int k = 0; k < kPA; ++k)  // P stage 1
                         tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO,
                                      k == 0 ? acc0 : 1u);
                     if (!(ok = warp_wait(&bars[L::bPRest + s], pf, abort_flag, wd))) break;
                     pf ^= 1u;
                     tc_fence_after();
 #pragma unroll
-                    for (int k = 6; k < BN / 16; ++k)  // keys 96-127: P stage 2
+                    for (int k = kPA; k < BN / 16; ++k)  // P stage 2
                         tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO, 1u);
                 }
                 if (do_s) {
@@ -671,11 +694,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t kd = dk0 + (uint64_t)(ent_off >> 4);
 #pragma unroll
                     for (int k = 0; k < D * L::kElem / 32; ++k) {
-                        const uint64_t off = (uint64_t)(((k >> 2) * L::kChunkBytesQ + (k & 3) * 32) >> 4);
+                        const uint64_t oq = (uint64_t)(((k >> 2) * L::kChunkBytesQ + (k & 3) * 32) >> 4);
+                        const uint64_t ok_ = (uint64_t)(((k >> 2) * L::kChunkBytesKV + (k & 3) * 32) >> 4);
                         if (F8)
-                            tc_mma_ss_f8_by(leader, tmem + colS, dq + off, kd + off, idS, k > 0 ? 1u : 0u);
+                            tc_mma_ss_f8_by(leader, tmem + colS, dq + oq, kd + ok_, idS, k > 0 ? 1u : 0u);
                         else
-                            tc_mma_ss_by(leader, tmem + colS, dq + off, kd + off, idS, k > 0 ? 1u : 0u);
+                            tc_mma_ss_by(leader, tmem + colS, dq + oq, kd + ok_, idS, k > 0 ? 1u : 0u);
                     }
                 }
                 __syncwarp();
@@ -713,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int w = snake_index(r);
             if (w >= total) continue;
             Tile t;
-            get_tile(p, po, w, t);
+            get_tile<BN>(p, po, w, t);
             const int ns = s ? t.n[1] : t.n[0];
             if (ns == 0) continue;
             const int tile_row0 = t.r0 + s * BM;
@@ -726,16 +750,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sf ^= 1u;
                 tc_fence_after();
                 ATTN_TL_DECL(long long ts1 = clock64());
-                uint32_t r[4][32];
-                tmem_ld32(tS + 0, r[0]);
-                tmem_ld32(tS + 32, r[1]);
-                tmem_ld32(tS + 64, r[2]);
-                tmem_ld32(tS + 96, r[3]);
+                uint32_t r[BN / 32][32];
+#pragma unroll
+                for (int i = 0; i < BN / 32; ++i) tmem_ld32(tS + 32 * i, r[i]);
                 tc_wait_ld();
-                reg_fence(r[0]);
-                reg_fence(r[1]);
-                reg_fence(r[2]);
-                reg_fence(r[3]);
+#pragma unroll
+                for (int i = 0; i < BN / 32; ++i) reg_fence(r[i]);
                 float sv[BN];
 #pragma unroll
                 for (int c = 0; c < BN; ++c) sv[c] = __uint_as_float(r[c >> 5][c & 31]);
@@ -763,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float alpha = (m == -INFINITY) ? 0.0f : ex2_mufu((m - m_cand) * sl2);
                     if (n > 0) {
 #pragma unroll 1
-                        for (int c = 0; c < D; c += 16) {
+                        for (int c = 0; c < DV; c += 16) {
                             uint32_t o[16];
                             tmem_ld16(tO + c, o);
                             tc_wait_ld();
@@ -782,7 +802,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // exponent arguments two at a time (packed FMA), exponentials, packed row sums;
                 // P goes out in two stages (keys 0-95, then 96-127)
                 float sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                uint32_t pk[64];
+                uint32_t pk[BN / 2];
+                constexpr int kSA = (3 * BN / 4) / 16 * 16;  // keys in P stage 1 (whole MMA k-steps)
                 auto exp_pair = [&](int c) {
                     float x0, x1;
                     ffma2(x0, x1, sv[c], sv[c + 1], sl2, sl2, neg, neg);
@@ -799,16 +820,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pk[c >> 1] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
                 };
 #pragma unroll
-                for (int c = 0; c < 3 * BN / 4; c += 2) exp_pair(c);
-                tmem_st32(tS + 0, &pk[0]);
-                tmem_st16(tS + 32, &pk[32]);
+                for (int c = 0; c < kSA; c += 2) exp_pair(c);
+                store_p_cols<0, kSA / 2>(tS, pk);
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[L::bPFull + s]);
 #pragma unroll
-                for (int c = 3 * BN / 4; c < BN; c += 2) exp_pair(c);
-                tmem_st16(tS + 48, &pk[48]);
+                for (int c = kSA; c < BN; c += 2) exp_pair(c);
+                store_p_cols<kSA / 2, BN / 2>(tS, pk);
                 l += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
                 tc_wait_st();
                 tc_fence_before();
@@ -849,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int w = snake_index(r);
             if (w >= total) continue;
             Tile t;
-            get_tile(p, po, w, t);
+            get_tile<BN>(p, po, w, t);
             if constexpr (F8 != 0) {
                 // Widen this tile's 8-bit V tiles first (rows 32*quarter .. +31 of each), in ring
                 // order. The MMA warps wait for them (bVConv) before each P V product and only
@@ -874,12 +894,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (t.r0 + s * BM >= t.Lq) continue;
                 const bool valid = qrow < t.Lq;
                 const long long tok = (long long)t.q0 + qrow;
-                __nv_bfloat16* orow = p.o + (tok * p.Hq + t.h) * D;
+                __nv_bfloat16* orow = p.o + (tok * p.Hq + t.h) * DV;
                 if (t.n[s] == 0) {
                     if (valid) {
                         uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-                        for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+                        for (int c = 0; c < DV / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
                         p.lse[tok * p.Hq + t.h] = -INFINITY;
                     }
                     continue;
@@ -894,7 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float inv = l > 0.0f ? p.out_scale / l : 0.0f;
                 const uint32_t tO = tmem + lane_off + (s ? kColO1 : kColO0);
 #pragma unroll 1
-                for (int c = 0; c < D; c += 32) {
+                for (int c = 0; c < DV; c += 32) {
                     uint32_t o[32];
                     tmem_ld32(tO + c, o);
                     tc_wait_ld();
@@ -929,25 +949,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, int POLY, int F8>
+template <int D, int POLY, int F8, int DV = D, int BNT = BN>
 cudaError_t launch_t(const FwdTmaps& tm, const FwdParams& p, int grid, cudaStream_t stream) {
-    using L = Layout<D, F8>;
+    using L = Layout<D, F8, DV, BNT>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(attn_fwd_kernel<D, POLY, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+        e = cudaFuncSetAttribute(attn_fwd_kernel<D, POLY, F8, DV, BNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 L::kAlloc);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    attn_fwd_kernel<D, POLY, F8><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.k, tm.v, p);
+    attn_fwd_kernel<D, POLY, F8, DV, BNT><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.k, tm.v, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int fwd_max_varlen_batch() { return kMaxVarlenB; }
+int fwd_max_varlen_batch(int d) { return d > 128 ? Layout<192, 0, 128, kBNWide>::kMaxB : kMaxVarlenB; }
+
+cudaError_t launch_attn_fwd_hd(const FwdTmaps& tm, const FwdParams& p, int d, int dv, int grid, cudaStream_t stream) {
+    if (d == 192 && dv == 128) return launch_t<192, 0, 0, 128, kBNWide>(tm, p, grid, stream);
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_attn_fwd(const FwdTmaps& tm, const FwdParams& p, int d, int exp_poly, int grid,
                             cudaStream_t stream) {

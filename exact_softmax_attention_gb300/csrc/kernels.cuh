@@ -47,7 +47,10 @@ cudaError_t launch_attn_fwd(const FwdTmaps& tm, const FwdParams& p, int d, int e
 // descales and p.out_scale is the v descale.
 cudaError_t launch_attn_fwd_fp8(const FwdTmaps& tm, const FwdParams& p, int d, int fmt, int grid,
                                 cudaStream_t stream);
-int fwd_max_varlen_batch();
+// Head dims (d, dv) = (192, 128): q, k 192 wide, v, o 128 wide; key tiles of 96 rows.
+cudaError_t launch_attn_fwd_hd(const FwdTmaps& tm, const FwdParams& p, int d, int dv, int grid, cudaStream_t stream);
+// Largest number of packed sequences of one call for query/key width d.
+int fwd_max_varlen_batch(int d);
 
 struct DecodeParams {
     const __nv_bfloat16* q;        // [B, Hq, d]

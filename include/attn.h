@@ -86,6 +86,24 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens, void* stream);
 
 /*
+ * attn_fwd with values (and outputs) narrower than queries and keys: head dims (d, dv) =
+ * (192, 128), the DeepSeek-V3 configuration ("FlashAttention-4: Blackwell algorithm-pipeline
+ * co-design", performance section). Scores use all d = 192 columns of q and k; the output
+ * is the probability-weighted sum of the dv = 128 wide values.
+ *
+ * q           device, bf16 [T, Hq, d]      k  device, bf16 [Tk, Hkv, d]
+ * v           device, bf16 [Tk, Hkv, dv]   o  device, bf16 [T, Hq, dv] (written)
+ * lse         device, fp32 [T, Hq] (written)
+ * d, dv       (192, 128); (64, 64) and (128, 128) are also accepted and behave as attn_fwd.
+ *             Anything else is ATTN_ERR_BAD_SHAPE.
+ * Everything else is as for attn_fwd. With (192, 128) the kernel uses 96-key tiles (the
+ * 192-wide query and key tiles leave no room in shared memory for 128-key tiles), and a
+ * call with cu_seqlens takes at most 256 sequences.
+ */
+attn_status_t attn_fwd_hd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                          int Nq, int Nk, int d, int dv, float scale, int causal, const int* cu_seqlens, void* stream);
+
+/*
  * attn_fwd on Q/K/V given in 8-bit floating point ("Faster, more flexible FA4 for LLM
  * inference", PR 2109: e4m3 or e5m2 inputs).
  *

@@ -79,6 +79,19 @@ def test_decode_host_validation(lib):
     assert _dec(lib, B=0) == A.ATTN_OK
 
 
+def test_hd_host_validation(lib):
+    import exact_softmax_attention_gb300 as A
+    f = lib.attn_fwd_hd
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [vp] * 5 + [i] * 7 + [ctypes.c_float, i, vp, vp]
+    call = lambda d, dv, B=1, cu=None: f(16, 16, 16, 16, 16, B, 2, 2, 64, 64, d, dv, 0.1, 1, cu, None)
+    assert call(192, 64) == A.ATTN_ERR_BAD_SHAPE
+    assert call(128, 192) == A.ATTN_ERR_BAD_SHAPE
+    assert call(96, 96) == A.ATTN_ERR_BAD_SHAPE
+    assert call(192, 128, B=257, cu=16) == A.ATTN_ERR_BAD_SHAPE  # at most 256 packed sequences at d = 192
+    assert call(192, 128, B=0) == A.ATTN_OK
+
+
 def _dec8(lib, fmt=0, kds=0.5, vds=2.0, **kw):
     f = lib.attn_decode_paged_fp8
     vp = ctypes.c_void_p
