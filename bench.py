@@ -13,7 +13,8 @@ inputs are larger than L2, so no flush is needed between steps.
 After the timed steps, attn_decode_paged_fp8 runs the same decode workload with
 e4m3 key/value caches for as many timed calls; its GB/s (algorithmic bytes of the
 8-bit caches) is reported under ``decode_fp8``, outside ``value``. Likewise
-attn_fwd_fp8 on the long causal prefill with e4m3 Q/K/V, under ``prefill_fp8``.
+attn_fwd_fp8 on the long causal prefill with e4m3 Q/K/V, under ``prefill_fp8``, and
+attn_fwd_hd on the same geometry with head dims (192, 128), under ``prefill_hd``.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 With --gpus N > 1 the script runs under torch.distributed.run, one rank per GPU,
@@ -46,6 +47,7 @@ FWD_KERNEL = "attn_fwd_kernel"
 DEC_KERNEL = "decode_split_kernel"
 DEC8_KERNEL = "decode_split_fp8_kernel"
 FWD8_KERNEL = "attn_fwd_kernel<128, 0, 1>"
+FWDHD_KERNEL = "attn_fwd_kernel<192, 0, 0, 128, 96>"
 
 
 def parse():
@@ -76,7 +78,8 @@ def peaks():
 KERNEL_SOURCES = {FWD_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"],
                   DEC_KERNEL: ["attn_decode.cu", "ptx.cuh", "kernels.cuh"],
                   DEC8_KERNEL: ["attn_decode.cu", "ptx.cuh", "kernels.cuh"],
-                  FWD8_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"]}
+                  FWD8_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"],
+                  FWDHD_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"]}
 
 
 def source_sha(kernel: str) -> str:
@@ -367,6 +370,18 @@ def run_ours(args):
         A.attn_fwd_fp8(Q8, K8, V8, O, LSE, fc.B, fc.Hq, fc.Hkv, fc.Nq, fc.Nk, fc.d, fc.scale, fc.causal, None,
                        s_handle, "e4m3", qds, kds8, vds8)
 
+    # head dims (192, 128) on the long causal geometry: a leg of its own, timed after the step
+    hc = W.PrefillCase("long_causal_hd", fc.B, fc.Hq, fc.Hkv, fc.Nq, fc.Nk, 192, 1.0 / math.sqrt(192), True,
+                       fc.seed, fc.q_mult, dv=128)
+    hq, hk, hv = hc.generate()
+    with torch.cuda.stream(stream):
+        HQ, HK, HV = to_dev(hq), to_dev(hk), to_dev(hv)
+        HO = torch.empty((hc.total_q, hc.Hq, 128), dtype=torch.bfloat16, device=dev)
+    stream.synchronize()
+
+    def fwd_hd():
+        A.attn_fwd_hd(HQ, HK, HV, HO, LSE, hc.B, hc.Hq, hc.Hkv, hc.Nq, hc.Nk, 192, 128, hc.scale, True, None, s_handle)
+
     def dec8():
         A.attn_decode_paged_fp8(DQ, KC8, VC8, PT, SL, dc8.page_size, DO, DLSE, s_handle, dc8.B, dc8.Hq, dc8.Hkv,
                                 dc8.d, dc8.max_pages, dc8.num_pages, dc8.scale, 0, dc8.kv_fmt, kds, vds)
@@ -441,6 +456,21 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device status after the FP8 forward leg: {A.status_string(st)}")
     fwd8_ms = max_over_ranks(sf8.elapsed_time(ef8), world, dev)
+
+    # head dims (192, 128) leg
+    for _ in range(args.warmup):
+        fwd_hd()
+    barrier()
+    sh, eh = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sh.record(stream)
+    for _ in range(K_):
+        fwd_hd()
+    eh.record(stream)
+    barrier()
+    st = A.attn_get_device_status(s_handle)
+    if st != 0:
+        raise RuntimeError(f"device status after the (192, 128) forward leg: {A.status_string(st)}")
+    fwdhd_ms = max_over_ranks(sh.elapsed_time(eh), world, dev)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -532,6 +562,15 @@ def run_ours(args):
                                      "traffic": ncu_traffic(FWD8_KERNEL), "kernel": FWD8_KERNEL,
                                      "peak_source": f"{src} bf16 burst x 4/3 (half the FLOPs in fp8 at 2x, half in "
                                                     "f16 at 1x)"}},
+        "prefill_hd": {"value": world * K_ * hc.flops() / (fwdhd_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "ms_per_call": fwdhd_ms / K_, "calls": K_, "gpu_launches": K_,
+                       "workload": "long causal prefill B1 H32 N8192 with head dims (192, 128), bf16",
+                       "flops_per_call": hc.flops(),
+                       "roofline": {"bound": "tensor", "achieved": hc.flops() / (fwdhd_ms / K_ * 1e-3) / 1e12,
+                                    "peak": bf16, "unit": "TFLOP/s",
+                                    "frac": hc.flops() / (fwdhd_ms / K_ * 1e-3) / 1e12 / bf16,
+                                    "traffic": ncu_traffic(FWDHD_KERNEL), "kernel": FWDHD_KERNEL,
+                                    "peak_source": f"{src} bf16 burst"}},
         "prefill_ms_per_step": fwd_ms / K_,
         "gpu_launches": K_ * launches_per_step,
         "clocks": clk.summary(),
