@@ -34,7 +34,8 @@ ATTN_FP8_E5M2 = 1
 FP8_FORMATS = {"e4m3": ATTN_FP8_E4M3, "e5m2": ATTN_FP8_E5M2}
 
 #: every symbol the header declares
-EXPORTS = ("attn_fwd", "attn_fwd_hd", "attn_fwd_fp8", "attn_decode_paged", "attn_decode_paged_fp8", "attn_decode_paged_noalloc", "attn_decode_plan", "attn_status_string", "attn_get_device_status",
+EXPORTS = ("attn_fwd", "attn_fwd_hd", "attn_fwd_fp8", "attn_decode_paged", "attn_decode_paged_fp8", "attn_decode_paged_noalloc", "attn_decode_plan",
+           "attn_decode_workspace_bytes", "attn_status_string", "attn_get_device_status",
            "attn_set_option", "attn_get_option", "attn_read_counters", "attn_debug_exp2", "attn_debug_watchdog",
            "attn_version")
 
@@ -66,6 +67,8 @@ lib.attn_decode_paged_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp,
 lib.attn_decode_paged_noalloc.restype = _i
 lib.attn_decode_plan.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]
 lib.attn_decode_plan.restype = _i
+lib.attn_decode_workspace_bytes.argtypes = [_i, _i, _i, _i]
+lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
 lib.attn_status_string.argtypes = [_i]
 lib.attn_status_string.restype = ctypes.c_char_p
 lib.attn_get_device_status.argtypes = [_vp]
@@ -182,6 +185,11 @@ def attn_decode_plan(B, Hkv, max_pages_per_seq, page_size, num_splits=0, num_sms
                               ctypes.byref(c), ctypes.byref(s))
     _check(rc, "attn_decode_plan", True)
     return c.value, s.value
+
+
+def attn_decode_workspace_bytes(B, Hq, d, max_splits) -> int:
+    """Bytes of split-KV workspace attn_decode_paged takes for these sizes."""
+    return int(lib.attn_decode_workspace_bytes(int(B), int(Hq), int(d), int(max_splits)))
 
 
 def attn_get_device_status(stream=None) -> int:

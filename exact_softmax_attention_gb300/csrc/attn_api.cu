@@ -281,6 +281,11 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
                k_descale, v_descale);
 }
 
+size_t attn_decode_workspace_bytes(int B, int Hq, int d, int max_splits) {
+    if (B <= 0 || Hq <= 0 || d <= 0 || max_splits <= 1) return 0;
+    return (size_t)B * (size_t)Hq * (size_t)max_splits * ((size_t)d + 1) * sizeof(float);
+}
+
 attn_status_t attn_decode_plan(int B, int Hkv, int max_pages_per_seq, int page_size, int num_splits, int num_sms,
                                int* chunk, int* max_splits) {
     if (!chunk || !max_splits) return ATTN_ERR_NULL_PTR;
@@ -381,8 +386,8 @@ static attn_status_t decode_paged(const void* q, const void* k_cache, const void
             }
         }
         const size_t n_o = (size_t)B * Hq * max_splits * d;
-        const size_t n_l = (size_t)B * Hq * max_splits;
-        if (cudaMallocFromPoolAsync(&ws, (n_o + n_l) * sizeof(float), ds->pool, s) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (cudaMallocFromPoolAsync(&ws, attn_decode_workspace_bytes(B, Hq, d, max_splits), ds->pool, s) != cudaSuccess)
+            return ATTN_ERR_CUDA;
         p.ws_o = reinterpret_cast<float*>(ws);
         p.ws_lse = p.ws_o + n_o;
     }

@@ -214,6 +214,16 @@ attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_cache, cons
 attn_status_t attn_decode_plan(int B, int Hkv, int max_pages_per_seq, int page_size, int num_splits, int num_sms,
                                int* chunk, int* max_splits);
 
+/*
+ * Bytes of split-KV workspace attn_decode_paged takes for these sizes: B * Hq * max_splits
+ * partial outputs of d floats plus as many partial log-sum-exps (fp32), with max_splits
+ * from attn_decode_plan (a call with max_splits = 1 writes its results directly and needs
+ * none). Returns 0 for max_splits <= 1 or non-positive sizes. Pure host arithmetic.
+ * attn_decode_paged takes this memory from a library-owned stream-ordered pool;
+ * attn_decode_paged_noalloc compares it with its fixed 32 MiB array.
+ */
+size_t attn_decode_workspace_bytes(int B, int Hq, int d, int max_splits);
+
 /* Static description of a status code. Never NULL. */
 const char* attn_status_string(attn_status_t status);
 

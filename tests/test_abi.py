@@ -79,6 +79,15 @@ def test_decode_host_validation(lib):
     assert _dec(lib, B=0) == A.ATTN_OK
 
 
+def test_decode_workspace_bytes():
+    import exact_softmax_attention_gb300 as A
+    assert A.attn_decode_workspace_bytes(64, 32, 128, 19) == 64 * 32 * 19 * 129 * 4
+    assert A.attn_decode_workspace_bytes(64, 32, 128, 1) == 0  # one split writes o and lse directly
+    assert A.attn_decode_workspace_bytes(0, 32, 128, 4) == 0
+    _, splits = A.attn_decode_plan(64, 8, 2048, 16, 0, 152)
+    assert A.attn_decode_workspace_bytes(64, 32, 128, splits) < 32 << 20  # the decode workload fits the no-alloc array
+
+
 def test_hd_host_validation(lib):
     import exact_softmax_attention_gb300 as A
     f = lib.attn_fwd_hd
