@@ -68,6 +68,7 @@ CASES = [
     case("no_key_blocks", 1, 2, 2, 600, 100, True, 45),
     case("sharp", 1, 4, 4, 1024, 1024, True, 46, 3.0),
     case("varlen", 0, 4, 2, 0, 0, True, 47, lens=[1, 129, 0, 256, 257, 5, 600]),
+    case("gqa16", 1, 32, 2, 300, 300, True, 50),
 ]
 
 

@@ -69,6 +69,7 @@ CASES = [
     case("sharp", 1, 4, 4, 1024, 1024, True, 67, 2.0),
     case("varlen", 0, 4, 2, 0, 0, True, 68, lens=[1, 129, 0, 256, 257, 5, 600]),
     case("varlen_nc", 0, 2, 2, 0, 0, False, 69, lens=[300, 17, 96, 97]),
+    case("mqa16", 1, 16, 1, 257, 257, True, 72),
 ]
 
 

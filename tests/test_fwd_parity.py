@@ -80,6 +80,8 @@ SMALL = [
     # causal with Nq much larger than Nk: whole 256-row blocks see no key at all
     case("no_key_blocks", 1, 2, 2, 600, 100, 128, True, 18),
     case("no_key_blocks_d64", 2, 2, 1, 900, 64, 64, True, 19),
+    case("gqa16_causal", 1, 32, 2, 300, 300, 128, True, 20),
+    case("mqa32_noncausal", 2, 32, 1, 200, 350, 64, False, 21),
     case("varlen_small", 0, 4, 2, 0, 0, 128, True, 13, lens=[1, 129, 0, 256, 257, 5, 600]),
     case("varlen_d64_nc", 0, 2, 2, 0, 0, 64, False, 14, lens=[300, 17, 128]),
     # more than 32 sequences (several passes of the work-order build), empties and equal lengths
