@@ -38,7 +38,8 @@ def _to_fp8(c: np.ndarray, fmt: str):
     top = int(mag.max()) if mag.size else 0  # |x| orders like its magnitude bits (no NaN inputs)
     amax = float(bf16_to_f32(np.array([top], dtype=np.uint16))[0])
     ds = float(np.float32(amax / FP8_MAX[fmt])) if amax > 0 else 1.0
-    vals = bf16_to_f32(np.arange(65536, dtype=np.uint32).astype(np.uint16)).astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        vals = bf16_to_f32(np.arange(65536, dtype=np.uint32).astype(np.uint16)).astype(np.float64)
     vals[~np.isfinite(vals)] = 0.0  # NaN / inf patterns: not produced by the generator
     table = fp8_encode(vals / ds, fmt)
     return table[c], ds
