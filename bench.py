@@ -252,13 +252,15 @@ def oracle_decode_sample(case, inputs, n_seq, n_threads):
     return nbytes, dt
 
 
-def cpu_baseline(fwd_case, fwd_inputs, dec_case, dec_inputs, budget_s=12.0):
+def cpu_baseline(fwd_case, fwd_inputs, dec_case, dec_inputs, budget_s=15.0):
     """The oracle as it stands, on a bounded sample sized for ~budget_s of CPU time."""
     threads = os.cpu_count() or 1
-    # calibrate on a small sample, then size the measured one
-    f0, t0 = oracle_fwd_sample(fwd_case, *fwd_inputs, 64, 7, threads)
+    # calibrate on a sample large enough to amortise the thread start-up, then size the
+    # measured one for ~85 % of the budget (the decode sample takes the rest)
+    n0 = 512
+    f0, t0 = oracle_fwd_sample(fwd_case, *fwd_inputs, n0, 7, threads)
     rate = f0 / max(t0, 1e-6)
-    rows = int(min(fwd_case.total_q * fwd_case.Hq, max(64, 64 * (budget_s * 0.7) / max(t0, 1e-6))))
+    rows = int(min(fwd_case.total_q * fwd_case.Hq, max(n0, n0 * (budget_s * 0.85) / max(t0, 1e-6))))
     f, t = oracle_fwd_sample(fwd_case, *fwd_inputs, rows, 8, threads)
     d_seq = 2
     b, td = oracle_decode_sample(dec_case, dec_inputs, d_seq, threads)
