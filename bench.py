@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
+                    help="library tuning option (attn_set_option) applied before timing; repeatable")
     return ap.parse_args()
 
 
@@ -325,6 +327,10 @@ def run_ours(args):
 
     import exact_softmax_attention_gb300 as A
 
+    for opt in args.option:
+        name, value = opt.split("=", 1)
+        A.attn_set_option(name, float(value))
+
     fc, dc = W.long_causal(), W.decode()
     q, k, v = fc.generate()
     dq, kc, vc, pt, sl = dc.generate()
@@ -582,6 +588,8 @@ def run_ours(args):
         line["e2e"] = e2e
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(fc, (q, k, v), dc, (dq, kc, vc, pt, sl))
+    if args.option:
+        line["config"]["options"] = dict(o.split("=", 1) for o in args.option)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
