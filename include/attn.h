@@ -243,7 +243,10 @@ attn_status_t attn_get_device_status(void* stream);
  *                        powers of two (default 8, i.e. a factor 256, "FlashAttention4 精读"
  *                        section 3.1.4); 0 rescales on every increase
  *   "decode_chunk"       tokens per decode split when num_splits = 0 (0 = heuristic)
- *   "sec_heads"          query heads per forward scheduling section (0 = heuristic)
+ *   "sec_heads"          forward scheduling section (0 = heuristic): dense batches, the
+ *                        (batch, query head) pairs ordered together (rounded up to whole
+ *                        GQA groups; by default all of them unless the work spans 16 or more
+ *                        waves of the grid); packed sequences, query heads per section
  *   "count"              1: count softmax rescale decisions and exponentials (attn_read_counters)
  *   "watchdog_ms"        device wait limit before a kernel gives up (default 4000)
  * Returns ATTN_ERR_BAD_ARG for an unknown name or an invalid value.
