@@ -14,7 +14,8 @@ After the timed steps, attn_decode_paged_fp8 runs the same decode workload with
 e4m3 key/value caches for as many timed calls; its GB/s (algorithmic bytes of the
 8-bit caches) is reported under ``decode_fp8``, outside ``value``. Likewise
 attn_fwd_fp8 on the long causal prefill with e4m3 Q/K/V, under ``prefill_fp8``, and
-attn_fwd_hd on the same geometry with head dims (192, 128), under ``prefill_hd``.
+attn_fwd_hd on the same geometry with head dims (192, 128), under ``prefill_hd``, and
+attn_fwd with head width 256 on the same geometry, under ``prefill_d256``.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 With --gpus N > 1 the script runs under torch.distributed.run, one rank per GPU,
@@ -48,6 +49,7 @@ DEC_KERNEL = "decode_split_kernel"
 DEC8_KERNEL = "decode_split_fp8_kernel"
 FWD8_KERNEL = "attn_fwd_kernel<128, 0, 1>"
 FWDHD_KERNEL = "attn_fwd_kernel<192, 0, 0, 128, 96>"
+FWDW_KERNEL = "attn_fwd_wide_kernel"
 
 
 def parse():
@@ -81,7 +83,8 @@ KERNEL_SOURCES = {FWD_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"],
                   DEC_KERNEL: ["attn_decode.cu", "ptx.cuh", "kernels.cuh"],
                   DEC8_KERNEL: ["attn_decode.cu", "ptx.cuh", "kernels.cuh"],
                   FWD8_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"],
-                  FWDHD_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"]}
+                  FWDHD_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"],
+                  FWDW_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"]}
 
 
 def source_sha(kernel: str) -> str:
@@ -390,6 +393,19 @@ def run_ours(args):
     def fwd_hd():
         A.attn_fwd_hd(HQ, HK, HV, HO, LSE, hc.B, hc.Hq, hc.Hkv, hc.Nq, hc.Nk, 192, 128, hc.scale, True, None, s_handle)
 
+    # head width 256 on the long causal geometry: a leg of its own, timed after the step
+    wc = W.PrefillCase("long_causal_d256", fc.B, fc.Hq, fc.Hkv, fc.Nq, fc.Nk, 256, 1.0 / math.sqrt(256), True,
+                       fc.seed, fc.q_mult)
+    wq, wk, wv = wc.generate()
+    with torch.cuda.stream(stream):
+        WQ, WK, WV = to_dev(wq), to_dev(wk), to_dev(wv)
+        WO = torch.empty((wc.total_q, wc.Hq, 256), dtype=torch.bfloat16, device=dev)
+    stream.synchronize()
+    del wq, wk, wv
+
+    def fwd_w():
+        A.attn_fwd(WQ, WK, WV, WO, LSE, wc.B, wc.Hq, wc.Hkv, wc.Nq, wc.Nk, 256, wc.scale, True, None, s_handle)
+
     def dec8():
         A.attn_decode_paged_fp8(DQ, KC8, VC8, PT, SL, dc8.page_size, DO, DLSE, s_handle, dc8.B, dc8.Hq, dc8.Hkv,
                                 dc8.d, dc8.max_pages, dc8.num_pages, dc8.scale, 0, dc8.kv_fmt, kds, vds)
@@ -479,6 +495,21 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device status after the (192, 128) forward leg: {A.status_string(st)}")
     fwdhd_ms = max_over_ranks(sh.elapsed_time(eh), world, dev)
+
+    # head width 256 leg
+    for _ in range(args.warmup):
+        fwd_w()
+    barrier()
+    sw, ew = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sw.record(stream)
+    for _ in range(K_):
+        fwd_w()
+    ew.record(stream)
+    barrier()
+    st = A.attn_get_device_status(s_handle)
+    if st != 0:
+        raise RuntimeError(f"device status after the d = 256 forward leg: {A.status_string(st)}")
+    fwdw_ms = max_over_ranks(sw.elapsed_time(ew), world, dev)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -579,6 +610,15 @@ def run_ours(args):
                                     "frac": hc.flops() / (fwdhd_ms / K_ * 1e-3) / 1e12 / bf16,
                                     "traffic": ncu_traffic(FWDHD_KERNEL), "kernel": FWDHD_KERNEL,
                                     "peak_source": f"{src} bf16 burst"}},
+        "prefill_d256": {"value": world * K_ * wc.flops() / (fwdw_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                         "ms_per_call": fwdw_ms / K_, "calls": K_, "gpu_launches": K_,
+                         "workload": "long causal prefill B1 H32 N8192 with head width 256, bf16",
+                         "flops_per_call": wc.flops(),
+                         "roofline": {"bound": "tensor", "achieved": wc.flops() / (fwdw_ms / K_ * 1e-3) / 1e12,
+                                      "peak": bf16, "unit": "TFLOP/s",
+                                      "frac": wc.flops() / (fwdw_ms / K_ * 1e-3) / 1e12 / bf16,
+                                      "traffic": ncu_traffic(FWDW_KERNEL), "kernel": FWDW_KERNEL,
+                                      "peak_source": f"{src} bf16 burst"}},
         "prefill_ms_per_step": fwd_ms / K_,
         "gpu_launches": K_ * launches_per_step,
         "clocks": clk.summary(),

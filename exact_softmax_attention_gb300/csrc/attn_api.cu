@@ -179,7 +179,7 @@ static attn_status_t fwd(const void* q, const void* k, const void* v, void* o, f
                          float q_descale, float k_descale, float v_descale, int dv = -1) {
     if (dv < 0) dv = d;
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL_PTR;
-    const bool shape_ok = (d == dv && (d == 64 || d == 128)) || (d == 192 && dv == 128);
+    const bool shape_ok = (d == dv && (d == 64 || d == 128 || d == 256)) || (d == 192 && dv == 128);
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq < 0 || Nk < 0 || !shape_ok) return ATTN_ERR_BAD_SHAPE;
     if (fp8 >= 0 && d != 128) return ATTN_ERR_BAD_SHAPE;
     if (causal != 0 && causal != 1) return ATTN_ERR_BAD_SHAPE;
@@ -200,7 +200,7 @@ static attn_status_t fwd(const void* q, const void* k, const void* v, void* o, f
     if ((st = encode_fn()) != ATTN_OK) return st;
     FwdTmaps tm;
     const int elem = fp8 >= 0 ? 1 : 2;
-    const int kv_rows = d > 128 ? 96 : 128;  // keys per K/V tile of the kernel instantiation
+    const int kv_rows = d == 192 ? 96 : 128;  // keys per K/V tile of the kernel instantiation
     if (make_map(&tm.q, q, Tq, Hq, d, elem) != ATTN_OK || make_map(&tm.k, k, Tk, Hkv, d, elem, kv_rows) != ATTN_OK ||
         make_map(&tm.v, v, Tk, Hkv, dv, elem, kv_rows) != ATTN_OK)
         return ATTN_ERR_CUDA;
@@ -254,9 +254,10 @@ static attn_status_t fwd(const void* q, const void* k, const void* v, void* o, f
     }
     if (grid <= 0) return ATTN_OK;
     const cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = fp8 >= 0  ? attn::launch_attn_fwd_fp8(tm, p, d, fp8, grid, st_)
-                          : d != dv ? attn::launch_attn_fwd_hd(tm, p, d, dv, grid, st_)
-                                    : attn::launch_attn_fwd(tm, p, d, opt.exp_poly, grid, st_);
+    const cudaError_t e = fp8 >= 0   ? attn::launch_attn_fwd_fp8(tm, p, d, fp8, grid, st_)
+                          : d != dv  ? attn::launch_attn_fwd_hd(tm, p, d, dv, grid, st_)
+                          : d == 256 ? attn::launch_attn_fwd_wide(tm, p, grid, st_)
+                                     : attn::launch_attn_fwd(tm, p, d, opt.exp_poly, grid, st_);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -316,6 +317,7 @@ attn_status_t attn_decode_plan(int B, int Hkv, int max_pages_per_seq, int page_s
     c = ((c + 63) / 64) * 64;
     if (c > lmax) c = ((lmax + 63) / 64) * 64;
     if (c < 64) c = 64;
+    if (cdiv(lmax, c) * (long long)Hkv > INT32_MAX) return ATTN_ERR_BAD_SHAPE;  // one grid row per (split, kv head)
     *chunk = (int)c;
     *max_splits = cdiv(lmax, c);
     return ATTN_OK;

@@ -14,10 +14,11 @@
 // section 02) runs per warp over its tokens; the warps of a CTA and then the splits
 // are merged with the same max-shifted LSE weighting.
 //
-// Split kernel: grid (split, kv head, sequence), 4 warps. Each warp owns a private
-// cp.async ring of NST stages of 16 tokens (K and V rows, 128-byte XOR swizzle) and
-// processes token groups w, w+4, w+8, ... of the split, so the main loop needs no
-// CTA-wide barrier. Scores S = Q K^T use m16n8k16 bf16 MMAs with the (up to 16) query
+// Split kernel: grid (split x kv head, sequence) with the kv heads of one split adjacent,
+// so CTAs running side by side read neighbouring pieces of the same cache rows; 4 warps.
+// Each warp owns a private cp.async ring of NST stages of 16 tokens (K and V rows,
+// 128-byte XOR swizzle) and processes token groups w, w+4, w+8, ... of the split, so the
+// main loop needs no CTA-wide barrier. Scores S = Q K^T use m16n8k16 bf16 MMAs with the (up to 16) query
 // heads of the group as rows; O^T += V^T P^T reuses the score accumulators as the B
 // operand directly.
 #include "kernels.cuh"
@@ -125,7 +126,7 @@ template <int D, int GN, int NST>
 __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeParams p) {
     using L = DecLayout<D>;
     extern __shared__ __align__(128) uint8_t smem[];
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int kvh = (int)(blockIdx.x % (unsigned)p.Hkv), split = (int)(blockIdx.x / (unsigned)p.Hkv), b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long max_len = (long long)p.max_pages * p.page_size;
 
@@ -394,7 +395,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_fp8_kernel(const Dec
     constexpr int kTile = kGroup * D;   // bytes of one K or V warp-stage tile
     constexpr int kChunks = D / 16;     // 16-byte chunks per cache row
     extern __shared__ __align__(128) uint8_t smem[];
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int kvh = (int)(blockIdx.x % (unsigned)p.Hkv), split = (int)(blockIdx.x / (unsigned)p.Hkv), b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long max_len = (long long)p.max_pages * p.page_size;
 
@@ -670,7 +671,7 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    const dim3 grid(p.max_splits, p.Hkv, p.B);
+    const dim3 grid((unsigned)(p.max_splits * p.Hkv), p.B);  // kv heads of one split side by side
     decode_split_kernel<D, GN, NST><<<grid, kWarps * 32, bytes, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -697,7 +698,7 @@ cudaError_t launch_fp8_t(const DecodeParams& p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    const dim3 grid(p.max_splits, p.Hkv, p.B);
+    const dim3 grid((unsigned)(p.max_splits * p.Hkv), p.B);  // kv heads of one split side by side
     decode_split_fp8_kernel<D, GN, NST, FMT><<<grid, kWarps * 32, bytes, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

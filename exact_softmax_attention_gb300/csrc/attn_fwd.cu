@@ -966,9 +966,497 @@ cudaError_t launch_t(const FwdTmaps& tm, const FwdParams& p, int grid, cudaStrea
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ d = 256
+// Head width 256: the accumulator O of one 128-row Q tile takes 256 of the 512 TMEM columns,
+// so a CTA works on one Q tile at a time (the two tiles of a 256-row work tile in turn) and
+// uses the other 256 columns for two S buffers: S(n+1) = Q K_{n+1}^T is computed while the
+// softmax works on S(n), and each KV step issues O += P(n) V_n then S(n+2) = Q K_{n+2}^T
+// into the buffer P(n) came from. K and V tiles (128 keys x 256) travel as 32 KB halves
+// (d 0-127 and 128-255) through a ring of five slots. The softmax warps also write the
+// finished rows, so no separate epilogue warps or statistics exchange are needed.
+// TMEM columns: O [0,256), S0 [256,384), S1 [384,512).
+constexpr int kWideD = 256;
+constexpr int kWideThreads = 256;  // warp 0 TMA, warp 1 MMA, warp 2 packed order, warps 4-7 softmax
+constexpr uint32_t kWideColO = 0, kWideColS = 256;
+
+struct LayoutWide {
+    static constexpr int kQBytes = BM * kWideD * 2;          // 4 chunks of [128 rows x 128 bytes]
+    static constexpr int kChunkBytes = 128 * 128;            // one [128 rows x 128 bytes] chunk
+    static constexpr int kSlots = 5;
+    static constexpr int kSlotBytes = 2 * kChunkBytes;       // half a K or V tile: d 0-127 or 128-255
+    static constexpr int kQOff = 0;
+    static constexpr int kSlotOff = kQBytes;
+    static constexpr int kBarOff = kSlotOff + kSlots * kSlotBytes;
+    // S-buffer barriers come in pairs: the softmax may finish P(n) and P(n+1) before the MMA
+    // warp reads either, so P's barriers are per buffer like S's (one phase per use of a buffer).
+    static constexpr int bQFull = 0, bQEmpty = 1, bSlot = 2, bSFull = bSlot + kSlots, bPFull = bSFull + 2,
+                         bPRest = bPFull + 2, bVDone = bPRest + 2, bOFull = bVDone + 1, bDrain = bOFull + 1;
+    static constexpr int kNumBars = bDrain + 1;
+    static constexpr int kMiscOff = kBarOff + ((kNumBars * 8 + 15) / 16) * 16;
+    // packed-sequence order tables (small: the tiles leave about 2 KB)
+    static constexpr int kMaxB = 64;
+    static constexpr int kMaxLv = 192;
+    static constexpr int kPreOff = kMiscOff + 16;
+    static constexpr int kLvlOff = kPreOff + ((kMaxB + 1) * 4 + 15) / 16 * 16;
+    static constexpr int kPermOff = kLvlOff + ((kMaxLv + 2) * 4 + 15) / 16 * 16;
+    static constexpr int kNbOff = kPermOff + kMaxB * 4;
+    static constexpr int kBytes = kNbOff + kMaxB * 4;
+    static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+};
+
+// K/V half tiles in the order the MMA warp consumes them, per Q tile with ns key tiles:
+// K0a K0b K1a K1b | V0a V0b K2a K2b | V1a V1b K3a K3b | ... (K_{n+2} only while n + 2 < ns).
+// Item i lives in slot i % 5. The producer refills a slot once the products that read its
+// item are complete: S(m) = Q K_m^T for a K half (the S-buffer barrier of m % 2), O += P(n)
+// V_n for a V half (bVDone, one phase per step). Both sides enumerate the same sequence, and
+// slots are refilled in the order they were filled, so every parity wait below is at most
+// one phase behind or ahead of the barrier it reads.
+constexpr uint32_t kNoEvent = 0xffffffffu;
+
+// Release events of the items in the ring, oldest first (barrier index, parity); five slots.
+struct WideRing {
+    uint32_t b0, b1, b2, b3, b4;
+    uint32_t p0, p1, p2, p3, p4;
+};
+
+// Load K or V half h (d 128h .. 128h+127) of the key tile at key row `row` into the next ring
+// slot, once the item it replaces has been released; record the event that will release this
+// one. False on a timeout.
+__device__ __forceinline__ bool wide_load_half(uint64_t* bars, uint8_t* smem, WideRing& q, long long& item,
+                                               const CUtensorMap* map, int kvh, int row, int h, uint32_t rel_bar,
+                                               uint32_t rel_par, uint32_t leader, volatile int* abort_flag,
+                                               uint64_t wd) {
+    using L = LayoutWide;
+    static_assert(L::kSlots == 5, "ring of five slots");
+    if (q.b0 != kNoEvent && !warp_wait(&bars[q.b0], q.p0, abort_flag, wd)) return false;
+    q.b0 = q.b1, q.b1 = q.b2, q.b2 = q.b3, q.b3 = q.b4, q.b4 = rel_bar;
+    q.p0 = q.p1, q.p1 = q.p2, q.p2 = q.p3, q.p3 = q.p4, q.p4 = rel_par;
+    const int slot = (int)(item % L::kSlots);
+    uint8_t* dst = smem + L::kSlotOff + slot * L::kSlotBytes;
+    mbar_arrive_expect_tx_by(leader, &bars[L::bSlot + slot], L::kSlotBytes);
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+        tma_load_3d_by(leader, dst + c * L::kChunkBytes, map, &bars[L::bSlot + slot], (2 * h + c) * 64, kvh, row);
+    ++item;
+    return true;
+}
+
+__global__ void __launch_bounds__(kWideThreads, 1)
+    attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+    using L = LayoutWide;
+    static_assert(L::kAlloc <= 232448, "shared memory");
+    constexpr int D = kWideD;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+    int* misc = reinterpret_cast<int*>(smem + L::kMiscOff);
+    int* pre = reinterpret_cast<int*>(smem + L::kPreOff);
+    int* lvl = reinterpret_cast<int*>(smem + L::kLvlOff);
+    int* perm = reinterpret_cast<int*>(smem + L::kPermOff);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[L::bQFull], 1);
+        mbar_init(&bars[L::bQEmpty], 1);
+        for (int i = 0; i < L::kSlots; ++i) mbar_init(&bars[L::bSlot + i], 1);
+        mbar_init(&bars[L::bSFull + 0], 1);
+        mbar_init(&bars[L::bSFull + 1], 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars[L::bPFull + b], 4);
+            mbar_init(&bars[L::bPRest + b], 4);
+        }
+        mbar_init(&bars[L::bVDone], 1);
+        mbar_init(&bars[L::bOFull], 1);
+        mbar_init(&bars[L::bDrain], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (p.cu_seqlens && warp == 2) {
+        int levels, tiles;
+        build_packed_order(p, pre, lvl, perm, reinterpret_cast<int*>(smem + L::kNbOff), lane, L::kMaxLv, levels, tiles);
+        if (lane == 0) {
+            misc[2] = levels;
+            misc[3] = tiles;
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    int total = p.total_tiles;
+    const PackedOrder po{pre, lvl, perm, p.cu_seqlens ? misc[2] : 0};
+    if (p.cu_seqlens) total = misc[3];
+    const uint32_t tmem = *tmem_slot;
+    const uint64_t wd = p.watchdog_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        const uint32_t leader = lane == 0;
+        uint32_t qph = 0;
+        WideRing ring{kNoEvent, kNoEvent, kNoEvent, kNoEvent, kNoEvent, 0, 0, 0, 0, 0};
+        uint32_t pv_par = 0, s_par = 0;  // parity of the next O += P V event; bit b: of the next S-buffer-b event
+        long long item = 0;
+        bool ok = true;
+        for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
+            const int w = snake_index(r);
+            if (w >= total) continue;
+            Tile t;
+            get_tile<BN>(p, po, w, t);
+            for (int s = 0; s < 2 && ok; ++s) {
+                const int ns = s ? t.n[1] : t.n[0];
+                if (ns == 0) continue;
+                if (!(ok = warp_wait(&bars[L::bQEmpty], qph ^ 1u, abort_flag, wd))) break;
+                qph ^= 1u;
+                mbar_arrive_expect_tx_by(leader, &bars[L::bQFull], L::kQBytes);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tma_load_3d_by(leader, smem + L::kQOff + c * L::kChunkBytes, &tmQ, &bars[L::bQFull], c * 64, t.h,
+                                   t.q0 + t.r0 + s * BM);
+                // K halves of tiles 0 and 1, then per step V_n and K_{n+2}
+                for (int m = 0; m < ns && m < 2 && ok; ++m) {
+                    const uint32_t sb = (uint32_t)(m & 1), par = (s_par >> sb) & 1u;
+                    for (int h = 0; h < 2 && ok; ++h)
+                        ok = wide_load_half(bars, smem, ring, item, &tmK, t.kvh, t.k0 + m * BN, h, L::bSFull + sb, par,
+                                            leader, abort_flag, wd);
+                    s_par ^= 1u << sb;
+                }
+                for (int n = 0; n < ns && ok; ++n) {
+                    for (int h = 0; h < 2 && ok; ++h)
+                        ok = wide_load_half(bars, smem, ring, item, &tmV, t.kvh, t.k0 + n * BN, h, L::bVDone, pv_par,
+                                            leader, abort_flag, wd);
+                    pv_par ^= 1u;
+                    if (n + 2 < ns) {
+                        const uint32_t sb = (uint32_t)(n & 1), par = (s_par >> sb) & 1u;
+                        for (int h = 0; h < 2 && ok; ++h)
+                            ok = wide_load_half(bars, smem, ring, item, &tmK, t.kvh, t.k0 + (n + 2) * BN, h,
+                                                L::bSFull + sb, par, leader, abort_flag, wd);
+                        s_par ^= 1u << sb;
+                    }
+                }
+            }
+        }
+        if (!ok) {
+            // Let copies already in flight land before the CTA can exit.
+            for (int i = 0; i < L::kSlots && i < item; ++i) {
+                const long long it = item - 1 - i;
+                int dummy = 0;
+                mbar_wait(&bars[L::bSlot + (int)(it % L::kSlots)], (uint32_t)((it / L::kSlots) & 1), &dummy, 20000000ull);
+            }
+            int dummy = 0;
+            mbar_wait(&bars[L::bQFull], qph ^ 1u, &dummy, 20000000ull);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        // Per Q tile: S(0), S(1); then per step n: O += P(n) V_n (both 128-column halves of O,
+        // the first three quarters of the keys as soon as P stage 1 is written), one commit
+        // (bVDone), then S(n+2) into the buffer of P(n) and its commit. The S(n+2) products
+        // follow O += P(n) V_n in issue order, so they overwrite P(n) only after it is read.
+        const uint32_t leader = lane == 0;
+        constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0);
+        constexpr uint32_t idO = idesc_bf16_f32(BM, 128, 1);
+        constexpr int kPA = (3 * BN / 4) / 16;  // P stage 1: k-steps 0 .. kPA-1
+        const uint32_t q_base = smem_u32(smem + L::kQOff);
+        const uint32_t slot_base = smem_u32(smem + L::kSlotOff);
+        const uint64_t dq = smem_desc_sw128(q_base, 16, 1024);
+        const uint64_t dk0 = smem_desc_sw128(slot_base, 16, 1024);
+        const uint64_t dv0 = smem_desc_sw128(slot_base, L::kChunkBytes, 1024);
+        uint32_t qf = 0, pf = 0;  // pf bit b: parity of the next P phase of S buffer b
+        long long item = 0;
+        bool ok = true, any = false;
+        // Wait for the next ring item; returns its slot.
+        auto next_slot = [&](int& slot) -> bool {
+            slot = (int)(item % L::kSlots);
+            const uint32_t par = (uint32_t)((item / L::kSlots) & 1);
+            ++item;
+            return warp_wait(&bars[L::bSlot + slot], par, abort_flag, wd);
+        };
+        // S(m) = Q K_m^T into S buffer sb, from the two K halves in slots ka and kb
+        auto issue_s = [&](int ka, int kb, uint32_t sb) {
+            const uint32_t colS = kWideColS + 128u * sb;
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const int chunk = k >> 2;
+                const int slot = chunk < 2 ? ka : kb;
+                const uint64_t oq = (uint64_t)((chunk * L::kChunkBytes + (k & 3) * 32) >> 4);
+                const uint64_t ok_ =
+                    (uint64_t)((slot * L::kSlotBytes + (chunk & 1) * L::kChunkBytes + (k & 3) * 32) >> 4);
+                tc_mma_ss_by(leader, tmem + colS, dq + oq, dk0 + ok_, idS, k > 0 ? 1u : 0u);
+            }
+        };
+        for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
+            const int w = snake_index(r);
+            if (w >= total) continue;
+            Tile t;
+            get_tile<BN>(p, po, w, t);
+            for (int s = 0; s < 2 && ok; ++s) {
+                const int ns = s ? t.n[1] : t.n[0];
+                if (ns == 0) continue;
+                if (!(ok = warp_wait(&bars[L::bQFull], qf, abort_flag, wd))) break;
+                qf ^= 1u;
+                any = true;
+                tc_fence_after();
+                for (int m = 0; m < ns && m < 2; ++m) {
+                    int ka, kb;
+                    if (!(ok = next_slot(ka)) || !(ok = next_slot(kb))) break;
+                    tc_fence_after();
+                    issue_s(ka, kb, (uint32_t)(m & 1));
+                    __syncwarp();
+                    tc_commit_by(leader, &bars[L::bSFull + (m & 1)]);
+                    if (m == ns - 1) tc_commit_by(leader, &bars[L::bQEmpty]);
+                }
+                for (int n = 0; n < ns && ok; ++n) {
+                    const uint32_t sb = (uint32_t)(n & 1);
+                    const uint32_t colS = kWideColS + 128u * sb;
+                    if (!(ok = warp_wait(&bars[L::bPFull + sb], (pf >> sb) & 1u, abort_flag, wd))) break;
+                    int va, vb;
+                    if (!(ok = next_slot(va)) || !(ok = next_slot(vb))) break;
+                    tc_fence_after();
+                    const uint64_t vda = dv0 + (uint64_t)((va * L::kSlotBytes) >> 4);
+                    const uint64_t vdb = dv0 + (uint64_t)((vb * L::kSlotBytes) >> 4);
+                    const uint32_t acc0 = n > 0 ? 1u : 0u;
+#pragma unroll
+                    for (int k = 0; k < kPA; ++k) {  // P stage 1, both halves of O
+                        tc_mma_ts_by(leader, tmem + kWideColO, tmem + colS + k * 8, vda + (uint64_t)(k * (2048 >> 4)),
+                                     idO, k == 0 ? acc0 : 1u);
+                        tc_mma_ts_by(leader, tmem + kWideColO + 128, tmem + colS + k * 8,
+                                     vdb + (uint64_t)(k * (2048 >> 4)), idO, k == 0 ? acc0 : 1u);
+                    }
+                    if (!(ok = warp_wait(&bars[L::bPRest + sb], (pf >> sb) & 1u, abort_flag, wd))) break;
+                    pf ^= 1u << sb;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = kPA; k < BN / 16; ++k) {  // P stage 2
+                        tc_mma_ts_by(leader, tmem + kWideColO, tmem + colS + k * 8, vda + (uint64_t)(k * (2048 >> 4)),
+                                     idO, 1u);
+                        tc_mma_ts_by(leader, tmem + kWideColO + 128, tmem + colS + k * 8,
+                                     vdb + (uint64_t)(k * (2048 >> 4)), idO, 1u);
+                    }
+                    __syncwarp();
+                    tc_commit_by(leader, &bars[L::bVDone]);
+                    if (n == ns - 1) tc_commit_by(leader, &bars[L::bOFull]);
+                    if (n + 2 < ns) {
+                        int ka, kb;
+                        if (!(ok = next_slot(ka)) || !(ok = next_slot(kb))) break;
+                        tc_fence_after();
+                        issue_s(ka, kb, sb);
+                        __syncwarp();
+                        tc_commit_by(leader, &bars[L::bSFull + sb]);
+                        if (n + 2 == ns - 1) tc_commit_by(leader, &bars[L::bQEmpty]);
+                    }
+                }
+            }
+        }
+        if (any) {
+            // Wait until every MMA this warp issued has completed before TMEM can be released.
+            tc_commit_by(leader, &bars[L::bDrain]);
+            int dummy = 0;
+            if (leader) mbar_wait(&bars[L::bDrain], 0, &dummy, 50000000ull);
+            __syncwarp();
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------------ softmax + output
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tO = tmem + lane_off + kWideColO;
+        const float sl2 = p.scale_log2;
+        uint32_t sf = 0, of = 0, pv_done = 0;  // sf bit b: S buffer b parity; pv_done: O += P V steps before this tile
+        unsigned long long c_dec = 0, c_res = 0;
+        bool ok = true;
+        for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
+            const int w = snake_index(r);
+            if (w >= total) continue;
+            Tile t;
+            get_tile<BN>(p, po, w, t);
+            for (int s = 0; s < 2 && ok; ++s) {
+                const int tile_row0 = t.r0 + s * BM;
+                if (tile_row0 >= t.Lq) continue;
+                const int ns = s ? t.n[1] : t.n[0];
+                const int qrow = tile_row0 + row;
+                const bool valid = qrow < t.Lq;
+                const long long tok = (long long)t.q0 + qrow;
+                __nv_bfloat16* orow = p.o + (tok * p.Hq + t.h) * D;
+                if (ns == 0) {  // no visible key: zero output, LSE -inf
+                    if (valid) {
+                        const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                        for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+                        p.lse[tok * p.Hq + t.h] = -INFINITY;
+                    }
+                    continue;
+                }
+                const int off = t.Lk - t.Lq;
+                float m = -INFINITY, l = 0.0f;
+                for (int n = 0; n < ns; ++n) {
+                    const uint32_t sb = (uint32_t)(n & 1);
+                    const uint32_t tS = tmem + lane_off + kWideColS + 128u * sb;
+                    if (!warp_wait(&bars[L::bSFull + sb], (sf >> sb) & 1u, abort_flag, wd)) { ok = false; break; }
+                    sf ^= 1u << sb;
+                    tc_fence_after();
+                    uint32_t rr[BN / 32][32];
+#pragma unroll
+                    for (int i = 0; i < BN / 32; ++i) tmem_ld32(tS + 32 * i, rr[i]);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < BN / 32; ++i) reg_fence(rr[i]);
+                    float sv[BN];
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) sv[c] = __uint_as_float(rr[c >> 5][c & 31]);
+                    const int kb = n * BN;
+                    const bool need_mask = (kb + BN > t.Lk) || (p.causal && kb + BN - 1 > tile_row0 + off);
+                    if (need_mask) {
+                        const int lim = (p.causal ? min(t.Lk, qrow + off + 1) : t.Lk) - kb;
+#pragma unroll
+                        for (int c = 0; c < BN; ++c)
+                            if (c >= lim) sv[c] = -INFINITY;
+                    }
+                    float mx[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[i], sv[i + 8]);
+#pragma unroll
+                    for (int c = 16; c < BN; c += 16)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mx[i] = max3f(mx[i], sv[c + i], sv[c + 8 + i]);
+                    const float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+                    const float m_cand = fmaxf(m, mt);
+                    const bool need = (m_cand - m) * sl2 > p.rescale_thr;  // NaN (both -inf) is false
+                    if (__any_sync(0xffffffffu, need)) {
+                        const float alpha = (m == -INFINITY) ? 0.0f : ex2_mufu((m - m_cand) * sl2);
+                        if (n > 0) {
+                            // O += P(n-1) V_{n-1} must be complete before O is rescaled (S(n) was
+                            // issued before it, so the S barrier does not cover it).
+                            if (!warp_wait(&bars[L::bVDone], (pv_done + (uint32_t)n - 1u) & 1u, abort_flag, wd)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+#pragma unroll 1
+                            for (int c = 0; c < D; c += 16) {
+                                uint32_t o[16];
+                                tmem_ld16(tO + c, o);
+                                tc_wait_ld();
+                                reg_fence(o);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                                tmem_st16(tO + c, o);
+                            }
+                        }
+                        l *= alpha;
+                        m = m_cand;
+                        ++c_res;
+                    }
+                    ++c_dec;
+                    const float neg = (m == -INFINITY) ? 0.0f : -m * sl2;
+                    float sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                    uint32_t pk[BN / 2];
+                    constexpr int kSA = (3 * BN / 4) / 16 * 16;
+                    auto exp_pair = [&](int c) {
+                        float x0, x1;
+                        ffma2(x0, x1, sv[c], sv[c + 1], sl2, sl2, neg, neg);
+                        const float p0 = ex2_mufu(x0), p1 = ex2_mufu(x1);
+                        const int a = ((c >> 1) & 3) * 2;
+                        fadd2(sum[a], sum[a + 1], sum[a], sum[a + 1], p0, p1);
+                        pk[c >> 1] = pack_bf16x2(p0, p1);
+                    };
+#pragma unroll
+                    for (int c = 0; c < kSA; c += 2) exp_pair(c);
+                    store_p_cols<0, kSA / 2>(tS, pk);
+                    tc_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[L::bPFull + sb]);
+#pragma unroll
+                    for (int c = kSA; c < BN; c += 2) exp_pair(c);
+                    store_p_cols<kSA / 2, BN / 2>(tS, pk);
+                    l += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+                    tc_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[L::bPRest + sb]);
+                }
+                if (!ok) break;
+                pv_done += (uint32_t)ns;
+                // output: O / l in bf16 and the LSE, once the last O += P V is complete
+                if (!warp_wait(&bars[L::bOFull], of, abort_flag, wd)) { ok = false; break; }
+                of ^= 1u;
+                tc_fence_after();
+                const float inv = l > 0.0f ? p.out_scale / l : 0.0f;
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c, o);
+                    tc_wait_ld();
+                    reg_fence(o);
+                    if (valid) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+                        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
+                }
+                // the next tile's first P V product overwrites O: the loads above are ordered
+                // before it by the fence and arrive that publish that tile's P
+                if (valid) p.lse[tok * p.Hq + t.h] = l > 0.0f ? m * p.scale + logf(l) : -INFINITY;
+            }
+        }
+        if (p.counters && lane == 0) {
+            atomicAdd(p.counters + 0, c_dec);
+            atomicAdd(p.counters + 1, c_res);
+            atomicAdd(p.counters + 3, c_dec * 32ull * BN);
+        }
+    }
+
+    // ---------------------------------------------------------------------- teardown
+    __syncwarp();
+    tc_fence_before();
+    named_bar_sync(1, kWideThreads);
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (threadIdx.x == 0 && *abort_flag && p.status) {
+        atomicCAS(p.status, 0, kDevTimeout);
+        atomicAdd(p.status + 1, 1);
+    }
+}
+
+cudaError_t launch_wide(const FwdTmaps& tm, const FwdParams& p, int grid, cudaStream_t stream) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(attn_fwd_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, LayoutWide::kAlloc);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    attn_fwd_wide_kernel<<<grid, kWideThreads, LayoutWide::kAlloc, stream>>>(tm.q, tm.k, tm.v, p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
-int fwd_max_varlen_batch(int d) { return d > 128 ? Layout<192, 0, 128, kBNWide>::kMaxB : kMaxVarlenB; }
+int fwd_max_varlen_batch(int d) {
+    if (d == kWideD) return LayoutWide::kMaxB;
+    return d > 128 ? Layout<192, 0, 128, kBNWide>::kMaxB : kMaxVarlenB;
+}
+
+cudaError_t launch_attn_fwd_wide(const FwdTmaps& tm, const FwdParams& p, int grid, cudaStream_t stream) {
+    return launch_wide(tm, p, grid, stream);
+}
 
 cudaError_t launch_attn_fwd_hd(const FwdTmaps& tm, const FwdParams& p, int d, int dv, int grid, cudaStream_t stream) {
     if (d == 192 && dv == 128) return launch_t<192, 0, 0, 128, kBNWide>(tm, p, grid, stream);

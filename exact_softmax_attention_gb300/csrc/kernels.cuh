@@ -49,6 +49,8 @@ cudaError_t launch_attn_fwd_fp8(const FwdTmaps& tm, const FwdParams& p, int d, i
                                 cudaStream_t stream);
 // Head dims (d, dv) = (192, 128): q, k 192 wide, v, o 128 wide; key tiles of 96 rows.
 cudaError_t launch_attn_fwd_hd(const FwdTmaps& tm, const FwdParams& p, int d, int dv, int grid, cudaStream_t stream);
+// Head width 256 (q, k, v, o): one 128-row Q tile at a time, two S buffers in TMEM.
+cudaError_t launch_attn_fwd_wide(const FwdTmaps& tm, const FwdParams& p, int grid, cudaStream_t stream);
 // Largest number of packed sequences of one call for query/key width d.
 int fwd_max_varlen_batch(int d);
 

@@ -72,13 +72,15 @@ typedef int attn_status_t;
  *           k/v (the sequence lengths come from cu_seqlens and queries and keys share them;
  *           a sequence reaching past Nq or Nk is treated as empty and recorded as
  *           ATTN_ERR_DEVICE_BAD_INDEX)
- * d         head dimension, 64 or 128
+ * d         head dimension, 64, 128 or 256 (256: one 128-row query tile per CTA at a time,
+ *           key/value tiles streamed in 128-column halves; packed calls take at most 64
+ *           sequences)
  * scale     multiplier of q.k (typically 1/sqrt(d)); must be finite
  * causal    0: every key is visible. 1: bottom-right aligned mask, key j visible to query
  *           row i of its sequence iff j <= i + (Nk - Nq). Rows that see no key get o = 0
  *           and lse = -inf.
  * cu_seqlens NULL for dense batches, else device int32 [B+1] prefix offsets of packed
- *           sequences (non-decreasing; B <= 1024).
+ *           sequences (non-decreasing; B <= 1024, and B <= 64 when d = 256).
  * Alignment: q, k, v, o 16 bytes; lse 4 bytes.
  * Returns ATTN_OK or an error code; see the conventions above.
  */
@@ -94,7 +96,8 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
  * q           device, bf16 [T, Hq, d]      k  device, bf16 [Tk, Hkv, d]
  * v           device, bf16 [Tk, Hkv, dv]   o  device, bf16 [T, Hq, dv] (written)
  * lse         device, fp32 [T, Hq] (written)
- * d, dv       (192, 128); (64, 64) and (128, 128) are also accepted and behave as attn_fwd.
+ * d, dv       (192, 128); (64, 64), (128, 128) and (256, 256) are also accepted and behave as
+ *             attn_fwd.
  *             Anything else is ATTN_ERR_BAD_SHAPE.
  * Everything else is as for attn_fwd. With (192, 128) the kernel uses 96-key tiles (the
  * 192-wide query and key tiles leave no room in shared memory for 128-key tiles), and a
