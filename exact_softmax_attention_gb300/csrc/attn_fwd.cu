@@ -1008,29 +1008,49 @@ struct LayoutWide {
 // K0a K0b K1a K1b | V0a V0b K2a K2b | V1a V1b K3a K3b | ... (K_{n+2} only while n + 2 < ns).
 // Item i lives in slot i % 5. The producer refills a slot once the products that read its
 // item are complete: S(m) = Q K_m^T for a K half (the S-buffer barrier of m % 2), O += P(n)
-// V_n for a V half (bVDone, one phase per step). Both sides enumerate the same sequence, and
-// slots are refilled in the order they were filled, so every parity wait below is at most
-// one phase behind or ahead of the barrier it reads.
+// V_n for a V half (bVDone, one phase per step). Those barriers are shared by several items,
+// and a parity wait is only meaningful while the barrier is at most one phase past the phase
+// waited for, so the producer observes every phase of them in order and, before loading the
+// item that lets the next product of a barrier start (the second half of V_n or of K_m), it
+// first observes that barrier's previous product. A barrier then never completes a phase
+// the producer has not yet observed and the one after it.
 constexpr uint32_t kNoEvent = 0xffffffffu;
+constexpr uint32_t kEvPV = 0u, kEvS0 = 1u, kEvS1 = 2u;  // event kinds: bVDone, bSFull + 0, bSFull + 1
 
-// Release events of the items in the ring, oldest first (barrier index, parity); five slots.
-struct WideRing {
-    uint32_t b0, b1, b2, b3, b4;
-    uint32_t p0, p1, p2, p3, p4;
+// Events observed so far per barrier, and the release events of the items in the ring
+// (kind << 30 | index of the event on its barrier), oldest first.
+struct WideEvents {
+    uint32_t seen[3];
+    uint32_t r0, r1, r2, r3, r4;
 };
 
+// Wait until the event barrier of `kind` has completed phases 0 .. upto-1, one phase at a time.
+__device__ __forceinline__ bool wide_observe(uint64_t* bars, WideEvents& ev, uint32_t kind, uint32_t upto,
+                                             volatile int* abort_flag, uint64_t wd) {
+    using L = LayoutWide;
+    uint64_t* bar = &bars[kind == kEvPV ? L::bVDone : L::bSFull + (kind - kEvS0)];
+    uint32_t seen = kind == kEvPV ? ev.seen[0] : (kind == kEvS0 ? ev.seen[1] : ev.seen[2]);
+    while (seen < upto) {
+        if (!warp_wait(bar, seen & 1u, abort_flag, wd)) return false;
+        ++seen;
+    }
+    if (kind == kEvPV) ev.seen[0] = seen;
+    else if (kind == kEvS0) ev.seen[1] = seen;
+    else ev.seen[2] = seen;
+    return true;
+}
+
 // Load K or V half h (d 128h .. 128h+127) of the key tile at key row `row` into the next ring
-// slot, once the item it replaces has been released; record the event that will release this
-// one. False on a timeout.
-__device__ __forceinline__ bool wide_load_half(uint64_t* bars, uint8_t* smem, WideRing& q, long long& item,
-                                               const CUtensorMap* map, int kvh, int row, int h, uint32_t rel_bar,
-                                               uint32_t rel_par, uint32_t leader, volatile int* abort_flag,
-                                               uint64_t wd) {
+// slot, once the item it replaces has been released; `rel` is the event that will release
+// this item (kind << 30 | index). False on a timeout.
+__device__ __forceinline__ bool wide_load_half(uint64_t* bars, uint8_t* smem, WideEvents& ev, long long& item,
+                                               const CUtensorMap* map, int kvh, int row, int h, uint32_t rel,
+                                               uint32_t leader, volatile int* abort_flag, uint64_t wd) {
     using L = LayoutWide;
     static_assert(L::kSlots == 5, "ring of five slots");
-    if (q.b0 != kNoEvent && !warp_wait(&bars[q.b0], q.p0, abort_flag, wd)) return false;
-    q.b0 = q.b1, q.b1 = q.b2, q.b2 = q.b3, q.b3 = q.b4, q.b4 = rel_bar;
-    q.p0 = q.p1, q.p1 = q.p2, q.p2 = q.p3, q.p3 = q.p4, q.p4 = rel_par;
+    if (ev.r0 != kNoEvent && !wide_observe(bars, ev, ev.r0 >> 30, (ev.r0 & 0x3fffffffu) + 1u, abort_flag, wd))
+        return false;
+    ev.r0 = ev.r1, ev.r1 = ev.r2, ev.r2 = ev.r3, ev.r3 = ev.r4, ev.r4 = rel;
     const int slot = (int)(item % L::kSlots);
     uint8_t* dst = smem + L::kSlotOff + slot * L::kSlotBytes;
     mbar_arrive_expect_tx_by(leader, &bars[L::bSlot + slot], L::kSlotBytes);
@@ -1058,6 +1078,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     int* perm = reinterpret_cast<int*>(smem + L::kPermOff);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    ATTN_TL_DECL(int tl_idx = 0);
 
     if (threadIdx.x == 0) {
         mbar_init(&bars[L::bQFull], 1);
@@ -1105,8 +1126,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         // ------------------------------------------------------------------ TMA producer
         const uint32_t leader = lane == 0;
         uint32_t qph = 0;
-        WideRing ring{kNoEvent, kNoEvent, kNoEvent, kNoEvent, kNoEvent, 0, 0, 0, 0, 0};
-        uint32_t pv_par = 0, s_par = 0;  // parity of the next O += P V event; bit b: of the next S-buffer-b event
+        WideEvents ev{{0, 0, 0}, kNoEvent, kNoEvent, kNoEvent, kNoEvent, kNoEvent};
+        uint32_t n_pv = 0, n_s0 = 0, n_s1 = 0;  // products assigned so far: O += P V steps, S per buffer
         long long item = 0;
         bool ok = true;
         for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
@@ -1124,25 +1145,30 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 for (int c = 0; c < 4; ++c)
                     tma_load_3d_by(leader, smem + L::kQOff + c * L::kChunkBytes, &tmQ, &bars[L::bQFull], c * 64, t.h,
                                    t.q0 + t.r0 + s * BM);
-                // K halves of tiles 0 and 1, then per step V_n and K_{n+2}
-                for (int m = 0; m < ns && m < 2 && ok; ++m) {
-                    const uint32_t sb = (uint32_t)(m & 1), par = (s_par >> sb) & 1u;
-                    for (int h = 0; h < 2 && ok; ++h)
-                        ok = wide_load_half(bars, smem, ring, item, &tmK, t.kvh, t.k0 + m * BN, h, L::bSFull + sb, par,
-                                            leader, abort_flag, wd);
-                    s_par ^= 1u << sb;
-                }
+                // S(m) on buffer m % 2: its two K halves; the second lets the product start
+                auto load_k = [&](int m) {
+                    const uint32_t b = (uint32_t)(m & 1), kind = b ? kEvS1 : kEvS0, idx = b ? n_s1++ : n_s0++;
+                    ok = wide_load_half(bars, smem, ev, item, &tmK, t.kvh, t.k0 + m * BN, 0, (kind << 30) | idx, leader,
+                                        abort_flag, wd) &&
+                         wide_observe(bars, ev, kind, idx, abort_flag, wd) &&
+                         wide_load_half(bars, smem, ev, item, &tmK, t.kvh, t.k0 + m * BN, 1, (kind << 30) | idx, leader,
+                                        abort_flag, wd);
+                };
+                for (int m = 0; m < ns && m < 2 && ok; ++m) load_k(m);
                 for (int n = 0; n < ns && ok; ++n) {
-                    for (int h = 0; h < 2 && ok; ++h)
-                        ok = wide_load_half(bars, smem, ring, item, &tmV, t.kvh, t.k0 + n * BN, h, L::bVDone, pv_par,
-                                            leader, abort_flag, wd);
-                    pv_par ^= 1u;
-                    if (n + 2 < ns) {
-                        const uint32_t sb = (uint32_t)(n & 1), par = (s_par >> sb) & 1u;
-                        for (int h = 0; h < 2 && ok; ++h)
-                            ok = wide_load_half(bars, smem, ring, item, &tmK, t.kvh, t.k0 + (n + 2) * BN, h,
-                                                L::bSFull + sb, par, leader, abort_flag, wd);
-                        s_par ^= 1u << sb;
+                    ATTN_TL_DECL(long long tv = clock64());
+                    // O += P(n) V_n: its two V halves; the second lets the product start
+                    const uint32_t idx = n_pv++;
+                    ok = wide_load_half(bars, smem, ev, item, &tmV, t.kvh, t.k0 + n * BN, 0, (kEvPV << 30) | idx, leader,
+                                        abort_flag, wd) &&
+                         wide_observe(bars, ev, kEvPV, idx, abort_flag, wd) &&
+                         wide_load_half(bars, smem, ev, item, &tmV, t.kvh, t.k0 + n * BN, 1, (kEvPV << 30) | idx, leader,
+                                        abort_flag, wd);
+                    ATTN_TL(0, 0, n, tv, clock64());
+                    if (n + 2 < ns && ok) {
+                        ATTN_TL_DECL(long long tk = clock64());
+                        load_k(n + 2);
+                        ATTN_TL(0, 1, n, tk, clock64());
                     }
                 }
             }
@@ -1182,18 +1208,25 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             ++item;
             return warp_wait(&bars[L::bSlot + slot], par, abort_flag, wd);
         };
-        // S(m) = Q K_m^T into S buffer sb, from the two K halves in slots ka and kb
-        auto issue_s = [&](int ka, int kb, uint32_t sb) {
+        // S(m) = Q K_m^T into S buffer sb: the k-steps of the first K half (d 0-127) as soon as it
+        // has landed, then those of the second; false on a timeout
+        auto issue_s = [&](uint32_t sb) -> bool {
             const uint32_t colS = kWideColS + 128u * sb;
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const int chunk = k >> 2;
-                const int slot = chunk < 2 ? ka : kb;
-                const uint64_t oq = (uint64_t)((chunk * L::kChunkBytes + (k & 3) * 32) >> 4);
-                const uint64_t ok_ =
-                    (uint64_t)((slot * L::kSlotBytes + (chunk & 1) * L::kChunkBytes + (k & 3) * 32) >> 4);
-                tc_mma_ss_by(leader, tmem + colS, dq + oq, dk0 + ok_, idS, k > 0 ? 1u : 0u);
+            for (int h = 0; h < 2; ++h) {
+                int slot;
+                if (!next_slot(slot)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int k = 8 * h + kk;
+                    const uint64_t oq = (uint64_t)(((k >> 2) * L::kChunkBytes + (k & 3) * 32) >> 4);
+                    const uint64_t ok_ =
+                        (uint64_t)((slot * L::kSlotBytes + ((kk >> 2) & 1) * L::kChunkBytes + (k & 3) * 32) >> 4);
+                    tc_mma_ss_by(leader, tmem + colS, dq + oq, dk0 + ok_, idS, k > 0 ? 1u : 0u);
+                }
             }
+            return true;
         };
         for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
             const int w = snake_index(r);
@@ -1208,10 +1241,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 any = true;
                 tc_fence_after();
                 for (int m = 0; m < ns && m < 2; ++m) {
-                    int ka, kb;
-                    if (!(ok = next_slot(ka)) || !(ok = next_slot(kb))) break;
-                    tc_fence_after();
-                    issue_s(ka, kb, (uint32_t)(m & 1));
+                    if (!(ok = issue_s((uint32_t)(m & 1)))) break;
                     __syncwarp();
                     tc_commit_by(leader, &bars[L::bSFull + (m & 1)]);
                     if (m == ns - 1) tc_commit_by(leader, &bars[L::bQEmpty]);
@@ -1219,20 +1249,29 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 for (int n = 0; n < ns && ok; ++n) {
                     const uint32_t sb = (uint32_t)(n & 1);
                     const uint32_t colS = kWideColS + 128u * sb;
+                    ATTN_TL_DECL(long long t0 = clock64());
                     if (!(ok = warp_wait(&bars[L::bPFull + sb], (pf >> sb) & 1u, abort_flag, wd))) break;
+                    ATTN_TL_DECL(long long t1 = clock64());
+                    // P stage 1 (keys 0-95) with each V half as soon as it has landed: O columns
+                    // 0-127 from V_n's d 0-127, then columns 128-255 from d 128-255
+                    const uint32_t acc0 = n > 0 ? 1u : 0u;
                     int va, vb;
-                    if (!(ok = next_slot(va)) || !(ok = next_slot(vb))) break;
+                    if (!(ok = next_slot(va))) break;
+                    ATTN_TL(1, 100, n, t0, t1);
+                    ATTN_TL(1, 101, n, clock64(), 0);
                     tc_fence_after();
                     const uint64_t vda = dv0 + (uint64_t)((va * L::kSlotBytes) >> 4);
-                    const uint64_t vdb = dv0 + (uint64_t)((vb * L::kSlotBytes) >> 4);
-                    const uint32_t acc0 = n > 0 ? 1u : 0u;
 #pragma unroll
-                    for (int k = 0; k < kPA; ++k) {  // P stage 1, both halves of O
+                    for (int k = 0; k < kPA; ++k)
                         tc_mma_ts_by(leader, tmem + kWideColO, tmem + colS + k * 8, vda + (uint64_t)(k * (2048 >> 4)),
                                      idO, k == 0 ? acc0 : 1u);
+                    if (!(ok = next_slot(vb))) break;
+                    tc_fence_after();
+                    const uint64_t vdb = dv0 + (uint64_t)((vb * L::kSlotBytes) >> 4);
+#pragma unroll
+                    for (int k = 0; k < kPA; ++k)
                         tc_mma_ts_by(leader, tmem + kWideColO + 128, tmem + colS + k * 8,
                                      vdb + (uint64_t)(k * (2048 >> 4)), idO, k == 0 ? acc0 : 1u);
-                    }
                     if (!(ok = warp_wait(&bars[L::bPRest + sb], (pf >> sb) & 1u, abort_flag, wd))) break;
                     pf ^= 1u << sb;
                     tc_fence_after();
@@ -1246,14 +1285,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                     __syncwarp();
                     tc_commit_by(leader, &bars[L::bVDone]);
                     if (n == ns - 1) tc_commit_by(leader, &bars[L::bOFull]);
+                    ATTN_TL(1, 102, n, clock64(), 0);
                     if (n + 2 < ns) {
-                        int ka, kb;
-                        if (!(ok = next_slot(ka)) || !(ok = next_slot(kb))) break;
-                        tc_fence_after();
-                        issue_s(ka, kb, sb);
+                        ATTN_TL(1, 103, n, clock64(), 0);
+                        if (!(ok = issue_s(sb))) break;
                         __syncwarp();
                         tc_commit_by(leader, &bars[L::bSFull + sb]);
                         if (n + 2 == ns - 1) tc_commit_by(leader, &bars[L::bQEmpty]);
+                        ATTN_TL(1, 104, n, clock64(), 0);
                     }
                 }
             }
@@ -1302,7 +1341,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 for (int n = 0; n < ns; ++n) {
                     const uint32_t sb = (uint32_t)(n & 1);
                     const uint32_t tS = tmem + lane_off + kWideColS + 128u * sb;
+                    ATTN_TL_DECL(long long ts0 = clock64());
                     if (!warp_wait(&bars[L::bSFull + sb], (sf >> sb) & 1u, abort_flag, wd)) { ok = false; break; }
+                    ATTN_TL_DECL(long long ts1 = clock64());
                     sf ^= 1u << sb;
                     tc_fence_after();
                     uint32_t rr[BN / 32][32];
@@ -1385,6 +1426,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars[L::bPRest + sb]);
+                    if (quarter == 0) ATTN_TL(2, n, ts0, ts1, clock64());
                 }
                 if (!ok) break;
                 pv_done += (uint32_t)ns;
