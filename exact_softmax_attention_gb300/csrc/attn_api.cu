@@ -232,7 +232,8 @@ static attn_status_t fwd(const void* q, const void* k, const void* v, void* o, f
         const long long tiles = pairs * nblk;
         if (tiles > INT32_MAX / 2) return ATTN_ERR_BAD_SHAPE;
         p.total_tiles = (int)tiles;
-        if (tiles < grid) grid = (int)tiles;
+        const long long units = d == 256 ? 2 * tiles : tiles;  // the d = 256 kernel takes one Q tile at a time
+        if (units < grid) grid = (int)units;
         // Section of (batch, head) pairs: all of them unless the tiles make 16 or more waves
         // of the grid; then sections of at least 8 waves each, which keeps the heaviest-first
         // order balanced within a section while fewer key/value heads share the L2.

@@ -968,10 +968,12 @@ cudaError_t launch_t(const FwdTmaps& tm, const FwdParams& p, int grid, cudaStrea
 
 // ------------------------------------------------------------------ d = 256
 // Head width 256: the accumulator O of one 128-row Q tile takes 256 of the 512 TMEM columns,
-// so a CTA works on one Q tile at a time (the two tiles of a 256-row work tile in turn) and
-// uses the other 256 columns for two S buffers: S(n+1) = Q K_{n+1}^T is computed while the
-// softmax works on S(n), and each KV step issues O += P(n) V_n then S(n+2) = Q K_{n+2}^T
-// into the buffer P(n) came from. K and V tiles (128 keys x 256) travel as 32 KB halves
+// so a CTA works on one Q tile at a time and uses the other 256 columns for two S buffers. The
+// unit of work is one Q tile; the two Q tiles of a 256-row work tile are consecutive units, so
+// neighbouring CTAs of a round take them and stream the same K/V tiles at about the same time
+// (the second read of each tile can hit the L2). S(n+1) = Q K_{n+1}^T is computed while the
+// softmax works on S(n), and each KV step issues O += P(n) V_n then S(n+2) = Q K_{n+2}^T into
+// the buffer P(n) came from. K and V tiles (128 keys x 256) travel as 32 KB halves
 // (d 0-127 and 128-255) through a ring of five slots. The softmax warps also write the
 // finished rows, so no separate epilogue warps or statistics exchange are needed.
 // TMEM columns: O [0,256), S0 [256,384), S1 [384,512).
@@ -1130,12 +1132,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         uint32_t n_pv = 0, n_s0 = 0, n_s1 = 0;  // products assigned so far: O += P V steps, S per buffer
         long long item = 0;
         bool ok = true;
-        for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
-            const int w = snake_index(r);
-            if (w >= total) continue;
+        for (int r = 0; r * (int)gridDim.x < 2 * total && ok; ++r) {
+            const int u = snake_index(r);
+            if (u >= 2 * total) continue;
             Tile t;
-            get_tile<BN>(p, po, w, t);
-            for (int s = 0; s < 2 && ok; ++s) {
+            get_tile<BN>(p, po, u >> 1, t);
+            {
+                const int s = u & 1;
                 const int ns = s ? t.n[1] : t.n[0];
                 if (ns == 0) continue;
                 if (!(ok = warp_wait(&bars[L::bQEmpty], qph ^ 1u, abort_flag, wd))) break;
@@ -1228,12 +1231,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             }
             return true;
         };
-        for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
-            const int w = snake_index(r);
-            if (w >= total) continue;
+        for (int r = 0; r * (int)gridDim.x < 2 * total && ok; ++r) {
+            const int u = snake_index(r);
+            if (u >= 2 * total) continue;
             Tile t;
-            get_tile<BN>(p, po, w, t);
-            for (int s = 0; s < 2 && ok; ++s) {
+            get_tile<BN>(p, po, u >> 1, t);
+            {
+                const int s = u & 1;
                 const int ns = s ? t.n[1] : t.n[0];
                 if (ns == 0) continue;
                 if (!(ok = warp_wait(&bars[L::bQFull], qf, abort_flag, wd))) break;
@@ -1314,12 +1318,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         uint32_t sf = 0, of = 0, pv_done = 0;  // sf bit b: S buffer b parity; pv_done: O += P V steps before this tile
         unsigned long long c_dec = 0, c_res = 0;
         bool ok = true;
-        for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
-            const int w = snake_index(r);
-            if (w >= total) continue;
+        for (int r = 0; r * (int)gridDim.x < 2 * total && ok; ++r) {
+            const int u = snake_index(r);
+            if (u >= 2 * total) continue;
             Tile t;
-            get_tile<BN>(p, po, w, t);
-            for (int s = 0; s < 2 && ok; ++s) {
+            get_tile<BN>(p, po, u >> 1, t);
+            {
+                const int s = u & 1;
                 const int tile_row0 = t.r0 + s * BM;
                 if (tile_row0 >= t.Lq) continue;
                 const int ns = s ? t.n[1] : t.n[0];
