@@ -116,3 +116,13 @@ def test_d256_through_attn_fwd_hd(A):
         outs.append((o, lse))
     torch.cuda.synchronize()
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_d256_noncausal_gqa_sampled(A):
+    """A non-causal GQA prefill (B2 Hq8 Hkv2 N4096, d 256) on sampled rows."""
+    c = case("d256_nc", 2, 8, 2, 4096, 4096, False, 96)
+    T = c.total_q
+    rng = np.random.default_rng(6)
+    rows = np.unique(np.concatenate([rng.choice(T * c.Hq, size=1200, replace=False), np.arange(c.Hq),
+                                     (T - 1) * c.Hq + np.arange(c.Hq)])).astype(np.int64)
+    check(A, c, rows=rows)
