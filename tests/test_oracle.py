@@ -96,7 +96,7 @@ def _torch_reference(q, k, v, scale, causal, Nq, Nk, G):
 
 @pytest.mark.parametrize("Nq,Nk,Hq,Hkv,d,causal", [
     (7, 7, 2, 2, 4, True), (5, 9, 4, 2, 8, True), (9, 9, 6, 3, 5, False), (16, 16, 4, 1, 16, True),
-    (3, 11, 8, 2, 3, False), (12, 12, 2, 2, 64, True)])
+    (3, 11, 8, 2, 3, False), (12, 12, 2, 2, 64, True), (10, 13, 4, 2, 256, True), (9, 6, 2, 1, 256, False)])
 def test_matches_torch_sdpa_float64(Nq, Nk, Hq, Hkv, d, causal):
     seed = 1000 + Nq * 31 + Nk * 7 + Hq + d
     q = _rand_case(seed, Nq, Hq, d)
