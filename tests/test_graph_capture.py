@@ -1,0 +1,97 @@
+"""Calls captured into a CUDA graph. The forward (d = 128 and the separate d = 256 kernel) and the
+allocation-free decode are captured once into one graph; replays give the same bytes as eager
+calls, and after new inputs are copied into the captured buffers a replay follows them. A
+serving loop drives the library this way instead of paying the host cost of each call (argument
+checks, tensor-map encoding, launch planning) every step."""
+import math
+
+import numpy as np
+import pytest
+
+import synth
+from helpers import ensure_built, to_dev
+from synth import workloads as W
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def A():
+    ensure_built()
+    import exact_softmax_attention_gb300 as mod
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return mod
+
+
+class Problem:
+    """Device buffers of one forward (d = 128), one forward (d = 256) and one paged decode."""
+
+    def __init__(self, seed):
+        self.f = W.PrefillCase("g128", 1, 4, 2, 600, 600, 128, 1.0 / math.sqrt(128), True, seed)
+        self.w = W.PrefillCase("g256", 1, 2, 1, 400, 400, 256, 1.0 / 16.0, True, seed + 1)
+        lens = synth.uniform_ints(4, 43, 100, 3000)  # same decode geometry for every seed
+        mp = int((int(lens.max()) + 15) // 16) + 1
+        self.d = W.DecodeCase("gdec", 4, 8, 2, 128, 16, lens, mp, 1.0 / math.sqrt(128), seed + 3)
+        self.fin = [to_dev(a, DEV) for a in self.f.generate()]
+        self.win = [to_dev(a, DEV) for a in self.w.generate()]
+        q, kc, vc, pt, sl = self.d.generate()
+        self.din = [to_dev(q, DEV), to_dev(kc, DEV), to_dev(vc, DEV), torch.from_numpy(pt).to(DEV),
+                    torch.from_numpy(sl).to(DEV)]
+        bf, f32 = torch.bfloat16, torch.float32
+        self.fo = torch.empty((self.f.total_q, 4, 128), dtype=bf, device=DEV)
+        self.fl = torch.empty((self.f.total_q, 4), dtype=f32, device=DEV)
+        self.wo = torch.empty((self.w.total_q, 2, 256), dtype=bf, device=DEV)
+        self.wl = torch.empty((self.w.total_q, 2), dtype=f32, device=DEV)
+        self.do = torch.empty((4, 8, 128), dtype=bf, device=DEV)
+        self.dl = torch.empty((4, 8), dtype=f32, device=DEV)
+
+    def run(self, A):
+        f, w, d = self.f, self.w, self.d
+        A.attn_fwd(*self.fin, self.fo, self.fl, f.B, f.Hq, f.Hkv, f.Nq, f.Nk, 128, f.scale, f.causal)
+        A.attn_fwd(*self.win, self.wo, self.wl, w.B, w.Hq, w.Hkv, w.Nq, w.Nk, 256, w.scale, w.causal)
+        q, kc, vc, pt, sl = self.din
+        A.attn_decode_paged_noalloc(q, kc, vc, pt, sl, d.page_size, self.do, self.dl, None, d.B, d.Hq, d.Hkv, d.d,
+                                    d.max_pages, d.num_pages, d.scale)
+
+    def outputs(self):
+        return [t.clone() for t in (self.fo, self.fl, self.wo, self.wl, self.do, self.dl)]
+
+    def poison(self):
+        for t in (self.fo, self.fl, self.wo, self.wl, self.do, self.dl):
+            t.fill_(float("nan"))
+
+
+def test_graph_replay_matches_eager(A):
+    p = Problem(41)
+    p.run(A)  # eager first: one-time set-up (device state, kernel attributes) stays out of the capture
+    torch.cuda.synchronize()
+    assert A.attn_get_device_status() == 0
+    ref = p.outputs()
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        p.run(A)
+    for _ in range(3):
+        p.poison()
+        g.replay()
+    torch.cuda.synchronize()
+    assert A.attn_get_device_status() == 0
+    for got, want in zip(p.outputs(), ref):
+        assert torch.equal(got, want)
+
+    # new inputs in the captured buffers: the replay computes on them
+    q = Problem(77)
+    for dst, src in zip(p.fin + p.win + p.din, q.fin + q.win + q.din):
+        dst.copy_(src)
+    q.run(A)
+    torch.cuda.synchronize()
+    ref2 = q.outputs()
+    p.poison()
+    g.replay()
+    torch.cuda.synchronize()
+    assert A.attn_get_device_status() == 0
+    for got, want in zip(p.outputs(), ref2):
+        assert torch.equal(got, want)
