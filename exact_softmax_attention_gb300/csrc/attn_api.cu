@@ -185,7 +185,6 @@ static attn_status_t fwd(const void* q, const void* k, const void* v, void* o, f
     if (causal != 0 && causal != 1) return ATTN_ERR_BAD_SHAPE;
     if (!isfinite(scale)) return ATTN_ERR_BAD_SHAPE;
     if (Hq > 65535 || Hkv > 65535) return ATTN_ERR_BAD_SHAPE;
-    if (cu_seqlens && B > attn::fwd_max_varlen_batch(d)) return ATTN_ERR_BAD_SHAPE;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
         (cu_seqlens && !aligned(cu_seqlens, 4)))
         return ATTN_ERR_ALIGN;
@@ -255,11 +254,24 @@ static attn_status_t fwd(const void* q, const void* k, const void* v, void* o, f
     }
     if (grid <= 0) return ATTN_OK;
     const cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = fp8 >= 0   ? attn::launch_attn_fwd_fp8(tm, p, d, fp8, grid, st_)
-                          : d != dv  ? attn::launch_attn_fwd_hd(tm, p, d, dv, grid, st_)
-                          : d == 256 ? attn::launch_attn_fwd_wide(tm, p, grid, st_)
-                                     : attn::launch_attn_fwd(tm, p, d, opt.exp_poly, grid, st_);
-    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    auto launch = [&](const FwdParams& lp) {
+        return fp8 >= 0   ? attn::launch_attn_fwd_fp8(tm, lp, d, fp8, grid, st_)
+               : d != dv  ? attn::launch_attn_fwd_hd(tm, lp, d, dv, grid, st_)
+               : d == 256 ? attn::launch_attn_fwd_wide(tm, lp, grid, st_)
+                          : attn::launch_attn_fwd(tm, lp, d, opt.exp_poly, grid, st_);
+    };
+    if (!cu_seqlens) return launch(p) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    // Packed sequences: one launch builds its work order in shared memory for at most maxB
+    // sequences, so a larger batch runs as consecutive launches of maxB sequences each (the
+    // offsets in cu_seqlens are absolute rows of q/k, so a launch only needs its slice of them).
+    const int maxB = attn::fwd_max_varlen_batch(d);
+    for (int b0 = 0; b0 < B; b0 += maxB) {
+        FwdParams lp = p;
+        lp.cu_seqlens = cu_seqlens + b0;
+        lp.B = B - b0 < maxB ? B - b0 : maxB;
+        if (launch(lp) != cudaSuccess) return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
 }
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,

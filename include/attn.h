@@ -73,14 +73,14 @@ typedef int attn_status_t;
  *           a sequence reaching past Nq or Nk is treated as empty and recorded as
  *           ATTN_ERR_DEVICE_BAD_INDEX)
  * d         head dimension, 64, 128 or 256 (256: one 128-row query tile per CTA at a time,
- *           key/value tiles streamed in 128-column halves; packed calls take at most 64
- *           sequences)
+ *           key/value tiles streamed in 128-column halves)
  * scale     multiplier of q.k (typically 1/sqrt(d)); must be finite
  * causal    0: every key is visible. 1: bottom-right aligned mask, key j visible to query
  *           row i of its sequence iff j <= i + (Nk - Nq). Rows that see no key get o = 0
  *           and lse = -inf.
  * cu_seqlens NULL for dense batches, else device int32 [B+1] prefix offsets of packed
- *           sequences (non-decreasing; B <= 1024, and B <= 64 when d = 256).
+ *           sequences (non-decreasing). One kernel launch takes up to 1024 sequences (64 at
+ *           d = 256); a larger B runs as consecutive launches of that many sequences each.
  * Alignment: q, k, v, o 16 bytes; lse 4 bytes.
  * Returns ATTN_OK or an error code; see the conventions above.
  */
@@ -100,8 +100,8 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
  *             attn_fwd.
  *             Anything else is ATTN_ERR_BAD_SHAPE.
  * Everything else is as for attn_fwd. With (192, 128) the kernel uses 96-key tiles (the
- * 192-wide query and key tiles leave no room in shared memory for 128-key tiles), and a
- * call with cu_seqlens takes at most 256 sequences.
+ * 192-wide query and key tiles leave no room in shared memory for 128-key tiles), and one
+ * launch takes up to 256 packed sequences (a larger batch runs as several launches).
  */
 attn_status_t attn_fwd_hd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                           int Nq, int Nk, int d, int dv, float scale, int causal, const int* cu_seqlens, void* stream);

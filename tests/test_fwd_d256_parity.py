@@ -126,3 +126,9 @@ def test_d256_noncausal_gqa_sampled(A):
     rows = np.unique(np.concatenate([rng.choice(T * c.Hq, size=1200, replace=False), np.arange(c.Hq),
                                      (T - 1) * c.Hq + np.arange(c.Hq)])).astype(np.int64)
     check(A, c, rows=rows)
+
+
+def test_d256_varlen_several_launches(A):
+    """150 packed sequences at d = 256: three launches of at most 64 sequences."""
+    rng = np.random.default_rng(97)
+    check(A, case("varlen150", 0, 2, 1, 0, 0, False, 98, lens=[int(x) for x in rng.integers(1, 300, size=150)]))

@@ -104,3 +104,9 @@ def test_hd_equal_dims_match_attn_fwd(A):
         outs.append((o, lse))
     torch.cuda.synchronize()
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_hd_varlen_several_launches(A):
+    """300 packed sequences with head dims (192, 128): two launches of at most 256 sequences."""
+    rng = np.random.default_rng(73)
+    check(A, case("varlen300", 0, 2, 2, 0, 0, True, 74, lens=[int(x) for x in rng.integers(1, 200, size=300)]))

@@ -179,3 +179,11 @@ def test_counters_report_skipped_rescales(A):
     # one decision per softmax warp and KV tile; first tiles always rescale
     assert dec > 0 and 0 < res < dec
     assert poly == 0 and mufu == dec * 32 * 128
+
+
+def test_varlen_more_sequences_than_one_launch(A):
+    """1100 packed sequences (lengths 1 .. 64): more than one launch's work-order tables hold, so
+    the call runs as two launches (1024 + 76 sequences)."""
+    rng = np.random.default_rng(31)
+    lens = [int(x) for x in rng.integers(1, 65, size=1100)]
+    check_full(A, case("varlen1100", 0, 2, 1, 0, 0, 128, True, 32, lens=lens))
