@@ -343,7 +343,7 @@ static attn_status_t decode_paged(const void* q, const void* k_cache, const void
                                   int Hkv, int d, int max_pages_per_seq, int num_pages, float scale, int num_splits,
                                   int kv_format, float k_descale, float v_descale) {
     if (!q || !k_cache || !v_cache || !page_table || !seqlens || !o || !lse) return ATTN_ERR_NULL_PTR;
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq / Hkv > 16 || (d != 64 && d != 128) || page_size <= 0 ||
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128) || page_size <= 0 ||
         max_pages_per_seq <= 0 || num_pages <= 0 || num_splits < 0 || B > 65535 || Hkv > 65535)
         return ATTN_ERR_BAD_SHAPE;
     if (!isfinite(scale)) return ATTN_ERR_BAD_SHAPE;
@@ -371,6 +371,7 @@ static attn_status_t decode_paged(const void* q, const void* k_cache, const void
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.G = Hq / Hkv;
+    p.g_stride = Hq / Hkv;  // the launchers split G > 16 into groups of 16
     p.page_size = page_size;
     p.max_pages = max_pages_per_seq;
     p.num_pages = num_pages;

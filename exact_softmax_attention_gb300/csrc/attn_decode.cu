@@ -111,7 +111,7 @@ __device__ __forceinline__ void merge_and_store(const DecodeParams& p, uint8_t* 
         }
         const float o = ll > 0.0f ? acc / ll * out_scale : 0.0f;
         const float lse = ll > 0.0f ? mm * p.scale + logf(ll) : -INFINITY;
-        const long long bh = (long long)b * p.Hq + kvh * p.G + hh;
+        const long long bh = (long long)b * p.Hq + kvh * p.g_stride + p.g_base + hh;
         if (direct) {
             p.o[bh * D + d] = __float2bfloat16(o);
             if (d == 0) p.lse[bh] = lse;
@@ -141,10 +141,10 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeP
         // No cached keys: the output is 0 and the log-sum-exp is -inf (written by split 0).
         if (split == 0) {
             for (int i = threadIdx.x; i < p.G * D; i += blockDim.x) {
-                const int h = kvh * p.G + i / D;
+                const int h = kvh * p.g_stride + p.g_base + i / D;
                 p.o[((long long)b * p.Hq + h) * D + (i % D)] = __float2bfloat16(0.0f);
             }
-            if (threadIdx.x < p.G) p.lse[(long long)b * p.Hq + kvh * p.G + threadIdx.x] = -INFINITY;
+            if (threadIdx.x < p.G) p.lse[(long long)b * p.Hq + kvh * p.g_stride + p.g_base + threadIdx.x] = -INFINITY;
         }
         return;
     }
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeP
 
     // ---- query fragments: rows = query heads of this kv head (padded to 16), k = d
     const int g0 = lane >> 2;
-    const int h0 = kvh * p.G + g0, h1 = kvh * p.G + g0 + 8;
+    const int h0 = kvh * p.g_stride + p.g_base + g0, h1 = kvh * p.g_stride + p.g_base + g0 + 8;
     const bool v0 = g0 < p.G, v1 = (GN == 16) && (g0 + 8 < p.G);
     const uint32_t* q0p = reinterpret_cast<const uint32_t*>(p.q + ((long long)b * p.Hq + h0) * D);
     const uint32_t* q1p = reinterpret_cast<const uint32_t*>(p.q + ((long long)b * p.Hq + h1) * D);
@@ -409,10 +409,10 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_fp8_kernel(const Dec
     if (len == 0) {
         if (split == 0) {
             for (int i = threadIdx.x; i < p.G * D; i += blockDim.x) {
-                const int h = kvh * p.G + i / D;
+                const int h = kvh * p.g_stride + p.g_base + i / D;
                 p.o[((long long)b * p.Hq + h) * D + (i % D)] = __float2bfloat16(0.0f);
             }
-            if (threadIdx.x < p.G) p.lse[(long long)b * p.Hq + kvh * p.G + threadIdx.x] = -INFINITY;
+            if (threadIdx.x < p.G) p.lse[(long long)b * p.Hq + kvh * p.g_stride + p.g_base + threadIdx.x] = -INFINITY;
         }
         return;
     }
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_fp8_kernel(const Dec
     // ---- query fragments (f16), rows = query heads of this kv head. Permuted d: column
     // 2 qd + e of k-step kk is d = (D/4) qd + 4 kk + e, column 2 qd + 8 + e is that + 2.
     const int g0 = lane >> 2, qd = lane & 3;
-    const int h0 = kvh * p.G + g0, h1 = kvh * p.G + g0 + 8;
+    const int h0 = kvh * p.g_stride + p.g_base + g0, h1 = kvh * p.g_stride + p.g_base + g0 + 8;
     const bool v0 = g0 < p.G, v1 = (GN == 16) && (g0 + 8 < p.G);
     const uint32_t* q0p = reinterpret_cast<const uint32_t*>(p.q + ((long long)b * p.Hq + h0) * D);
     const uint32_t* q1p = reinterpret_cast<const uint32_t*>(p.q + ((long long)b * p.Hq + h1) * D);
@@ -606,14 +606,18 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_fp8_kernel(const Dec
     merge_and_store<D, GN, true>(p, smem, oacc, m0, m1, l0, l1, split, nsplit, kvh, b, p.v_descale);
 }
 
-// One warp per (sequence, query head): LSE = log sum_s exp(lse_s) (max-shifted, warp
-// shuffles over the splits), O = sum_s exp(lse_s - LSE) O_s.
+// One warp per (sequence, query head of this launch): LSE = log sum_s exp(lse_s) (max-shifted,
+// warp shuffles over the splits), O = sum_s exp(lse_s - LSE) O_s.
 template <int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long bh = (long long)blockIdx.x * 4 + warp;
-    if (bh >= (long long)p.B * p.Hq) return;
-    const int b = (int)(bh / p.Hq);
+    // row (b, kv head, g) of this launch's heads -> query row b * Hq + kvh * g_stride + g_base + g
+    const long long row = (long long)blockIdx.x * 4 + warp;
+    const long long per_b = (long long)p.Hkv * p.G;
+    if (row >= (long long)p.B * per_b) return;
+    const int b = (int)(row / per_b);
+    const int rem = (int)(row - b * per_b);
+    const long long bh = (long long)b * p.Hq + (long long)(rem / p.G) * p.g_stride + p.g_base + rem % p.G;
     const long long max_len = (long long)p.max_pages * p.page_size;
     int len = __ldg(p.seqlens + b);
     len = len < 0 ? 0 : (len > max_len ? (int)max_len : len);
@@ -676,7 +680,7 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.max_splits > 1) {
-        const long long rows = (long long)p.B * p.Hq;
+        const long long rows = (long long)p.B * p.Hkv * p.G;
         decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
         e = cudaGetLastError();
     }
@@ -703,7 +707,7 @@ cudaError_t launch_fp8_t(const DecodeParams& p, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.max_splits > 1) {
-        const long long rows = (long long)p.B * p.Hq;
+        const long long rows = (long long)p.B * p.Hkv * p.G;
         decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
         e = cudaGetLastError();
     }
@@ -720,14 +724,30 @@ cudaError_t launch_fp8_fmt(const DecodeParams& p, int d, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_attn_decode_fp8(const DecodeParams& p, int d, int fmt, cudaStream_t stream) {
-    return fmt == 0 ? launch_fp8_fmt<0>(p, d, stream) : launch_fp8_fmt<1>(p, d, stream);
+// The query heads of a kv head are the rows of the kernels' tensor-core products (at most 16):
+// more than 16 run as one launch (split kernel, then combine) per group of 16.
+cudaError_t launch_attn_decode_fp8(const DecodeParams& p_in, int d, int fmt, cudaStream_t stream) {
+    for (int g0 = 0; g0 < p_in.g_stride; g0 += 16) {
+        DecodeParams p = p_in;
+        p.g_base = g0;
+        p.G = p_in.g_stride - g0 < 16 ? p_in.g_stride - g0 : 16;
+        const cudaError_t e = fmt == 0 ? launch_fp8_fmt<0>(p, d, stream) : launch_fp8_fmt<1>(p, d, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
-cudaError_t launch_attn_decode(const DecodeParams& p, int d, cudaStream_t stream) {
+cudaError_t launch_attn_decode(const DecodeParams& p_in, int d, cudaStream_t stream) {
     constexpr int NST = 3;
-    if (d == 128) return p.G <= 8 ? launch_t<128, 8, NST>(p, stream) : launch_t<128, 16, NST>(p, stream);
-    return p.G <= 8 ? launch_t<64, 8, NST>(p, stream) : launch_t<64, 16, NST>(p, stream);
+    for (int g0 = 0; g0 < p_in.g_stride; g0 += 16) {  // groups of at most 16 query heads, as above
+        DecodeParams p = p_in;
+        p.g_base = g0;
+        p.G = p_in.g_stride - g0 < 16 ? p_in.g_stride - g0 : 16;
+        const cudaError_t e = d == 128 ? (p.G <= 8 ? launch_t<128, 8, NST>(p, stream) : launch_t<128, 16, NST>(p, stream))
+                                       : (p.G <= 8 ? launch_t<64, 8, NST>(p, stream) : launch_t<64, 16, NST>(p, stream));
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace attn

@@ -48,7 +48,7 @@ extern "C" attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_
                                                    float* lse, void* stream, int B, int Hq, int Hkv, int d,
                                                    int max_pages_per_seq, int num_pages, float scale, int num_splits) {
     if (!q || !k_cache || !v_cache || !page_table || !seqlens || !o || !lse) return ATTN_ERR_NULL_PTR;
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq / Hkv > 16 || (d != 64 && d != 128) || page_size <= 0 ||
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128) || page_size <= 0 ||
         max_pages_per_seq <= 0 || num_pages <= 0 || num_splits < 0 || B > 65535 || Hkv > 65535)
         return ATTN_ERR_BAD_SHAPE;
     if (!isfinite(scale)) return ATTN_ERR_BAD_SHAPE;
@@ -88,6 +88,7 @@ extern "C" attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.G = Hq / Hkv;
+    p.g_stride = Hq / Hkv;  // the launcher splits G > 16 into groups of 16
     p.page_size = page_size;
     p.max_pages = max_pages_per_seq;
     p.num_pages = num_pages;

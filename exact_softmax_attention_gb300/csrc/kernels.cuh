@@ -64,7 +64,10 @@ struct DecodeParams {
     float* lse;                    // [B, Hq]
     float* ws_o;                   // [B, Hq, max_splits, d] partial outputs
     float* ws_lse;                 // [B, Hq, max_splits] partial LSE
-    int B, Hq, Hkv, G, page_size, max_pages, num_pages;
+    int B, Hq, Hkv, page_size, max_pages, num_pages;
+    // Query heads: one launch handles heads g_base .. g_base + G - 1 (G <= 16) of every kv head;
+    // g_stride = Hq / Hkv is their spacing in memory (query head h reads kv head h / g_stride).
+    int G, g_base, g_stride;
     int chunk;       // tokens per split (multiple of 64)
     int max_splits;  // splits per sequence the workspace holds
     float scale, scale_log2, rescale_thr;

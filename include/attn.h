@@ -143,7 +143,8 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
  *            max_pages_per_seq * page_size. A sequence of length 0 gets o = 0, lse = -inf.
  * page_size  tokens per page, >= 1 (any value)
  * o          device, bf16 [B, Hq, d] (written);  lse device, fp32 [B, Hq] (written)
- * B, Hq, Hkv, d  as for attn_fwd; Hq / Hkv <= 16
+ * B, Hq, Hkv, d  as for attn_fwd (d = 64 or 128); the query heads of a kv head are the rows
+ *            of one tile, so more than 16 per kv head run as one launch per group of 16
  * max_pages_per_seq  columns of page_table (>= 1)
  * num_pages  physical pages in each cache (>= 1); a page index outside [0, num_pages) is
  *            not read: its rows count as zeros and ATTN_ERR_DEVICE_BAD_INDEX is recorded

@@ -71,7 +71,7 @@ def _dec(lib, q=16, kc=16, vc=16, pt=16, sl=16, ps=16, o=16, lse=16, B=1, Hq=8, 
 def test_decode_host_validation(lib):
     import exact_softmax_attention_gb300 as A
     assert _dec(lib, pt=None) == A.ATTN_ERR_NULL_PTR
-    assert _dec(lib, Hq=36, Hkv=2) == A.ATTN_ERR_BAD_SHAPE   # 18 query heads per kv head
+    assert _dec(lib, Hq=36, Hkv=5) == A.ATTN_ERR_BAD_SHAPE   # Hq not a multiple of Hkv
     assert _dec(lib, ps=0) == A.ATTN_ERR_BAD_SHAPE
     assert _dec(lib, npg=0) == A.ATTN_ERR_BAD_SHAPE
     assert _dec(lib, ns=-1) == A.ATTN_ERR_BAD_SHAPE
