@@ -391,7 +391,8 @@ __device__ __forceinline__ void lds64(uint32_t addr, uint32_t* w) {
 }
 
 template <int D, int GN, int NST, int FMT>
-__global__ void __launch_bounds__(kWarps * 32) decode_split_fp8_kernel(const DecodeParams p) {
+// Four CTAs per SM (48 KB of rings each): at most 128 registers per thread.
+__global__ void __launch_bounds__(kWarps * 32, 4) decode_split_fp8_kernel(const DecodeParams p) {
     constexpr int kTile = kGroup * D;   // bytes of one K or V warp-stage tile
     constexpr int kChunks = D / 16;     // 16-byte chunks per cache row
     extern __shared__ __align__(128) uint8_t smem[];
