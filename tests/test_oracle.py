@@ -302,9 +302,9 @@ def _small_decode(seed=123, extra_pages=0, page_size=16, B=5, Hq=8, Hkv=2, d=32)
                         extra_pages=extra_pages)
 
 
-@pytest.mark.parametrize("page_size", [1, 3, 16])
-def test_decode_equals_contiguous_forward(page_size):
-    c = _small_decode(page_size=page_size)
+@pytest.mark.parametrize("page_size,Hq,Hkv", [(1, 8, 2), (3, 8, 2), (16, 8, 2), (16, 40, 1), (7, 48, 2)])
+def test_decode_equals_contiguous_forward(page_size, Hq, Hkv):
+    c = _small_decode(page_size=page_size, Hq=Hq, Hkv=Hkv)
     q, kc, vc, pt, sl = c.generate()
     o, lse = oracle.attn_decode_paged(q, kc, vc, pt, sl, c.page_size, c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.scale)
     for b in range(c.B):
