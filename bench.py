@@ -62,6 +62,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
                     help="library tuning option (attn_set_option) applied before timing; repeatable")
+    ap.add_argument("--legs", default="all",
+                    help="comma-separated legs to run besides the step (decode_fp8, prefill_fp8, prefill_hd, "
+                         "prefill_d256, prefill_tiny, prefill_2k, prefill_2k_causal, prefill_varlen_gqa, rescale), "
+                         "'all' or 'none'")
     return ap.parse_args()
 
 
@@ -317,6 +321,59 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ GPU leg
 
+class Timer:
+    """CUDA-event timing of repeated library calls on one stream, with the device status
+    checked after every timed leg (a watchdog timeout or a bad index fails the run)."""
+
+    def __init__(self, A, stream, barrier):
+        import torch
+        self.torch, self.A, self.stream, self.barrier = torch, A, stream, barrier
+
+    def check(self, what):
+        st = self.A.attn_get_device_status(self.stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"device status after {what}: {self.A.status_string(st)}")
+
+    def per_call_ms(self, fn, calls, warmup, what, flush=None):
+        """Average ms of one call. With ``flush`` (a callable that overwrites more than the L2)
+        each call is timed alone between its own events, with the flush outside them."""
+        torch = self.torch
+        for _ in range(warmup):
+            fn()
+        self.barrier()
+        if flush is None:
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(self.stream)
+            for _ in range(calls):
+                fn()
+            e.record(self.stream)
+            self.barrier()
+            ms = s.elapsed_time(e)
+        else:
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+            for s, e in evs:
+                flush()
+                s.record(self.stream)
+                fn()
+                e.record(self.stream)
+            self.barrier()
+            ms = sum(s.elapsed_time(e) for s, e in evs)
+        self.check(what)
+        return ms / calls
+
+
+def tensor_leg(name, workload, flops, ms, calls, launches, peak, peak_source, kernel, world, extra=None):
+    ach = flops / (ms * 1e-3) / 1e12
+    leg = {"value": world * ach, "unit": "TFLOP/s", "ms_per_call": ms, "calls": calls, "gpu_launches": launches,
+           "workload": workload, "flops_per_call": flops,
+           "roofline": {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                        "traffic": ncu_traffic(kernel) if kernel in KERNEL_SOURCES else None, "kernel": kernel,
+                        "peak_source": peak_source}}
+    if extra:
+        leg.update(extra)
+    return name, leg
+
+
 def run_ours(args):
     import torch
 
@@ -333,7 +390,13 @@ def run_ours(args):
     for opt in args.option:
         name, value = opt.split("=", 1)
         A.attn_set_option(name, float(value))
+    legs_wanted = set(args.legs.split(",")) if args.legs not in ("all", "none") else (
+        set() if args.legs == "none" else None)
 
+    def want(leg):
+        return legs_wanted is None or leg in legs_wanted
+
+    hbm, bf16, src = peaks()
     fc, dc = W.long_causal(), W.decode()
     q, k, v = fc.generate()
     dq, kc, vc, pt, sl = dc.generate()
@@ -353,62 +416,21 @@ def run_ours(args):
     stream.synchronize()
     s_handle = stream.cuda_stream
 
+    def fwd_on(q_, k_, v_, o_, lse_):
+        A.attn_fwd(q_, k_, v_, o_, lse_, fc.B, fc.Hq, fc.Hkv, fc.Nq, fc.Nk, fc.d, fc.scale, fc.causal, None, s_handle)
+
+    def dec_on(q_, kc_, vc_, pt_, sl_, o_, lse_):
+        A.attn_decode_paged(q_, kc_, vc_, pt_, sl_, dc.page_size, o_, lse_, s_handle, dc.B, dc.Hq, dc.Hkv, dc.d,
+                            dc.max_pages, dc.num_pages, dc.scale, 0)
+
     def fwd():
-        A.attn_fwd(Q, K, V, O, LSE, fc.B, fc.Hq, fc.Hkv, fc.Nq, fc.Nk, fc.d, fc.scale, fc.causal, None, s_handle)
+        fwd_on(Q, K, V, O, LSE)
 
     def dec():
-        A.attn_decode_paged(DQ, KC, VC, PT, SL, dc.page_size, DO, DLSE, s_handle, dc.B, dc.Hq, dc.Hkv, dc.d,
-                            dc.max_pages, dc.num_pages, dc.scale, 0)
+        dec_on(DQ, KC, VC, PT, SL, DO, DLSE)
 
     _, max_splits = A.attn_decode_plan(dc.B, dc.Hkv, dc.max_pages, dc.page_size, 0)
     launches_per_step = 1 + (2 if max_splits > 1 else 1)
-
-    # FP8 (e4m3) key/value caches of the same decode workload: a leg of its own, timed after
-    # the step
-    dc8 = W.decode_fp8()
-    _, kc8, vc8, _, _, kds, vds = dc8.generate_fp8()
-    with torch.cuda.stream(stream):
-        KC8, VC8 = torch.from_numpy(kc8).to(dev), torch.from_numpy(vc8).to(dev)
-    stream.synchronize()
-
-    # FP8 (e4m3) Q/K/V of the same long causal prefill: a leg of its own, timed after the step
-    q8, k8, v8, qds, kds8, vds8 = fc.generate_fp8("e4m3")
-    with torch.cuda.stream(stream):
-        Q8, K8, V8 = (torch.from_numpy(a).to(dev) for a in (q8, k8, v8))
-    stream.synchronize()
-
-    def fwd8():
-        A.attn_fwd_fp8(Q8, K8, V8, O, LSE, fc.B, fc.Hq, fc.Hkv, fc.Nq, fc.Nk, fc.d, fc.scale, fc.causal, None,
-                       s_handle, "e4m3", qds, kds8, vds8)
-
-    # head dims (192, 128) on the long causal geometry: a leg of its own, timed after the step
-    hc = W.PrefillCase("long_causal_hd", fc.B, fc.Hq, fc.Hkv, fc.Nq, fc.Nk, 192, 1.0 / math.sqrt(192), True,
-                       fc.seed, fc.q_mult, dv=128)
-    hq, hk, hv = hc.generate()
-    with torch.cuda.stream(stream):
-        HQ, HK, HV = to_dev(hq), to_dev(hk), to_dev(hv)
-        HO = torch.empty((hc.total_q, hc.Hq, 128), dtype=torch.bfloat16, device=dev)
-    stream.synchronize()
-
-    def fwd_hd():
-        A.attn_fwd_hd(HQ, HK, HV, HO, LSE, hc.B, hc.Hq, hc.Hkv, hc.Nq, hc.Nk, 192, 128, hc.scale, True, None, s_handle)
-
-    # head width 256 on the long causal geometry: a leg of its own, timed after the step
-    wc = W.PrefillCase("long_causal_d256", fc.B, fc.Hq, fc.Hkv, fc.Nq, fc.Nk, 256, 1.0 / math.sqrt(256), True,
-                       fc.seed, fc.q_mult)
-    wq, wk, wv = wc.generate()
-    with torch.cuda.stream(stream):
-        WQ, WK, WV = to_dev(wq), to_dev(wk), to_dev(wv)
-        WO = torch.empty((wc.total_q, wc.Hq, 256), dtype=torch.bfloat16, device=dev)
-    stream.synchronize()
-    del wq, wk, wv
-
-    def fwd_w():
-        A.attn_fwd(WQ, WK, WV, WO, LSE, wc.B, wc.Hq, wc.Hkv, wc.Nq, wc.Nk, 256, wc.scale, True, None, s_handle)
-
-    def dec8():
-        A.attn_decode_paged_fp8(DQ, KC8, VC8, PT, SL, dc8.page_size, DO, DLSE, s_handle, dc8.B, dc8.Hq, dc8.Hkv,
-                                dc8.d, dc8.max_pages, dc8.num_pages, dc8.scale, 0, dc8.kv_fmt, kds, vds)
 
     def barrier():
         if world > 1:
@@ -416,13 +438,13 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    timer = Timer(A, stream, barrier)
     for _ in range(args.warmup):
         fwd()
         dec()
-    st = A.attn_get_device_status(s_handle)
-    if st != 0:
-        raise RuntimeError(f"device status after warm-up: {A.status_string(st)}")
+    timer.check("warm-up")
 
+    # ---------------------------------------------------------------- the timed step
     K_ = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_)]
     barrier()
@@ -440,9 +462,7 @@ def run_ours(args):
         end.record(stream)
         barrier()
         t_wall = time.perf_counter() - t_wall0
-    st = A.attn_get_device_status(s_handle)
-    if st != 0:
-        raise RuntimeError(f"device status after timed region: {A.status_string(st)}")
+    timer.check("timed region")
     total_ms = start.elapsed_time(end)
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
     dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
@@ -451,108 +471,171 @@ def run_ours(args):
     fwd_ms = max_over_ranks(fwd_ms, world, dev)
     dec_ms = max_over_ranks(dec_ms, world, dev)
 
-    # FP8 decode leg: warm-up, then the same number of timed calls
-    for _ in range(args.warmup):
-        dec8()
-    barrier()
-    s8, e8 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s8.record(stream)
-    for _ in range(K_):
-        dec8()
-    e8.record(stream)
-    barrier()
-    st = A.attn_get_device_status(s_handle)
-    if st != 0:
-        raise RuntimeError(f"device status after the FP8 decode leg: {A.status_string(st)}")
-    dec8_ms = max_over_ranks(s8.elapsed_time(e8), world, dev)
+    extra = {}
+    mx = lambda x: max_over_ranks(x, world, dev)
 
-    # FP8 forward leg
-    for _ in range(args.warmup):
-        fwd8()
-    barrier()
-    sf8, ef8 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sf8.record(stream)
-    for _ in range(K_):
-        fwd8()
-    ef8.record(stream)
-    barrier()
-    st = A.attn_get_device_status(s_handle)
-    if st != 0:
-        raise RuntimeError(f"device status after the FP8 forward leg: {A.status_string(st)}")
-    fwd8_ms = max_over_ranks(sf8.elapsed_time(ef8), world, dev)
+    # ---------------------------------------------------------------- legs outside `value`
+    if want("decode_fp8"):
+        dc8 = W.decode_fp8()
+        _, kc8, vc8, _, _, kds, vds = dc8.generate_fp8()
+        with torch.cuda.stream(stream):
+            KC8, VC8 = torch.from_numpy(kc8).to(dev), torch.from_numpy(vc8).to(dev)
+        stream.synchronize()
+        del kc8, vc8
 
-    # head dims (192, 128) leg
-    for _ in range(args.warmup):
-        fwd_hd()
-    barrier()
-    sh, eh = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sh.record(stream)
-    for _ in range(K_):
-        fwd_hd()
-    eh.record(stream)
-    barrier()
-    st = A.attn_get_device_status(s_handle)
-    if st != 0:
-        raise RuntimeError(f"device status after the (192, 128) forward leg: {A.status_string(st)}")
-    fwdhd_ms = max_over_ranks(sh.elapsed_time(eh), world, dev)
+        def dec8():
+            A.attn_decode_paged_fp8(DQ, KC8, VC8, PT, SL, dc8.page_size, DO, DLSE, s_handle, dc8.B, dc8.Hq, dc8.Hkv,
+                                    dc8.d, dc8.max_pages, dc8.num_pages, dc8.scale, 0, dc8.kv_fmt, kds, vds)
 
-    # head width 256 leg
-    for _ in range(args.warmup):
-        fwd_w()
-    barrier()
-    sw, ew = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sw.record(stream)
-    for _ in range(K_):
-        fwd_w()
-    ew.record(stream)
-    barrier()
-    st = A.attn_get_device_status(s_handle)
-    if st != 0:
-        raise RuntimeError(f"device status after the d = 256 forward leg: {A.status_string(st)}")
-    fwdw_ms = max_over_ranks(sw.elapsed_time(ew), world, dev)
+        ms = mx(timer.per_call_ms(dec8, K_, args.warmup, "the FP8 decode leg"))
+        ach = dc8.bytes() / (ms * 1e-3) / 1e9
+        extra["decode_fp8"] = {
+            "value": world * ach, "unit": "GB/s", "ms_per_call": ms, "calls": K_,
+            "gpu_launches": K_ * (launches_per_step - 1),
+            "workload": "paged decode as above with e4m3 key/value caches (per-tensor descales)",
+            "bytes_per_call": dc8.bytes(), "speedup_vs_bf16_decode": (dec_ms / K_) / ms,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                         "traffic": ncu_traffic(DEC8_KERNEL), "kernel": DEC8_KERNEL, "peak_source": f"{src} copy"}}
+        del KC8, VC8
 
-    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    if want("prefill_fp8"):
+        q8, k8, v8, qds, kds8, vds8 = fc.generate_fp8("e4m3")
+        with torch.cuda.stream(stream):
+            Q8, K8, V8 = (torch.from_numpy(a).to(dev) for a in (q8, k8, v8))
+        stream.synchronize()
+
+        def fwd8():
+            A.attn_fwd_fp8(Q8, K8, V8, O, LSE, fc.B, fc.Hq, fc.Hkv, fc.Nq, fc.Nk, fc.d, fc.scale, fc.causal, None,
+                           s_handle, "e4m3", qds, kds8, vds8)
+
+        ms = mx(timer.per_call_ms(fwd8, K_, args.warmup, "the FP8 forward leg"))
+        name, leg = tensor_leg("prefill_fp8", "long causal prefill as above with e4m3 Q/K/V (per-tensor descales)",
+                               fc.flops(), ms, K_, K_, bf16 * 4.0 / 3.0,
+                               f"{src} bf16 burst x 4/3 (half the FLOPs in fp8 at 2x, half in f16 at 1x)",
+                               FWD8_KERNEL, world, {"speedup_vs_bf16_prefill": (fwd_ms / K_) / ms})
+        extra[name] = leg
+
+    if want("prefill_hd"):
+        hc = W.PrefillCase("long_causal_hd", fc.B, fc.Hq, fc.Hkv, fc.Nq, fc.Nk, 192, 1.0 / math.sqrt(192), True,
+                           fc.seed, fc.q_mult, dv=128)
+        hq, hk, hv = hc.generate()
+        with torch.cuda.stream(stream):
+            HQ, HK, HV = to_dev(hq), to_dev(hk), to_dev(hv)
+            HO = torch.empty((hc.total_q, hc.Hq, 128), dtype=torch.bfloat16, device=dev)
+        stream.synchronize()
+
+        def fwd_hd():
+            A.attn_fwd_hd(HQ, HK, HV, HO, LSE, hc.B, hc.Hq, hc.Hkv, hc.Nq, hc.Nk, 192, 128, hc.scale, True, None,
+                          s_handle)
+
+        ms = mx(timer.per_call_ms(fwd_hd, K_, args.warmup, "the (192, 128) forward leg"))
+        name, leg = tensor_leg("prefill_hd", "long causal prefill B1 H32 N8192 with head dims (192, 128), bf16",
+                               hc.flops(), ms, K_, K_, bf16, f"{src} bf16 burst", FWDHD_KERNEL, world)
+        extra[name] = leg
+        del HQ, HK, HV, HO
+
+    if want("prefill_d256"):
+        wc = W.PrefillCase("long_causal_d256", fc.B, fc.Hq, fc.Hkv, fc.Nq, fc.Nk, 256, 1.0 / math.sqrt(256), True,
+                           fc.seed, fc.q_mult)
+        wq, wk, wv = wc.generate()
+        with torch.cuda.stream(stream):
+            WQ, WK, WV = to_dev(wq), to_dev(wk), to_dev(wv)
+            WO = torch.empty((wc.total_q, wc.Hq, 256), dtype=torch.bfloat16, device=dev)
+        stream.synchronize()
+        del wq, wk, wv
+
+        def fwd_w():
+            A.attn_fwd(WQ, WK, WV, WO, LSE, wc.B, wc.Hq, wc.Hkv, wc.Nq, wc.Nk, 256, wc.scale, True, None, s_handle)
+
+        ms = mx(timer.per_call_ms(fwd_w, K_, args.warmup, "the d = 256 forward leg"))
+        name, leg = tensor_leg("prefill_d256", "long causal prefill B1 H32 N8192 with head width 256, bf16",
+                               wc.flops(), ms, K_, K_, bf16, f"{src} bf16 burst", FWDW_KERNEL, world)
+        extra[name] = leg
+        del WQ, WK, WV, WO
+
+    # the other prefill configurations: tiny (C1), prefill B2 H16 N2048 non-causal and causal
+    # (C2), packed GQA (C4, with the heaviest-first order across sequences and without it).
+    # C1 and C2 fit in the L2, so each call is timed alone after a write of 512 MB.
+    flush_buf = None
+
+    def flush():
+        with torch.cuda.stream(stream):  # ordered with the calls it separates
+            flush_buf.zero_()
+
+    small = [("prefill_tiny", W.tiny(), True), ("prefill_2k", W.prefill(False), True),
+             ("prefill_2k_causal", W.prefill(True), True), ("prefill_varlen_gqa", W.varlen_gqa(), False)]
+    for name, c, fits_l2 in small:
+        if not want(name):
+            continue
+        if fits_l2 and flush_buf is None:
+            with torch.cuda.stream(stream):
+                flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        cq, ck, cv = c.generate()
+        with torch.cuda.stream(stream):
+            CQ, CK, CV = to_dev(cq), to_dev(ck), to_dev(cv)
+            CO = torch.empty((c.total_q, c.Hq, c.d), dtype=torch.bfloat16, device=dev)
+            CL = torch.empty((c.total_q, c.Hq), dtype=torch.float32, device=dev)
+            CU = None if c.cu_seqlens is None else torch.from_numpy(c.cu_seqlens).to(dev)
+        stream.synchronize()
+        nq, nk = (c.Nq, c.Nk) if CU is None else (c.total_q, c.total_k)
+
+        def call(c=c, CQ=CQ, CK=CK, CV=CV, CO=CO, CL=CL, CU=CU, nq=nq, nk=nk):
+            A.attn_fwd(CQ, CK, CV, CO, CL, c.B, c.Hq, c.Hkv, nq, nk, c.d, c.scale, c.causal, CU, s_handle)
+
+        calls = K_ if not fits_l2 else max(K_, 50)
+        ms = mx(timer.per_call_ms(call, calls, args.warmup, f"the {name} leg", flush if fits_l2 else None))
+        desc = {"prefill_tiny": "tiny B1 H2 N256 d64 non-causal", "prefill_2k": "prefill B2 H16 N2048 d128 non-causal",
+                "prefill_2k_causal": "prefill B2 H16 N2048 d128 causal",
+                "prefill_varlen_gqa": "packed GQA: 8 sequences U[512,4096], Hq32 Hkv8 d128 causal"}[name]
+        kern = "attn_fwd_kernel<64, 0, 0>" if c.d == 64 else FWD_KERNEL
+        lx = {"l2": "each call after a 512 MB write (inputs fit in the L2)" if fits_l2 else "inputs larger than L2"}
+        if name == "prefill_varlen_gqa":
+            A.attn_set_option("packed_order", 0)
+            try:
+                ms_plain = mx(timer.per_call_ms(call, calls, args.warmup, "the plain-order packed leg"))
+            finally:
+                A.attn_set_option("packed_order", 1)
+            lx["plain_order"] = {"value": world * c.flops() / (ms_plain * 1e-3) / 1e12, "unit": "TFLOP/s",
+                                 "ms_per_call": ms_plain,
+                                 "order": "sequences in the given order, each one's blocks heaviest first"}
+            lx["sorted_order_gain"] = ms_plain / ms
+        extra[name] = tensor_leg(name, desc, c.flops(), ms, calls, calls, bf16, f"{src} bf16 burst", kern, world,
+                                 lx)[1]
+        del CQ, CK, CV, CO, CL
+    del flush_buf
+
+    # ---------------------------------------------------------------- rescale rate (untimed)
+    if want("rescale"):
+        rates = {}
+        A.attn_set_option("count", 1)
+        try:
+            A.attn_read_counters()
+            for name, c in (("long_causal", fc), ("prefill_2k_causal", W.prefill(True)),
+                            ("prefill_2k", W.prefill(False))):
+                if c is fc:
+                    fwd()
+                else:
+                    cq, ck, cv = c.generate()
+                    with torch.cuda.stream(stream):
+                        CQ, CK, CV = to_dev(cq), to_dev(ck), to_dev(cv)
+                        CO = torch.empty((c.total_q, c.Hq, c.d), dtype=torch.bfloat16, device=dev)
+                        CL = torch.empty((c.total_q, c.Hq), dtype=torch.float32, device=dev)
+                    A.attn_fwd(CQ, CK, CV, CO, CL, c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d, c.scale, c.causal, None,
+                               s_handle)
+                dec_all, raised, _, _, dec1, ores = A.attn_read_counters()
+                rates[name] = {"warp_steps": dec_all, "steps_after_first": dec1, "o_rescales": ores,
+                               "rescale_rate": ores / max(dec1, 1), "skipped": 1.0 - ores / max(dec1, 1)}
+        finally:
+            A.attn_set_option("count", 0)
+        extra["rescale"] = {"threshold_log2": A.attn_get_option("rescale_threshold"), "per_workload": rates,
+                            "note": "softmax warp steps (32 rows x one key tile) after the first key tile of their "
+                                    "Q tile, and how many of them rescaled O"}
+
+    # ---------------------------------------------------------------- end to end (host buffers)
     e2e = None
     if not args.no_e2e:
-        hq, hk, hv = (torch.from_numpy(a.view(np.int16)).pin_memory() for a in (q, k, v))
-        hdq, hkc, hvc = (torch.from_numpy(a.view(np.int16)).pin_memory() for a in (dq, kc, vc))
-        hpt, hsl = torch.from_numpy(pt).pin_memory(), torch.from_numpy(sl).pin_memory()
-        ho = torch.empty(O.shape, dtype=torch.bfloat16).pin_memory()
-        hlse = torch.empty(LSE.shape, dtype=torch.float32).pin_memory()
-        hdo = torch.empty(DO.shape, dtype=torch.bfloat16).pin_memory()
-        hdlse = torch.empty(DLSE.shape, dtype=torch.float32).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdq, hkc, hvc, hpt, hsl))
-        d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdo, hdlse))
-        n_e2e = max(1, min(K_, 5))
-        with torch.cuda.stream(stream):
-            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_e2e)]
-            barrier()
-            for i in range(n_e2e):
-                evs[i][0].record(stream)
-                Q.view(torch.int16).copy_(hq, non_blocking=True)
-                K.view(torch.int16).copy_(hk, non_blocking=True)
-                V.view(torch.int16).copy_(hv, non_blocking=True)
-                fwd()
-                ho.copy_(O, non_blocking=True)
-                hlse.copy_(LSE, non_blocking=True)
-                evs[i][1].record(stream)
-                DQ.view(torch.int16).copy_(hdq, non_blocking=True)
-                KC.view(torch.int16).copy_(hkc, non_blocking=True)
-                VC.view(torch.int16).copy_(hvc, non_blocking=True)
-                PT.copy_(hpt, non_blocking=True)
-                SL.copy_(hsl, non_blocking=True)
-                dec()
-                hdo.copy_(DO, non_blocking=True)
-                hdlse.copy_(DLSE, non_blocking=True)
-                evs[i][2].record(stream)
-            barrier()
-        e_f = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs), world, dev)
-        e_d = max_over_ranks(sum(e[1].elapsed_time(e[2]) for e in evs), world, dev)
-        e2e = {"value": world * n_e2e * fc.flops() / (e_f * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
-               "decode": {"value": world * n_e2e * dc.bytes() / (e_d * 1e-3) / 1e9, "unit": "GB/s"}}
-        if not np.isfinite(ho.float().numpy()).all():
-            raise RuntimeError("non-finite output in the end-to-end leg")
+        e2e = run_e2e(torch, A, dev, stream, barrier, world, K_, fc, dc, (q, k, v), (dq, kc, vc, pt, sl),
+                      (Q, K, V, O, LSE), (DQ, KC, VC, PT, SL, DO, DLSE), fwd_on, dec_on, mx)
 
     if rank != 0:
         if world > 1:
@@ -560,16 +643,13 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
-    hbm, bf16, src = peaks()
     fwd_avg_s = fwd_ms / K_ * 1e-3
     dec_avg_s = dec_ms / K_ * 1e-3
     f_ach = fc.flops() / fwd_avg_s / 1e12
     d_ach = dc.bytes() / dec_avg_s / 1e9
     value = world * K_ * fc.flops() / (fwd_ms * 1e-3) / 1e12
     dvalue = world * K_ * dc.bytes() / (dec_ms * 1e-3) / 1e9
-    tr_f = ncu_traffic(FWD_KERNEL)
-    tr_d = ncu_traffic(DEC_KERNEL)
-    d8_ach = dc8.bytes() / (dec8_ms / K_ * 1e-3) / 1e9
+    opts = {n: A.attn_get_option(n) for n in ("correction", "unroll_kv", "rescale_threshold", "exp_poly")}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K_, "warmup": args.warmup,
         "ms_per_step": total_ms / K_, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -578,52 +658,19 @@ def run_ours(args):
                                "L~U[1024,32768],page16)",
                    "prefill_flops_per_step": fc.flops(), "decode_bytes_per_step": dc.bytes(),
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
-                   "decode_splits_max": max_splits},
+                   "decode_splits_max": max_splits, "forward_options": opts},
         "roofline": {"bound": "tensor", "achieved": f_ach, "peak": bf16, "unit": "TFLOP/s", "frac": f_ach / bf16,
-                     "traffic": tr_f, "kernel": FWD_KERNEL, "peak_source": f"{src} bf16 burst"},
+                     "traffic": ncu_traffic(FWD_KERNEL), "kernel": FWD_KERNEL, "peak_source": f"{src} bf16 burst"},
         "decode": {"value": dvalue, "unit": "GB/s", "ms_per_step": dec_ms / K_,
                    "roofline": {"bound": "hbm", "achieved": d_ach, "peak": hbm, "unit": "GB/s", "frac": d_ach / hbm,
-                                "traffic": tr_d, "kernel": DEC_KERNEL, "peak_source": f"{src} copy"}},
-        "decode_fp8": {"value": world * K_ * dc8.bytes() / (dec8_ms * 1e-3) / 1e9, "unit": "GB/s",
-                       "ms_per_call": dec8_ms / K_, "calls": K_, "gpu_launches": K_ * (launches_per_step - 1),
-                       "workload": "paged decode as above with e4m3 key/value caches (per-tensor descales)",
-                       "bytes_per_call": dc8.bytes(), "speedup_vs_bf16_decode": (dec_ms / K_) / (dec8_ms / K_),
-                       "roofline": {"bound": "hbm", "achieved": d8_ach, "peak": hbm, "unit": "GB/s",
-                                    "frac": d8_ach / hbm, "traffic": ncu_traffic(DEC8_KERNEL), "kernel": DEC8_KERNEL,
-                                    "peak_source": f"{src} copy"}},
-        "prefill_fp8": {"value": world * K_ * fc.flops() / (fwd8_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                        "ms_per_call": fwd8_ms / K_, "calls": K_, "gpu_launches": K_,
-                        "workload": "long causal prefill as above with e4m3 Q/K/V (per-tensor descales)",
-                        "speedup_vs_bf16_prefill": (fwd_ms / K_) / (fwd8_ms / K_),
-                        "roofline": {"bound": "tensor", "achieved": fc.flops() / (fwd8_ms / K_ * 1e-3) / 1e12,
-                                     "peak": bf16 * 4.0 / 3.0, "unit": "TFLOP/s",
-                                     "frac": fc.flops() / (fwd8_ms / K_ * 1e-3) / 1e12 / (bf16 * 4.0 / 3.0),
-                                     "traffic": ncu_traffic(FWD8_KERNEL), "kernel": FWD8_KERNEL,
-                                     "peak_source": f"{src} bf16 burst x 4/3 (half the FLOPs in fp8 at 2x, half in "
-                                                    "f16 at 1x)"}},
-        "prefill_hd": {"value": world * K_ * hc.flops() / (fwdhd_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                       "ms_per_call": fwdhd_ms / K_, "calls": K_, "gpu_launches": K_,
-                       "workload": "long causal prefill B1 H32 N8192 with head dims (192, 128), bf16",
-                       "flops_per_call": hc.flops(),
-                       "roofline": {"bound": "tensor", "achieved": hc.flops() / (fwdhd_ms / K_ * 1e-3) / 1e12,
-                                    "peak": bf16, "unit": "TFLOP/s",
-                                    "frac": hc.flops() / (fwdhd_ms / K_ * 1e-3) / 1e12 / bf16,
-                                    "traffic": ncu_traffic(FWDHD_KERNEL), "kernel": FWDHD_KERNEL,
-                                    "peak_source": f"{src} bf16 burst"}},
-        "prefill_d256": {"value": world * K_ * wc.flops() / (fwdw_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                         "ms_per_call": fwdw_ms / K_, "calls": K_, "gpu_launches": K_,
-                         "workload": "long causal prefill B1 H32 N8192 with head width 256, bf16",
-                         "flops_per_call": wc.flops(),
-                         "roofline": {"bound": "tensor", "achieved": wc.flops() / (fwdw_ms / K_ * 1e-3) / 1e12,
-                                      "peak": bf16, "unit": "TFLOP/s",
-                                      "frac": wc.flops() / (fwdw_ms / K_ * 1e-3) / 1e12 / bf16,
-                                      "traffic": ncu_traffic(FWDW_KERNEL), "kernel": FWDW_KERNEL,
-                                      "peak_source": f"{src} bf16 burst"}},
+                                "traffic": ncu_traffic(DEC_KERNEL), "kernel": DEC_KERNEL,
+                                "peak_source": f"{src} copy"}},
         "prefill_ms_per_step": fwd_ms / K_,
         "gpu_launches": K_ * launches_per_step,
         "clocks": clk.summary(),
         "wall_s_timed": t_wall,
     }
+    line.update(extra)
     if e2e is not None:
         line["e2e"] = e2e
     if world == 1 and not args.no_cpu_baseline:
@@ -634,6 +681,96 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_e2e(torch, A, dev, stream, barrier, world, steps, fc, dc, fin, din, fdev, ddev, fwd_on, dec_on, mx):
+    """Both legs end to end from pinned host buffers: every step copies its inputs to the
+    device, runs the call and copies the outputs back, inside the timed region. Steps are
+    pipelined over two device buffer sets and three streams (host-to-device copies, compute,
+    device-to-host copies), so step i+1's inputs travel while step i computes and step i-1's
+    outputs return, as a serving loop would overlap them."""
+    n = max(3, min(steps, 6))
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def pin(a):
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        return t.pin_memory()
+
+    def leg(host_in, dev_sets, host_out_shapes, call):
+        h_in = [pin(a) for a in host_in]
+        h_out = [[torch.empty(sh, dtype=dt).pin_memory() for sh, dt in host_out_shapes] for _ in range(2)]
+        t_in, t_comp, t_out = [], [], []
+        barrier()
+        start, end = ev(), ev()
+        start.record(stream)
+        h2d_s.wait_event(start)
+        for i in range(n):
+            b = dev_sets[i % 2]
+            if i >= 2:
+                h2d_s.wait_event(t_comp[i - 2][1])  # the set's inputs were last read by step i-2
+            e0, e1 = ev(), ev()
+            e0.record(h2d_s)
+            with torch.cuda.stream(h2d_s):
+                for dst, src in zip(b["in"], h_in):
+                    (dst.view(torch.int16) if dst.dtype == torch.bfloat16 else dst).copy_(src, non_blocking=True)
+            e1.record(h2d_s)
+            t_in.append((e0, e1))
+            stream.wait_event(e1)
+            if i >= 2:
+                stream.wait_event(t_out[i - 2][1])  # its outputs of step i-2 have left the device
+            c0, c1 = ev(), ev()
+            c0.record(stream)
+            call(b)
+            c1.record(stream)
+            t_comp.append((c0, c1))
+            d2h_s.wait_event(c1)
+            o0, o1 = ev(), ev()
+            o0.record(d2h_s)
+            with torch.cuda.stream(d2h_s):
+                for dst, src in zip(h_out[i % 2], b["out"]):
+                    dst.copy_(src, non_blocking=True)
+            o1.record(d2h_s)
+            t_out.append((o0, o1))
+        stream.wait_event(t_out[-1][1])
+        end.record(stream)
+        barrier()
+        st = A.attn_get_device_status(stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"device status after the end-to-end leg: {A.status_string(st)}")
+        for o in h_out[(n - 1) % 2]:
+            if o.dtype.is_floating_point and not torch.isfinite(o.float()).all():
+                raise RuntimeError("non-finite output in the end-to-end leg")
+        total = mx(start.elapsed_time(end))
+        in_ms = sum(a.elapsed_time(b) for a, b in t_in) / n
+        out_ms = sum(a.elapsed_time(b) for a, b in t_out) / n
+        bi = sum(t.numel() * t.element_size() for t in h_in)
+        bo = sum(t.numel() * t.element_size() for t in h_out[0])
+        return total, bi, bo, in_ms, out_ms
+
+    Q, K, V, O, LSE = fdev
+    sets_f = [{"in": [Q, K, V], "out": [O, LSE]},
+              {"in": [torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)],
+               "out": [torch.empty_like(O), torch.empty_like(LSE)]}]
+    tf, bif, bof, inf_ms, outf_ms = leg(fin, sets_f, [(O.shape, torch.bfloat16), (LSE.shape, torch.float32)],
+                                        lambda b: fwd_on(*b["in"], *b["out"]))
+    del sets_f
+    DQ, KC, VC, PT, SL, DO, DLSE = ddev
+    sets_d = [{"in": [DQ, KC, VC, PT, SL], "out": [DO, DLSE]},
+              {"in": [torch.empty_like(x) for x in (DQ, KC, VC, PT, SL)],
+               "out": [torch.empty_like(DO), torch.empty_like(DLSE)]}]
+    td, bid, bod, ind_ms, outd_ms = leg(din, sets_d, [(DO.shape, torch.bfloat16), (DLSE.shape, torch.float32)],
+                                        lambda b: dec_on(*b["in"], *b["out"]))
+    del sets_d
+    return {"value": world * n * fc.flops() / (tf * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": bif + bid, "d2h_bytes_per_step": bof + bod, "steps": n,
+            "pipelined": "2 device buffer sets; H2D, compute and D2H on three streams",
+            "prefill": {"ms_per_step": tf / n, "h2d_gbs": bif / (inf_ms * 1e-3) / 1e9,
+                        "d2h_gbs": bof / (outf_ms * 1e-3) / 1e9, "h2d_bytes": bif, "d2h_bytes": bof},
+            "decode": {"value": world * n * dc.bytes() / (td * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": td / n,
+                       "h2d_gbs": bid / (ind_ms * 1e-3) / 1e9, "d2h_gbs": bod / (outd_ms * 1e-3) / 1e9,
+                       "h2d_bytes": bid, "d2h_bytes": bod}}
 
 
 def main():

@@ -208,8 +208,8 @@ def attn_get_option(name: str) -> float:
 
 
 def attn_read_counters():
-    out = (ctypes.c_ulonglong * 4)()
-    _check(lib.attn_read_counters(out, 4), "attn_read_counters", True)
+    out = (ctypes.c_ulonglong * 6)()
+    _check(lib.attn_read_counters(out, 6), "attn_read_counters", True)
     return list(out)
 
 

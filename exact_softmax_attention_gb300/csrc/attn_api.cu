@@ -29,6 +29,9 @@ struct Options {
     int sec_heads = 0;
     int count = 0;
     double watchdog_ms = 4000.0;
+    int packed_order = 1;
+    int correction = 1;
+    int unroll_kv = 1;
 };
 
 std::mutex g_mu;
@@ -153,6 +156,15 @@ attn_status_t attn_set_option(const char* name, double value) {
     } else if (!strcmp(name, "watchdog_ms")) {
         if (value < 1 || value > 600000) return ATTN_ERR_BAD_ARG;
         g_opt.watchdog_ms = value;
+    } else if (!strcmp(name, "packed_order")) {
+        if (value != 0 && value != 1) return ATTN_ERR_BAD_ARG;
+        g_opt.packed_order = (int)value;
+    } else if (!strcmp(name, "correction")) {
+        if (value != 0 && value != 1) return ATTN_ERR_BAD_ARG;
+        g_opt.correction = (int)value;
+    } else if (!strcmp(name, "unroll_kv")) {
+        if (value != 0 && value != 1) return ATTN_ERR_BAD_ARG;
+        g_opt.unroll_kv = (int)value;
     } else {
         return ATTN_ERR_BAD_ARG;
     }
@@ -168,6 +180,9 @@ attn_status_t attn_get_option(const char* name, double* value) {
     else if (!strcmp(name, "sec_heads")) *value = g_opt.sec_heads;
     else if (!strcmp(name, "count")) *value = g_opt.count;
     else if (!strcmp(name, "watchdog_ms")) *value = g_opt.watchdog_ms;
+    else if (!strcmp(name, "packed_order")) *value = g_opt.packed_order;
+    else if (!strcmp(name, "correction")) *value = g_opt.correction;
+    else if (!strcmp(name, "unroll_kv")) *value = g_opt.unroll_kv;
     else return ATTN_ERR_BAD_ARG;
     return ATTN_OK;
 }
@@ -224,6 +239,9 @@ static attn_status_t fwd(const void* q, const void* k, const void* v, void* o, f
     p.status = ds->status;
     p.counters = opt.count ? ds->counters : nullptr;
     p.watchdog_ns = (unsigned long long)(opt.watchdog_ms * 1e6);
+    p.packed_plain = opt.packed_order == 0;
+    p.corr_warp = opt.correction;
+    p.unroll_kv = opt.unroll_kv;
     int grid = ds->num_sms;
     if (!cu_seqlens) {
         const long long nblk = cdiv(Nq, 256);

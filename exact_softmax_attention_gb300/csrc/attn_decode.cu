@@ -667,15 +667,9 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
     constexpr int ring = kWarps * NST * 2 * DecLayout<D>::kTileBytes;
     constexpr int merge = (kWarps * GN * D + 2 * kWarps * GN) * 4;
     constexpr int bytes = ring > merge ? ring : merge;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<bool> attr_set[kMaxAttrDevices];
+    cudaError_t e = ensure_smem_attr(decode_split_kernel<D, GN, NST>, bytes, attr_set);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(decode_split_kernel<D, GN, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
     const dim3 grid((unsigned)(p.max_splits * p.Hkv), p.B);  // kv heads of one split side by side
     decode_split_kernel<D, GN, NST><<<grid, kWarps * 32, bytes, stream>>>(p);
     e = cudaGetLastError();
@@ -693,16 +687,9 @@ cudaError_t launch_fp8_t(const DecodeParams& p, cudaStream_t stream) {
     constexpr int ring = kWarps * NST * 2 * kGroup * D;
     constexpr int merge = (kWarps * GN * D + 2 * kWarps * GN) * 4;
     constexpr int bytes = ring > merge ? ring : merge;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<bool> attr_set[kMaxAttrDevices];
+    cudaError_t e = ensure_smem_attr(decode_split_fp8_kernel<D, GN, NST, FMT>, bytes, attr_set);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(decode_split_fp8_kernel<D, GN, NST, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 bytes);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
     const dim3 grid((unsigned)(p.max_splits * p.Hkv), p.B);  // kv heads of one split side by side
     decode_split_fp8_kernel<D, GN, NST, FMT><<<grid, kWarps * 32, bytes, stream>>>(p);
     e = cudaGetLastError();

@@ -83,9 +83,12 @@ struct Layout {
     // 8-bit inputs: [kEntries] the entry's 8-bit V tile has landed / has been widened. Only
     // entries that carry V advance them.
     static constexpr int bV8Full = bSFull + 16, bVConv = bV8Full + (F8 ? kEntries : 0);
-    static constexpr int kNumBars = bVConv + (F8 ? kEntries : 0);
+    // correction role: [4 s + quarter] the softmax warp's rescale factors for a step are
+    // published; [s] all four quarters of O_s are corrected for that step
+    static constexpr int bAlpha = bVConv + (F8 ? kEntries : 0), bCorr = bAlpha + 8;
+    static constexpr int kNumBars = bCorr + 2;
     static constexpr int kStatsOff = kBarOff + ((kNumBars * 8 + 15) / 16) * 16;
-    static constexpr int kMiscOff = kStatsOff + 2 * 2 * BM * 4;   // m[2][128], l[2][128]
+    static constexpr int kMiscOff = kStatsOff + 3 * 2 * BM * 4;   // m[2][128], l[2][128], alpha[2][128]
     // misc: tmem base, abort flag, packed-order levels, packed work tiles
     // packed-sequence work order (built once per CTA): pre, lvl, perm, nbs
     static constexpr int kPreOff = kMiscOff + 16;
@@ -356,7 +359,7 @@ __device__ void build_packed_order(const FwdParams& p, int* pre, int* lvl, int* 
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) maxnb = max(maxnb, __shfl_xor_sync(0xffffffffu, maxnb, o));
-    const bool sorted = maxnb <= max_levels;
+    const bool sorted = maxnb <= max_levels && !p.packed_plain;
     if (sorted) {
         for (int v = lane; v <= maxnb + 1; v += 32) lvl[v] = 0;
         __syncwarp();
@@ -464,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
     float* st_m = reinterpret_cast<float*>(smem + L::kStatsOff);  // [2][128]
     float* st_l = st_m + 2 * BM;                                    // [2][128]
+    float* st_a = st_l + 2 * BM;                                    // [2][128] rescale factor of the last step
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
@@ -491,6 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[L::bOFull + s], 1);
             mbar_init(&bars[L::bOEmpty + s], 4);
             mbar_init(&bars[L::bStats + s], 4);
+            mbar_init(&bars[L::bCorr + s], 4);  // the four correction warps
+            for (int q = 0; q < 4; ++q) mbar_init(&bars[L::bAlpha + 4 * s + q], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[L::bDrain + s], 1);
@@ -620,6 +626,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ring entry n is released once both have committed their reads of it (count 2).
         // Within a warp, lane 0 issues every tcgen05 instruction while the whole warp keeps the
         // descriptors and slots warp-uniform.
+        // unroll-KV at work-tile boundaries ("Low-precision FA4", section 2.1.2): the last
+        // burst of a work tile holds only PV(last), and the first of the next only S(0), so
+        // the tensor pipe would idle while the other tile's softmax finishes. With p.unroll_kv
+        // the two are one burst: PV_s(last) of this tile, then S_s(0) = Q'_s K'_0^T of the next
+        // (from the next ring entry; it overwrites P_s(last) only after the PV has read it).
         const int s = warp - 1;
         const uint32_t leader = lane == 0;
         constexpr uint32_t idS = F8 ? idesc_f8_f32(BM, BN, F8 - 1) : idesc_bf16_f32(BM, BN, 0);
@@ -628,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t colS = s ? kColS1 : kColS0;
         const uint32_t colO = s ? kColO1 : kColO0;
         uint32_t stage = 0, phase = 0;
-        uint32_t qf = 0, pf = 0, oe = 0, burst = 0;
+        uint32_t qf = 0, pf = 0, oe = 0, cf = 0, burst = 0;
         uint32_t vcv = 0;  // 8-bit inputs: phase bit per ring slot of the V-widened barrier
         const uint32_t q_base = smem_u32(smem + L::kQOff) + s * L::kQBytes;
         const uint32_t kv_base = smem_u32(smem + L::kKVOff);
@@ -636,20 +647,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dk0 = smem_desc_sw128(kv_base, 16, 1024);
         const uint64_t dv0 = smem_desc_sw128(kv_base, L::kChunkBytesKV, 1024);
         bool ok = true, any = false;
-        for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
-            const int w = snake_index(r);
-            if (w >= total) continue;
-            Tile t;
-            get_tile<BN>(p, po, w, t);
+        // The next work tile (from round r on) with at least one key tile; advances r past it.
+        auto next_tile = [&](int& r, Tile& t) -> bool {
+            for (; r * (int)gridDim.x < total; ++r) {
+                const int w = snake_index(r);
+                if (w >= total) continue;
+                get_tile<BN>(p, po, w, t);
+                if (max(t.n[0], t.n[1]) > 0) {
+                    ++r;
+                    return true;
+                }
+            }
+            return false;
+        };
+        // S = Q K^T of this warp's Q tile with the K tile in ring slot `slot`
+        auto issue_s = [&](uint32_t slot) {
+            // K steps of 32 bytes (16 bf16 or 32 8-bit elements), 4 per 128-byte chunk
+            const uint64_t kd = dk0 + (uint64_t)((slot * L::kEntryBytes) >> 4);
+#pragma unroll
+            for (int k = 0; k < D * L::kElem / 32; ++k) {
+                const uint64_t oq = (uint64_t)(((k >> 2) * L::kChunkBytesQ + (k & 3) * 32) >> 4);
+                const uint64_t ok_ = (uint64_t)(((k >> 2) * L::kChunkBytesKV + (k & 3) * 32) >> 4);
+                if (F8)
+                    tc_mma_ss_f8_by(leader, tmem + colS, dq + oq, kd + ok_, idS, k > 0 ? 1u : 0u);
+                else
+                    tc_mma_ss_by(leader, tmem + colS, dq + oq, kd + ok_, idS, k > 0 ? 1u : 0u);
+            }
+        };
+        int r = 0;
+        Tile t;
+        bool have = next_tile(r, t);
+        int n_first = 0;  // 1 when the previous burst already issued this tile's S(0)
+        while (have && ok) {
             const int nmax = max(t.n[0], t.n[1]);
             const int ns = s ? t.n[1] : t.n[0];
-            if (nmax == 0) continue;
-            if (ns > 0) {
+            if (n_first == 0 && ns > 0) {
                 if (!(ok = warp_wait(&bars[L::bQFull + s], qf, abort_flag, wd))) break;
                 qf ^= 1u;
                 any = true;
             }
-            for (int n = 0; n <= nmax && ok; ++n) {
+            Tile nt;
+            int r_next = r;
+            bool merged = false;
+            for (int n = n_first; n <= nmax && ok; ++n) {
                 const bool do_pv = n >= 1 && n - 1 < ns, do_s = n < ns;
                 const uint32_t e_slot = stage, e_par = phase;
                 if (++stage == (uint32_t)L::kEntries) { stage = 0; phase ^= 1u; }
@@ -660,11 +700,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (n - 1 == 0) {
                         if (!(ok = warp_wait(&bars[L::bOEmpty + s], oe ^ 1u, abort_flag, wd))) break;
                         oe ^= 1u;
+                    } else if (p.corr_warp) {  // O_s rescaled (or left as is) for step n-1
+                        if (!(ok = warp_wait(&bars[L::bCorr + s], cf, abort_flag, wd))) break;
+                        cf ^= 1u;
                     }
                 }
                 if (F8 && n >= 1) {  // every entry that carries V: wait until it has been widened
                     if (!(ok = warp_wait(&bars[L::bVConv + e_slot], (vcv >> e_slot) & 1u, abort_flag, wd))) break;
                     vcv ^= 1u << e_slot;
+                }
+                // unroll-KV: the next work tile's first entry and Q tile join the last burst
+                bool mg = false;
+                int nns = 0;
+                uint32_t m_slot = 0;
+                if (n == nmax && p.unroll_kv && next_tile(r_next, nt)) {
+                    mg = true;
+                    nns = s ? nt.n[1] : nt.n[0];
+                    m_slot = stage;
+                    const uint32_t m_par = phase;
+                    if (++stage == (uint32_t)L::kEntries) { stage = 0; phase ^= 1u; }
+                    if (!(ok = warp_wait(&bars[L::bEFull + m_slot], m_par, abort_flag, wd))) break;
+                    if (nns > 0) {
+                        if (!(ok = warp_wait(&bars[L::bQFull + s], qf, abort_flag, wd))) break;
+                        qf ^= 1u;
+                        any = true;
+                    }
                 }
                 // token: burst 0 of step n follows burst 1 of step n-1; burst 1 follows burst 0
                 if (s == 0) {
@@ -689,27 +749,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = kPA; k < BN / 16; ++k)  // P stage 2
                         tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO, 1u);
                 }
-                if (do_s) {
-                    // K steps of 32 bytes (16 bf16 or 32 8-bit elements), 4 per 128-byte chunk
-                    const uint64_t kd = dk0 + (uint64_t)(ent_off >> 4);
-#pragma unroll
-                    for (int k = 0; k < D * L::kElem / 32; ++k) {
-                        const uint64_t oq = (uint64_t)(((k >> 2) * L::kChunkBytesQ + (k & 3) * 32) >> 4);
-                        const uint64_t ok_ = (uint64_t)(((k >> 2) * L::kChunkBytesKV + (k & 3) * 32) >> 4);
-                        if (F8)
-                            tc_mma_ss_f8_by(leader, tmem + colS, dq + oq, kd + ok_, idS, k > 0 ? 1u : 0u);
-                        else
-                            tc_mma_ss_by(leader, tmem + colS, dq + oq, kd + ok_, idS, k > 0 ? 1u : 0u);
-                    }
-                }
+                if (do_s) issue_s(e_slot);
                 __syncwarp();
-                if (leader) mbar_arrive(&bars[L::bIssued + s]);
-                if (do_s) tc_commit_by(leader, &bars[L::bSFull + s]);
-                if (do_pv && n - 1 == ns - 1) tc_commit_by(leader, &bars[L::bOFull + s]);
-                if (do_s && n == ns - 1) tc_commit_by(leader, &bars[L::bQEmpty + s]);
-                tc_commit_by(leader, &bars[L::bEEmpty + e_slot]);
+                if (mg) {
+                    // this tile's completions first, so that its epilogue starts without waiting
+                    // for the next tile's S(0)
+                    if (do_pv && n - 1 == ns - 1) tc_commit_by(leader, &bars[L::bOFull + s]);
+                    tc_commit_by(leader, &bars[L::bEEmpty + e_slot]);
+                    if (nns > 0) issue_s(m_slot);
+                    __syncwarp();
+                    if (leader) mbar_arrive(&bars[L::bIssued + s]);
+                    if (nns > 0) tc_commit_by(leader, &bars[L::bSFull + s]);
+                    if (nns == 1) tc_commit_by(leader, &bars[L::bQEmpty + s]);
+                    tc_commit_by(leader, &bars[L::bEEmpty + m_slot]);
+                } else {
+                    if (leader) mbar_arrive(&bars[L::bIssued + s]);
+                    if (do_s) tc_commit_by(leader, &bars[L::bSFull + s]);
+                    if (do_pv && n - 1 == ns - 1) tc_commit_by(leader, &bars[L::bOFull + s]);
+                    if (do_s && n == ns - 1) tc_commit_by(leader, &bars[L::bQEmpty + s]);
+                    tc_commit_by(leader, &bars[L::bEEmpty + e_slot]);
+                }
                 ATTN_TL(s ? 4 : 1, 200 + s, n, clock64(), 0);
                 ++burst;
+                merged = mg;
+            }
+            if (!ok) break;
+            if (merged) {
+                t = nt;
+                r = r_next;
+                n_first = 1;
+            } else {
+                have = next_tile(r, t);
+                n_first = 0;
             }
         }
         if (any) {
@@ -731,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + (s ? kColO1 : kColO0);
         const float sl2 = p.scale_log2;
         uint32_t sf = 0, oe = 0;
-        unsigned long long c_dec = 0, c_res = 0;
+        uint32_t c_dec = 0, c_res = 0, c_dec1 = 0, c_ores = 0;  // per warp: far below 2^32
         bool ok = true;
         for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
             const int w = snake_index(r);
@@ -779,18 +850,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float m_cand = fmaxf(m, mt);
                 const bool need = (m_cand - m) * sl2 > p.rescale_thr;  // NaN (both -inf) is false
                 const bool warp_need = __any_sync(0xffffffffu, need);
+                float alpha = 1.0f;  // rows of a warp that keeps its maxima keep O as it is
                 if (warp_need) {
-                    const float alpha = (m == -INFINITY) ? 0.0f : ex2_mufu((m - m_cand) * sl2);
+                    alpha = (m == -INFINITY) ? 0.0f : ex2_mufu((m - m_cand) * sl2);
                     if (n > 0) {
+                        ++c_ores;
+                        if (!p.corr_warp) {
 #pragma unroll 1
-                        for (int c = 0; c < DV; c += 16) {
-                            uint32_t o[16];
-                            tmem_ld16(tO + c, o);
-                            tc_wait_ld();
-                            reg_fence(o);
+                            for (int c = 0; c < DV; c += 16) {
+                                uint32_t o[16];
+                                tmem_ld16(tO + c, o);
+                                tc_wait_ld();
+                                reg_fence(o);
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                            tmem_st16(tO + c, o);
+                                for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                                tmem_st16(tO + c, o);
+                            }
                         }
                     }
                     l *= alpha;
@@ -798,6 +873,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++c_res;
                 }
                 ++c_dec;
+                if (n > 0) {
+                    ++c_dec1;
+                    if (p.corr_warp) {
+                        // hand the rescale of O_s to the correction warp of this quarter (it runs
+                        // while the exponentials below are computed); alpha = 1 means no change
+                        st_a[s * BM + row] = alpha;
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars[L::bAlpha + 4 * s + quarter]);
+                    }
+                }
                 const float neg = (m == -INFINITY) ? 0.0f : -m * sl2;
                 // exponent arguments two at a time (packed FMA), exponentials, packed row sums;
                 // P goes out in two stages (keys 0-95, then 96-127)
@@ -846,15 +931,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&bars[L::bStats + s]);
         }
         if (p.counters && lane == 0) {
-            atomicAdd(p.counters + 0, c_dec);
-            atomicAdd(p.counters + 1, c_res);
+            atomicAdd(p.counters + 0, (unsigned long long)c_dec);
+            atomicAdd(p.counters + 1, (unsigned long long)c_res);
             const unsigned long long ex = c_dec * 32ull * BN;
             const unsigned long long poly = POLY_EVERY > 0 ? ex / POLY_EVERY : 0ull;
             atomicAdd(p.counters + 2, poly);
             atomicAdd(p.counters + 3, ex - poly);
+            atomicAdd(p.counters + 4, (unsigned long long)c_dec1);
+            atomicAdd(p.counters + 5, (unsigned long long)c_ores);
         }
     } else {
-        // ------------------------------------------------------------------ epilogue
+        // ------------------------------------------------------------------ correction + epilogue
+        // Warp 12 + q serves TMEM lane quarter q of both Q tiles. Per KV step it rescales the
+        // quarter's rows of O_s by the factors the softmax warp published, when any of them
+        // changed its maximum ("FlashAttention4 精读" section 3.1, correction warpgroup;
+        // "FlashAttention-4: Blackwell algorithm-pipeline co-design", conditional softmax
+        // rescaling), and signals the MMA warp, which issues the next O += P V only after
+        // that; with 8-bit inputs it also widens V tiles; after the last step it writes O / l
+        // and the LSE.
         if constexpr (F8 != 0)
             asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");  // also widens the 8-bit V tiles
         else
@@ -863,29 +957,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         uint32_t of[2] = {0, 0}, sp[2] = {0, 0};
+        uint32_t ap = 0;               // bit s: parity of the next phase of this quarter's alpha barrier of tile s
         uint32_t stage = 0, v8ph = 0;  // 8-bit inputs: ring slot and per-slot phase bits of bV8Full
         bool ok = true;
+        // O_s of this quarter's rows times the factors of the step just decided (all 1: nothing to do)
+        auto correct = [&](int s) -> bool {
+            if (!warp_wait(&bars[L::bAlpha + 4 * s + quarter], (ap >> s) & 1u, abort_flag, wd)) return false;
+            ap ^= 1u << s;
+            const float a = st_a[s * BM + row];
+            if (__any_sync(0xffffffffu, a != 1.0f)) {
+                tc_fence_after();
+                const uint32_t tO = tmem + lane_off + (s ? kColO1 : kColO0);
+#pragma unroll 1
+                for (int c = 0; c < DV; c += 16) {
+                    uint32_t o[16];
+                    tmem_ld16(tO + c, o);
+                    tc_wait_ld();
+                    reg_fence(o);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+                    tmem_st16(tO + c, o);
+                }
+                tc_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[L::bCorr + s]);
+            return true;
+        };
         for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
             const int w = snake_index(r);
             if (w >= total) continue;
             Tile t;
             get_tile<BN>(p, po, w, t);
-            if constexpr (F8 != 0) {
-                // Widen this tile's 8-bit V tiles first (rows 32*quarter .. +31 of each), in ring
-                // order. The MMA warps wait for them (bVConv) before each P V product and only
-                // then release the entry, so the 8-bit tile is never overwritten while read here.
-                const int nmax = max(t.n[0], t.n[1]);
-                for (int e = 0; e <= nmax && nmax > 0 && ok; ++e) {
-                    const uint32_t e_slot = stage;
-                    if (++stage == (uint32_t)L::kEntries) stage = 0;
-                    if (e == 0) continue;
-                    if (!(ok = warp_wait(&bars[L::bV8Full + e_slot], (v8ph >> e_slot) & 1u, abort_flag, wd))) break;
-                    v8ph ^= 1u << e_slot;
-                    const uint32_t ent = smem_u32(smem + L::kKVOff) + e_slot * L::kEntryBytes;
-                    widen_v_rows<D, F8>(ent + L::kV8Off, ent + L::kVOff, quarter * 32 + lane);
-                    fence_proxy_async_smem();  // make the generic-proxy stores visible to the MMA
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars[L::bVConv + e_slot]);
+            const int nmax = max(t.n[0], t.n[1]);
+            if (nmax > 0) {
+                // Per step e: the correction of tile 0, the widening of the 8-bit V tile of ring
+                // entry e + 1 (rows 32*quarter .. +31, in ring order), the correction of tile 1,
+                // in the order the MMA warps need them. The MMA warps wait for the widening
+                // (bVConv) before each P V product and only then release the entry, so the 8-bit
+                // tile is never overwritten while read here.
+                if constexpr (F8 != 0) {
+                    if (++stage == (uint32_t)L::kEntries) stage = 0;  // entry 0 carries no V
+                }
+                for (int e = 0; e < nmax && ok; ++e) {
+                    if (p.corr_warp && e >= 1 && e < t.n[0] && !(ok = correct(0))) break;
+                    if constexpr (F8 != 0) {
+                        const uint32_t e_slot = stage;
+                        if (++stage == (uint32_t)L::kEntries) stage = 0;
+                        if (!(ok = warp_wait(&bars[L::bV8Full + e_slot], (v8ph >> e_slot) & 1u, abort_flag, wd))) break;
+                        v8ph ^= 1u << e_slot;
+                        const uint32_t ent = smem_u32(smem + L::kKVOff) + e_slot * L::kEntryBytes;
+                        widen_v_rows<D, F8>(ent + L::kV8Off, ent + L::kVOff, quarter * 32 + lane);
+                        fence_proxy_async_smem();  // make the generic-proxy stores visible to the MMA
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars[L::bVConv + e_slot]);
+                    }
+                    if (p.corr_warp && e >= 1 && e < t.n[1] && !(ok = correct(1))) break;
                 }
                 if (!ok) break;
             }
@@ -952,16 +1080,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int POLY, int F8, int DV = D, int BNT = BN>
 cudaError_t launch_t(const FwdTmaps& tm, const FwdParams& p, int grid, cudaStream_t stream) {
     using L = Layout<D, F8, DV, BNT>;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<bool> attr_set[kMaxAttrDevices];
+    const cudaError_t e = ensure_smem_attr(attn_fwd_kernel<D, POLY, F8, DV, BNT>, L::kAlloc, attr_set);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(attn_fwd_kernel<D, POLY, F8, DV, BNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 L::kAlloc);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
     attn_fwd_kernel<D, POLY, F8, DV, BNT><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.k, tm.v, p);
     return cudaGetLastError();
 }
@@ -1316,7 +1437,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         const uint32_t tO = tmem + lane_off + kWideColO;
         const float sl2 = p.scale_log2;
         uint32_t sf = 0, of = 0, pv_done = 0;  // sf bit b: S buffer b parity; pv_done: O += P V steps before this tile
-        unsigned long long c_dec = 0, c_res = 0;
+        unsigned long long c_dec = 0, c_res = 0, c_dec1 = 0, c_ores = 0;
         bool ok = true;
         for (int r = 0; r * (int)gridDim.x < 2 * total && ok; ++r) {
             const int u = snake_index(r);
@@ -1381,6 +1502,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                     if (__any_sync(0xffffffffu, need)) {
                         const float alpha = (m == -INFINITY) ? 0.0f : ex2_mufu((m - m_cand) * sl2);
                         if (n > 0) {
+                            ++c_ores;
                             // O += P(n-1) V_{n-1} must be complete before O is rescaled (S(n) was
                             // issued before it, so the S barrier does not cover it).
                             if (!warp_wait(&bars[L::bVDone], (pv_done + (uint32_t)n - 1u) & 1u, abort_flag, wd)) {
@@ -1404,6 +1526,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                         ++c_res;
                     }
                     ++c_dec;
+                    if (n > 0) ++c_dec1;
                     const float neg = (m == -INFINITY) ? 0.0f : -m * sl2;
                     float sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
                     uint32_t pk[BN / 2];
@@ -1465,6 +1588,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             atomicAdd(p.counters + 0, c_dec);
             atomicAdd(p.counters + 1, c_res);
             atomicAdd(p.counters + 3, c_dec * 32ull * BN);
+            atomicAdd(p.counters + 4, c_dec1);
+            atomicAdd(p.counters + 5, c_ores);
         }
     }
 
@@ -1481,15 +1606,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 }
 
 cudaError_t launch_wide(const FwdTmaps& tm, const FwdParams& p, int grid, cudaStream_t stream) {
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<bool> attr_set[kMaxAttrDevices];
+    const cudaError_t e = ensure_smem_attr(attn_fwd_wide_kernel, LayoutWide::kAlloc, attr_set);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(attn_fwd_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, LayoutWide::kAlloc);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
     attn_fwd_wide_kernel<<<grid, kWideThreads, LayoutWide::kAlloc, stream>>>(tm.q, tm.k, tm.v, p);
     return cudaGetLastError();
 }

@@ -6,7 +6,24 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace attn {
+
+// Raise a kernel's dynamic shared-memory limit once per device (the current one). The flags
+// are atomics because launches can come from several host threads at once; setting the
+// attribute twice is harmless, so a race only repeats that call.
+constexpr int kMaxAttrDevices = 64;
+template <typename Kernel>
+inline cudaError_t ensure_smem_attr(Kernel kernel, int bytes, std::atomic<bool> (&done)[kMaxAttrDevices]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxAttrDevices && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < kMaxAttrDevices) done[dev].store(true, std::memory_order_release);
+    return e;
+}
 
 // Device status word layout (int[4]): [0] first error code (0 = ok), [1] detail, [2..3] reserved.
 enum DeviceErr : int {
@@ -15,9 +32,10 @@ enum DeviceErr : int {
     kDevBadIndex = -7,  // matches ATTN_ERR_DEVICE_BAD_INDEX
 };
 
-// Counters (unsigned long long[4]) when enabled: [0] softmax warp-tile decisions, [1] of which rescaled O,
-// [2] polynomial exponentials evaluated, [3] MUFU exponentials evaluated.
-constexpr int kNumCounters = 4;
+// Counters (unsigned long long[6]) when enabled: [0] softmax warp-tile decisions, [1] of which raised the
+// running maximum, [2] polynomial exponentials evaluated, [3] MUFU exponentials evaluated, [4] decisions
+// after the first key tile of a Q tile (O already holds a partial sum), [5] of which rescaled O.
+constexpr int kNumCounters = 6;
 
 struct FwdParams {
     __nv_bfloat16* o;
@@ -31,6 +49,9 @@ struct FwdParams {
     float out_scale;    // multiplies O at the end (8-bit inputs: the value descale; else 1)
     int sec_q;          // scheduling section, a multiple of G: dense, (batch, head) pairs; packed, query heads (divides Hq)
     int total_tiles;    // dense: number of work tiles; varlen: ignored (computed on device)
+    int packed_plain;   // packed sequences: 1 = sequences in the caller's order (no heaviest-first sort)
+    int corr_warp;      // 1: O is rescaled by the correction role (epilogue warps); 0: by the softmax warps
+    int unroll_kv;      // 1: the last P V product of a work tile and the first S = Q K^T of the next share a burst
     int* status;
     unsigned long long* counters;  // nullptr unless counting is enabled
     unsigned long long watchdog_ns;

@@ -253,6 +253,10 @@ attn_status_t attn_get_device_status(void* stream);
  *                        waves of the grid); packed sequences, query heads per section
  *   "count"              1: count softmax rescale decisions and exponentials (attn_read_counters)
  *   "watchdog_ms"        device wait limit before a kernel gives up (default 4000)
+ *   "packed_order"       packed sequences: 1 (default) orders work heaviest first across all
+ *                        sequences ("FlashAttention4 精读" section 3.3, LPT for varlen);
+ *                        0 keeps the sequences in the caller's order (each sequence's
+ *                        blocks still heaviest first), for measuring what the sort gains
  * Returns ATTN_ERR_BAD_ARG for an unknown name or an invalid value.
  */
 attn_status_t attn_set_option(const char* name, double value);
@@ -260,8 +264,12 @@ attn_status_t attn_get_option(const char* name, double* value);
 
 /*
  * Reads and clears the current device's counters (enabled by option "count"):
- * out[0] softmax warp-tile steps, out[1] of which rescaled O, out[2] exponentials on the
- * polynomial, out[3] exponentials on MUFU. n <= 4 values are written. Synchronises the device.
+ * out[0] softmax warp-tile steps (one warp's 32 rows against one key tile), out[1] of which
+ * raised the running maximum, out[2] exponentials on the polynomial, out[3] exponentials on
+ * MUFU, out[4] steps after the first key tile of a Q tile (O already holds a partial sum),
+ * out[5] of which rescaled O ("FlashAttention-4: Blackwell algorithm-pipeline co-design",
+ * conditional softmax rescaling: the fraction out[5] / out[4] is the rescale rate).
+ * n <= 6 values are written. Synchronises the device.
  */
 attn_status_t attn_read_counters(unsigned long long* out, int n);
 

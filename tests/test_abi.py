@@ -148,5 +148,13 @@ def test_options_roundtrip():
         A.attn_set_option("no_such_option", 1)
     with pytest.raises(A.AttnError):
         A.attn_set_option("exp_poly", 3)
+    # forward pipeline switches: on by default, 0 or 1 only
+    for name in ("correction", "unroll_kv", "packed_order"):
+        assert A.attn_get_option(name) == 1.0
+        A.attn_set_option(name, 0)
+        assert A.attn_get_option(name) == 0.0
+        A.attn_set_option(name, 1)
+        with pytest.raises(A.AttnError):
+            A.attn_set_option(name, 2)
     assert "sm_103a" in A.attn_version()
     assert A.status_string(A.ATTN_ERR_DEVICE_TIMEOUT).startswith("a kernel gave up")

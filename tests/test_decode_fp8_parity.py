@@ -112,15 +112,13 @@ def test_fp8_split_count_does_not_change_result(A):
         assert (lse - outs[0][1]).abs().max().item() <= 2e-3
 
 
-def test_fp8_decode_workload_sampled(A):
-    """The full e4m3 decode workload (64 sequences, lengths up to 32768) on the GPU, compared
-    with the oracle on 8 sequences including the longest."""
+def test_fp8_decode_workload_full(A):
+    """The full e4m3 decode workload (64 sequences, lengths up to 32768), every sequence and head."""
     c = W.decode_fp8()
     q, kc8, vc8, pt, sl, kds, vds = c.generate_fp8()
     o, lse = run(A, c, q, kc8, vc8, pt, sl, kds, vds)
-    rows = np.unique(np.concatenate([[int(np.argmax(sl)), int(np.argmin(sl))], np.arange(0, c.B, 10)]))
-    ro, rl = reference(c, q, kc8, vc8, pt, sl, kds, vds, rows)
-    do, dl = compare(o[torch.from_numpy(rows).to(DEV)], lse[torch.from_numpy(rows).to(DEV)], ro, rl)
+    ro, rl = reference(c, q, kc8, vc8, pt, sl, kds, vds)
+    do, dl = compare(o, lse, ro, rl)
     assert do <= TOL_O and dl <= TOL_LSE, f"max|dO|={do:.3e} max|dLSE|={dl:.3e}"
 
 

@@ -90,14 +90,9 @@ def test_d256_varlen_64_sequences(A):
     check(A, case("varlen64", 0, 2, 1, 0, 0, True, 93, lens=[int(x) for x in rng.integers(1, 301, size=64)]))
 
 
-def test_d256_long_causal_sampled(A):
-    """A long causal prefill (B1 H8 N8192, d 256) on sampled rows, every head's first and last row."""
-    c = case("d256_long", 1, 8, 8, 8192, 8192, True, 94)
-    T = c.total_q
-    rng = np.random.default_rng(5)
-    rows = np.unique(np.concatenate([rng.choice(T * c.Hq, size=1500, replace=False), np.arange(c.Hq),
-                                     (T - 1) * c.Hq + np.arange(c.Hq)])).astype(np.int64)
-    check(A, c, rows=rows)
+def test_d256_long_causal_full(A):
+    """The benchmark's head-width-256 leg (B1 H32 N8192 causal, Q x2), every row."""
+    check(A, case("d256_long", 1, 32, 32, 8192, 8192, True, W.long_causal().seed, 2.0))
 
 
 def test_d256_through_attn_fwd_hd(A):
@@ -118,14 +113,9 @@ def test_d256_through_attn_fwd_hd(A):
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
-def test_d256_noncausal_gqa_sampled(A):
-    """A non-causal GQA prefill (B2 Hq8 Hkv2 N4096, d 256) on sampled rows."""
-    c = case("d256_nc", 2, 8, 2, 4096, 4096, False, 96)
-    T = c.total_q
-    rng = np.random.default_rng(6)
-    rows = np.unique(np.concatenate([rng.choice(T * c.Hq, size=1200, replace=False), np.arange(c.Hq),
-                                     (T - 1) * c.Hq + np.arange(c.Hq)])).astype(np.int64)
-    check(A, c, rows=rows)
+def test_d256_noncausal_gqa_full(A):
+    """A non-causal GQA prefill (B2 Hq8 Hkv2 N4096, d 256), every row."""
+    check(A, case("d256_nc", 2, 8, 2, 4096, 4096, False, 96))
 
 
 def test_d256_varlen_several_launches(A):

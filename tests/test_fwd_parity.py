@@ -1,8 +1,8 @@
 """attn_fwd on the GPU against the float64 CPU oracle, element by element.
 
 Small cases span several 128x128 tiles with ragged tails; the full-size workloads
-(the same calls the benchmark times) are compared on sampled rows the oracle computes
-one by one. The bar is max|dO| <= 1.5e-2 and max|dLSE| <= 2e-3.
+(the same calls the benchmark times) are compared on every row. The bar is
+max|dO| <= 1.5e-2 and max|dLSE| <= 2e-3.
 """
 import math
 
@@ -106,31 +106,14 @@ def test_prefill_workload(A, causal):
     check_full(A, W.prefill(causal))
 
 
-def _sampled(A, c, n_rows, seed):
-    q, k, v = c.generate()
-    o, lse = run_fwd(A, c, q, k, v)
-    T = c.total_q
-    rng = np.random.default_rng(seed)
-    rows = rng.choice(T * c.Hq, size=n_rows, replace=False).astype(np.int64)
-    # always include the first and last rows of every head
-    edge = np.concatenate([np.arange(c.Hq), (T - 1) * c.Hq + np.arange(c.Hq)]).astype(np.int64)
-    rows = np.unique(np.concatenate([rows, edge]))
-    ro, rl = oracle.attn_fwd(q, k, v, c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d, c.scale, c.causal,
-                             cu_seqlens=c.cu_seqlens, rows=rows)
-    og = o.reshape(T * c.Hq, c.d)[torch.from_numpy(rows).to(DEV)]
-    lg = lse.reshape(-1)[torch.from_numpy(rows).to(DEV)]
-    do, dl = compare(og, lg, ro, rl)
-    assert do <= TOL_O and dl <= TOL_LSE, f"{c.name}: max|dO|={do:.3e} max|dLSE|={dl:.3e}"
-    # every row was written
-    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+def test_long_causal_workload_full(A):
+    """The long causal workload (B1 H32 N8192, Q x2) in the call the benchmark times, every row."""
+    check_full(A, W.long_causal())
 
 
-def test_long_causal_workload_sampled(A):
-    _sampled(A, W.long_causal(), 3000, 1)
-
-
-def test_varlen_gqa_workload_sampled(A):
-    _sampled(A, W.varlen_gqa(), 3000, 2)
+def test_varlen_gqa_workload_full(A):
+    """The packed GQA workload (8 sequences U[512, 4096], Hq32 Hkv8), every row."""
+    check_full(A, W.varlen_gqa())
 
 
 def test_varlen_packed_full(A):
@@ -167,18 +150,55 @@ def test_polynomial_exponentials(A):
 
 
 def test_counters_report_skipped_rescales(A):
+    c = W.prefill(True)
+    q, k, v = c.generate()
     A.attn_set_option("count", 1)
     try:
         A.attn_read_counters()
-        c = W.prefill(True)
-        q, k, v = c.generate()
         run_fwd(A, c, q, k, v)
-        dec, res, poly, mufu = A.attn_read_counters()
+        dec, res, poly, mufu, dec1, ores = A.attn_read_counters()
+        A.attn_set_option("rescale_threshold", 0.0)  # rescale on every increase of a maximum
+        run_fwd(A, c, q, k, v)
+        _, _, _, _, dec1_0, ores_0 = A.attn_read_counters()
     finally:
         A.attn_set_option("count", 0)
-    # one decision per softmax warp and KV tile; first tiles always rescale
+        A.attn_set_option("rescale_threshold", 8.0)
+    # one decision per softmax warp and KV tile; first tiles always raise the maximum
     assert dec > 0 and 0 < res < dec
     assert poly == 0 and mufu == dec * 32 * 128
+    # every (Q tile, warp) has one first step: 2 tiles x 4 warps per 256-row block
+    blocks = c.B * c.Hq * (c.Nq // 256)
+    assert dec - dec1 == 8 * blocks and dec1_0 == dec1
+    # O rescales are the raised maxima past the first step; the threshold skips most of them
+    assert res - ores == 8 * blocks
+    assert ores < ores_0 and ores_0 > 0 and ores <= dec1 // 10
+
+
+@pytest.mark.parametrize("corr,unroll", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_pipeline_switches_are_exact(A, corr, unroll):
+    """The correction role (on or off) and the unroll-KV burst at work-tile boundaries (on or
+    off) change only which warp rescales O and when products are issued, never the result
+    beyond rounding: each combination matches the oracle, with many rescales (Q x 4) and many
+    short work tiles per CTA (several 256-row blocks, GQA, ragged tails, packed sequences)."""
+    A.attn_set_option("correction", corr)
+    A.attn_set_option("unroll_kv", unroll)
+    try:
+        check_full(A, case(f"sw_sharp{corr}{unroll}", 2, 8, 2, 1300, 1300, 128, True, 40, 4.0), stress=True)
+        check_full(A, case(f"sw_nc{corr}{unroll}", 1, 4, 4, 700, 900, 64, False, 41))
+        check_full(A, case(f"sw_varlen{corr}{unroll}", 0, 4, 1, 0, 0, 128, True, 42,
+                           lens=[700, 1, 300, 0, 513, 256]))
+    finally:
+        A.attn_set_option("correction", 1)
+        A.attn_set_option("unroll_kv", 1)
+
+
+def test_packed_order_switch_is_exact(A):
+    """Sequences in the caller's order (no heaviest-first sort) give the same result."""
+    A.attn_set_option("packed_order", 0)
+    try:
+        check_full(A, W.varlen_gqa())
+    finally:
+        A.attn_set_option("packed_order", 1)
 
 
 def test_varlen_more_sequences_than_one_launch(A):

@@ -11,13 +11,19 @@ anything runs.
 The file name makes pytest collect it after every other test file.
 """
 import ctypes
+import json
 import math
+import os
+import subprocess
+import sys
+import textwrap
 
 import numpy as np
 import pytest
 
+import oracle
 import synth
-from helpers import TOL_LSE, TOL_O, ensure_built, to_dev
+from helpers import ROOT, TOL_LSE, TOL_O, compare, ensure_built, to_dev
 from synth import workloads as W
 
 torch = pytest.importorskip("torch")
@@ -76,11 +82,14 @@ def test_noalloc_matches_allocating_entry_point_over_calls_in_a_row(lib):
         inputs = (to_dev(q, DEV), to_dev(kc, DEV), to_dev(vc, DEV), torch.from_numpy(pt).to(DEV),
                   torch.from_numpy(sl).to(DEV))
         o_ref, l_ref = run(lib, "attn_decode_paged", c, inputs)
+        ro, rl = oracle.attn_decode_paged(q, kc, vc, pt, sl, c.page_size, c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.scale)
         for _ in range(2):  # two calls in a row on the same inputs
             o, l = run(lib, "attn_decode_paged_noalloc", c, inputs)
             assert torch.isfinite(o).all() and torch.isfinite(l).all()
             assert (o - o_ref).abs().max().item() <= TOL_O
             assert (l - l_ref).abs().max().item() <= TOL_LSE
+            do, dl = compare(o, l, ro, rl)  # and against the float64 oracle directly
+            assert do <= TOL_O and dl <= TOL_LSE, f"max|dO|={do:.3e} max|dLSE|={dl:.3e}"
 
 
 def test_noalloc_refuses_sizes_beyond_its_array(lib):
@@ -98,3 +107,84 @@ def test_noalloc_refuses_sizes_beyond_its_array(lib):
     assert rc == ATTN_ERR_SCRATCH_TOO_SMALL
     torch.cuda.synchronize()
     assert torch.isnan(o.float()).all() and torch.isnan(lse).all()  # nothing ran
+
+
+_FRESH = textwrap.dedent("""
+    import ctypes, json, math, re, sys
+    import numpy as np
+    import torch
+    sys.path.insert(0, ROOT)
+    import oracle
+    import synth
+    from synth import workloads as W
+    L = ctypes.CDLL(LIB)
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    f = L.attn_decode_paged_noalloc
+    f.argtypes = [vp, vp, vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, i, ctypes.c_float, i]
+    f.restype = i
+    L.attn_get_device_status.argtypes = [vp]
+    L.attn_get_device_status.restype = i
+    # the CUDA runtime the library uses, for the device's default memory pool
+    rt_path = next(l.split()[-1] for l in open("/proc/self/maps") if re.search(r"libcudart\\.so", l))
+    rt = ctypes.CDLL(rt_path)
+
+    def pool_high():
+        pool, v = ctypes.c_void_p(), ctypes.c_uint64()
+        if rt.cudaDeviceGetDefaultMemPool(ctypes.byref(pool), 0) != 0:
+            return None
+        out = []
+        for attr in (6, 8):  # reserved and used high watermarks
+            if rt.cudaMemPoolGetAttribute(pool, attr, ctypes.byref(v)) != 0:
+                return None
+            out.append(v.value)
+        return out
+
+    lens = synth.uniform_ints(64, 103, 2000, 9000)
+    c = W.DecodeCase("noalloc_fresh", 64, 32, 8, 128, 16, lens, int(lens.max()) // 16 + 2, 1 / math.sqrt(128), 103)
+    q, kc, vc, pt, sl = c.generate()
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    bf = lambda a: dev(a.view(np.int16)).view(torch.bfloat16)
+    Q, KC, VC, PT, SL = bf(q), bf(kc), bf(vc), dev(pt), dev(sl)
+    O = torch.empty((c.B, c.Hq, c.d), dtype=torch.bfloat16, device="cuda")
+    LSE = torch.empty((c.B, c.Hq), dtype=torch.float32, device="cuda")
+
+    def call():
+        rc = f(Q.data_ptr(), KC.data_ptr(), VC.data_ptr(), PT.data_ptr(), SL.data_ptr(), c.page_size, O.data_ptr(),
+               LSE.data_ptr(), None, c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.num_pages, c.scale, 0)
+        assert rc == 0, rc
+        assert L.attn_get_device_status(None) == 0  # synchronises
+
+    call()  # first call on the device: loads the kernels and resolves the array's address
+    torch.cuda.synchronize()
+    before = (torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated(), torch.cuda.memory_reserved(), pool_high())
+    res = []
+    for _ in range(2):
+        O.fill_(float("nan"))
+        LSE.fill_(float("nan"))
+        torch.cuda.synchronize()
+        mem0 = torch.cuda.mem_get_info()[0]
+        call()
+        res.append((O.float().cpu().numpy(), LSE.cpu().numpy()))
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == mem0
+    after = (torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated(), torch.cuda.memory_reserved(), pool_high())
+    ro, rl = oracle.attn_decode_paged(q, kc, vc, pt, sl, c.page_size, c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.scale)
+    err = [(float(np.abs(o - ro).max()), float(np.abs(l - rl).max())) for o, l in res]
+    print(json.dumps({"before": before, "after": after, "err": err}))
+""")
+
+
+def test_noalloc_in_a_fresh_process_allocates_nothing(lib):
+    """In a process that never calls the allocating decode, two calls in a row leave the free
+    device memory, PyTorch's allocator and the device's default memory pool exactly as they
+    were (a call that took its workspace from a retained pool or leaked it would show there),
+    and both match the float64 oracle."""
+    path = ensure_built()
+    env = dict(os.environ, PYTHONPATH=ROOT)
+    code = f"ROOT = {ROOT!r}\nLIB = {path!r}\n" + _FRESH
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-3000:]
+    r = json.loads(out.stdout.strip().splitlines()[-1])
+    assert r["before"] == r["after"], r
+    for do, dl in r["err"]:
+        assert do <= TOL_O and dl <= TOL_LSE, r["err"]
