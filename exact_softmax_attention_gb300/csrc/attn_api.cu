@@ -30,8 +30,8 @@ struct Options {
     int count = 0;
     double watchdog_ms = 4000.0;
     int packed_order = 1;
-    int correction = 1;
-    int unroll_kv = 1;
+    int correction = 0;
+    int unroll_kv = 0;
 };
 
 std::mutex g_mu;

@@ -83,12 +83,15 @@ struct Layout {
     // 8-bit inputs: [kEntries] the entry's 8-bit V tile has landed / has been widened. Only
     // entries that carry V advance them.
     static constexpr int bV8Full = bSFull + 16, bVConv = bV8Full + (F8 ? kEntries : 0);
-    // correction role: [4 s + quarter] the softmax warp's rescale factors for a step are
-    // published; [s] all four quarters of O_s are corrected for that step
-    static constexpr int bAlpha = bVConv + (F8 ? kEntries : 0), bCorr = bAlpha + 8;
-    static constexpr int kNumBars = bCorr + 2;
+    // correction role, [4 s + quarter]: a softmax warp's step after the first of its Q tile is
+    // decided (bAlpha: once per such step, with a flag saying whether it rescales O); in a
+    // rescaling step its first P stage is written (bPStage), after which the correction warp
+    // arrives on bPFull in its place once O is rescaled
+    static constexpr int bAlpha = bVConv + (F8 ? kEntries : 0), bPStage = bAlpha + 8;
+    static constexpr int kNumBars = bPStage + 8;
     static constexpr int kStatsOff = kBarOff + ((kNumBars * 8 + 15) / 16) * 16;
-    static constexpr int kMiscOff = kStatsOff + 3 * 2 * BM * 4;   // m[2][128], l[2][128], alpha[2][128]
+    // m[2][128], l[2][128], alpha[2][128], rescale flags [2][4]
+    static constexpr int kMiscOff = kStatsOff + (3 * 2 * BM + 8) * 4;
     // misc: tmem base, abort flag, packed-order levels, packed work tiles
     // packed-sequence work order (built once per CTA): pre, lvl, perm, nbs
     static constexpr int kPreOff = kMiscOff + 16;
@@ -454,7 +457,7 @@ __device__ __forceinline__ float ex2_poly(float x) {
     return __uint_as_float(__float_as_uint(q) + (__float_as_uint(t) << 23));
 }
 
-template <int D, int POLY_EVERY, int F8, int DV, int BNT>
+template <int D, int POLY_EVERY, int F8, int DV, int BNT, int UKV, int CORR>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -468,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* st_m = reinterpret_cast<float*>(smem + L::kStatsOff);  // [2][128]
     float* st_l = st_m + 2 * BM;                                    // [2][128]
     float* st_a = st_l + 2 * BM;                                    // [2][128] rescale factor of the last step
+    volatile int* st_f = reinterpret_cast<volatile int*>(st_a + 2 * BM);  // [2][4] that step rescales O
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
@@ -495,8 +499,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[L::bOFull + s], 1);
             mbar_init(&bars[L::bOEmpty + s], 4);
             mbar_init(&bars[L::bStats + s], 4);
-            mbar_init(&bars[L::bCorr + s], 4);  // the four correction warps
-            for (int q = 0; q < 4; ++q) mbar_init(&bars[L::bAlpha + 4 * s + q], 1);
+            for (int q = 0; q < 4; ++q) {
+                mbar_init(&bars[L::bAlpha + 4 * s + q], 1);
+                mbar_init(&bars[L::bPStage + 4 * s + q], 1);
+            }
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[L::bDrain + s], 1);
@@ -536,14 +542,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const uint64_t wd = p.watchdog_ns;
 
-    // Register split per warpgroup: producer/MMA 80, softmax 184 each, epilogue 64; with 8-bit
-    // inputs 72, 184, 184, 72 (the epilogue warps also widen V). Either sums to 512 = 4 x 128,
-    // the registers the CTA is launched with.
+    // Register split per warpgroup (producer/MMA, softmax, softmax, correction/epilogue): 72,
+    // 184, 184, 72; 80, 176, 176, 72 for 192-wide rows (the MMA warps need more, the softmax of
+    // 96-key tiles less); 80, 184, 184, 64 for the unroll-KV schedule. Each sums to at most
+    // 512 = 4 x 128, the registers the CTA is launched with.
+    constexpr int kRegLow = (D > 128 || UKV) ? 80 : 72;
+    constexpr int kRegSoftmax = D > 128 ? 176 : 184;
+    constexpr int kRegEpi = (UKV && D <= 128) ? 64 : 72;
+    static_assert(kRegLow + 2 * kRegSoftmax + kRegEpi <= 512, "register split");
     if (warp < 4) {
-        if constexpr (F8 != 0)
-            asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
-        else
-            asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegLow));
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
         // The whole warp walks the schedule so that addresses and coordinates stay
@@ -626,10 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ring entry n is released once both have committed their reads of it (count 2).
         // Within a warp, lane 0 issues every tcgen05 instruction while the whole warp keeps the
         // descriptors and slots warp-uniform.
-        // unroll-KV at work-tile boundaries ("Low-precision FA4", section 2.1.2): the last
-        // burst of a work tile holds only PV(last), and the first of the next only S(0), so
-        // the tensor pipe would idle while the other tile's softmax finishes. With p.unroll_kv
-        // the two are one burst: PV_s(last) of this tile, then S_s(0) = Q'_s K'_0^T of the next
+        // unroll-KV at work-tile boundaries ("Low-precision FA4", section 2.1.2; UKV = 1): the
+        // last burst of a work tile holds only PV(last), and the first of the next only S(0),
+        // so the tensor pipe would idle while the other tile's softmax finishes. With UKV the
+        // two are one burst: PV_s(last) of this tile, then S_s(0) = Q'_s K'_0^T of the next
         // (from the next ring entry; it overwrites P_s(last) only after the PV has read it).
         const int s = warp - 1;
         const uint32_t leader = lane == 0;
@@ -639,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t colS = s ? kColS1 : kColS0;
         const uint32_t colO = s ? kColO1 : kColO0;
         uint32_t stage = 0, phase = 0;
-        uint32_t qf = 0, pf = 0, oe = 0, cf = 0, burst = 0;
+        uint32_t qf = 0, pf = 0, oe = 0, burst = 0;
         uint32_t vcv = 0;  // 8-bit inputs: phase bit per ring slot of the V-widened barrier
         const uint32_t q_base = smem_u32(smem + L::kQOff) + s * L::kQBytes;
         const uint32_t kv_base = smem_u32(smem + L::kKVOff);
@@ -647,140 +655,216 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dk0 = smem_desc_sw128(kv_base, 16, 1024);
         const uint64_t dv0 = smem_desc_sw128(kv_base, L::kChunkBytesKV, 1024);
         bool ok = true, any = false;
-        // The next work tile (from round r on) with at least one key tile; advances r past it.
-        auto next_tile = [&](int& r, Tile& t) -> bool {
-            for (; r * (int)gridDim.x < total; ++r) {
+        if constexpr (UKV) {
+            // The next work tile (from round r on) with at least one key tile; advances r past it.
+            auto next_tile = [&](int& r, Tile& t) -> bool {
+                for (; r * (int)gridDim.x < total; ++r) {
+                    const int w = snake_index(r);
+                    if (w >= total) continue;
+                    get_tile<BN>(p, po, w, t);
+                    if (max(t.n[0], t.n[1]) > 0) {
+                        ++r;
+                        return true;
+                    }
+                }
+                return false;
+            };
+            // S = Q K^T of this warp's Q tile with the K tile in ring slot `slot`
+            auto issue_s = [&](uint32_t slot) {
+                // K steps of 32 bytes (16 bf16 or 32 8-bit elements), 4 per 128-byte chunk
+                const uint64_t kd = dk0 + (uint64_t)((slot * L::kEntryBytes) >> 4);
+    #pragma unroll
+                for (int k = 0; k < D * L::kElem / 32; ++k) {
+                    const uint64_t oq = (uint64_t)(((k >> 2) * L::kChunkBytesQ + (k & 3) * 32) >> 4);
+                    const uint64_t ok_ = (uint64_t)(((k >> 2) * L::kChunkBytesKV + (k & 3) * 32) >> 4);
+                    if (F8)
+                        tc_mma_ss_f8_by(leader, tmem + colS, dq + oq, kd + ok_, idS, k > 0 ? 1u : 0u);
+                    else
+                        tc_mma_ss_by(leader, tmem + colS, dq + oq, kd + ok_, idS, k > 0 ? 1u : 0u);
+                }
+            };
+            int r = 0;
+            Tile t;
+            bool have = next_tile(r, t);
+            int n_first = 0;  // 1 when the previous burst already issued this tile's S(0)
+            while (have && ok) {
+                const int nmax = max(t.n[0], t.n[1]);
+                const int ns = s ? t.n[1] : t.n[0];
+                if (n_first == 0 && ns > 0) {
+                    if (!(ok = warp_wait(&bars[L::bQFull + s], qf, abort_flag, wd))) break;
+                    qf ^= 1u;
+                    any = true;
+                }
+                Tile nt;
+                int r_next = r;
+                bool merged = false;
+                for (int n = n_first; n <= nmax && ok; ++n) {
+                    const bool do_pv = n >= 1 && n - 1 < ns, do_s = n < ns;
+                    const uint32_t e_slot = stage, e_par = phase;
+                    if (++stage == (uint32_t)L::kEntries) { stage = 0; phase ^= 1u; }
+                    ATTN_TL_DECL(long long tp = clock64());
+                    if (!(ok = warp_wait(&bars[L::bEFull + e_slot], e_par, abort_flag, wd))) break;
+                    if (do_pv) {
+                        if (!(ok = warp_wait(&bars[L::bPFull + s], pf, abort_flag, wd))) break;
+                        if (n - 1 == 0) {
+                            if (!(ok = warp_wait(&bars[L::bOEmpty + s], oe ^ 1u, abort_flag, wd))) break;
+                            oe ^= 1u;
+                        }
+                    }
+                    if (F8 && n >= 1) {  // every entry that carries V: wait until it has been widened
+                        if (!(ok = warp_wait(&bars[L::bVConv + e_slot], (vcv >> e_slot) & 1u, abort_flag, wd))) break;
+                        vcv ^= 1u << e_slot;
+                    }
+                    // unroll-KV: the next work tile's first entry and Q tile join the last burst
+                    bool mg = false;
+                    int nns = 0;
+                    uint32_t m_slot = 0;
+                    if (n == nmax && next_tile(r_next, nt)) {
+                        mg = true;
+                        nns = s ? nt.n[1] : nt.n[0];
+                        m_slot = stage;
+                        const uint32_t m_par = phase;
+                        if (++stage == (uint32_t)L::kEntries) { stage = 0; phase ^= 1u; }
+                        if (!(ok = warp_wait(&bars[L::bEFull + m_slot], m_par, abort_flag, wd))) break;
+                        if (nns > 0) {
+                            if (!(ok = warp_wait(&bars[L::bQFull + s], qf, abort_flag, wd))) break;
+                            qf ^= 1u;
+                            any = true;
+                        }
+                    }
+                    // token: burst 0 of step n follows burst 1 of step n-1; burst 1 follows burst 0
+                    if (s == 0) {
+                        if (burst > 0 && !(ok = warp_wait(&bars[L::bIssued + 1], (burst - 1) & 1u, abort_flag, wd))) break;
+                    } else {
+                        if (!(ok = warp_wait(&bars[L::bIssued + 0], burst & 1u, abort_flag, wd))) break;
+                    }
+                    ATTN_TL(s ? 4 : 1, 100 + s, n, tp, clock64());
+                    tc_fence_after();
+                    const uint32_t ent_off = e_slot * L::kEntryBytes;
+                    if (do_pv) {
+                        const uint64_t vd = dv0 + (uint64_t)((ent_off + L::kVOff) >> 4);
+                        const uint32_t acc0 = n - 1 > 0 ? 1u : 0u;
+    #pragma unroll
+                        for (int k = 0; k < kPA; ++k)  // P stage 1
+                            tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO,
+                                         k == 0 ? acc0 : 1u);
+                        if (!(ok = warp_wait(&bars[L::bPRest + s], pf, abort_flag, wd))) break;
+                        pf ^= 1u;
+                        tc_fence_after();
+    #pragma unroll
+                        for (int k = kPA; k < BN / 16; ++k)  // P stage 2
+                            tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO, 1u);
+                    }
+                    if (do_s) issue_s(e_slot);
+                    __syncwarp();
+                    if (mg) {
+                        // this tile's completions first, so that its epilogue starts without waiting
+                        // for the next tile's S(0)
+                        if (do_pv && n - 1 == ns - 1) tc_commit_by(leader, &bars[L::bOFull + s]);
+                        tc_commit_by(leader, &bars[L::bEEmpty + e_slot]);
+                        if (nns > 0) issue_s(m_slot);
+                        __syncwarp();
+                        if (leader) mbar_arrive(&bars[L::bIssued + s]);
+                        if (nns > 0) tc_commit_by(leader, &bars[L::bSFull + s]);
+                        if (nns == 1) tc_commit_by(leader, &bars[L::bQEmpty + s]);
+                        tc_commit_by(leader, &bars[L::bEEmpty + m_slot]);
+                    } else {
+                        if (leader) mbar_arrive(&bars[L::bIssued + s]);
+                        if (do_s) tc_commit_by(leader, &bars[L::bSFull + s]);
+                        if (do_pv && n - 1 == ns - 1) tc_commit_by(leader, &bars[L::bOFull + s]);
+                        if (do_s && n == ns - 1) tc_commit_by(leader, &bars[L::bQEmpty + s]);
+                        tc_commit_by(leader, &bars[L::bEEmpty + e_slot]);
+                    }
+                    ATTN_TL(s ? 4 : 1, 200 + s, n, clock64(), 0);
+                    ++burst;
+                    merged = mg;
+                }
+                if (!ok) break;
+                if (merged) {
+                    t = nt;
+                    r = r_next;
+                    n_first = 1;
+                } else {
+                    have = next_tile(r, t);
+                    n_first = 0;
+                }
+            }
+        } else {
+            for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
                 const int w = snake_index(r);
                 if (w >= total) continue;
+                Tile t;
                 get_tile<BN>(p, po, w, t);
-                if (max(t.n[0], t.n[1]) > 0) {
-                    ++r;
-                    return true;
+                const int nmax = max(t.n[0], t.n[1]);
+                const int ns = s ? t.n[1] : t.n[0];
+                if (nmax == 0) continue;
+                if (ns > 0) {
+                    if (!(ok = warp_wait(&bars[L::bQFull + s], qf, abort_flag, wd))) break;
+                    qf ^= 1u;
+                    any = true;
                 }
-            }
-            return false;
-        };
-        // S = Q K^T of this warp's Q tile with the K tile in ring slot `slot`
-        auto issue_s = [&](uint32_t slot) {
-            // K steps of 32 bytes (16 bf16 or 32 8-bit elements), 4 per 128-byte chunk
-            const uint64_t kd = dk0 + (uint64_t)((slot * L::kEntryBytes) >> 4);
-#pragma unroll
-            for (int k = 0; k < D * L::kElem / 32; ++k) {
-                const uint64_t oq = (uint64_t)(((k >> 2) * L::kChunkBytesQ + (k & 3) * 32) >> 4);
-                const uint64_t ok_ = (uint64_t)(((k >> 2) * L::kChunkBytesKV + (k & 3) * 32) >> 4);
-                if (F8)
-                    tc_mma_ss_f8_by(leader, tmem + colS, dq + oq, kd + ok_, idS, k > 0 ? 1u : 0u);
-                else
-                    tc_mma_ss_by(leader, tmem + colS, dq + oq, kd + ok_, idS, k > 0 ? 1u : 0u);
-            }
-        };
-        int r = 0;
-        Tile t;
-        bool have = next_tile(r, t);
-        int n_first = 0;  // 1 when the previous burst already issued this tile's S(0)
-        while (have && ok) {
-            const int nmax = max(t.n[0], t.n[1]);
-            const int ns = s ? t.n[1] : t.n[0];
-            if (n_first == 0 && ns > 0) {
-                if (!(ok = warp_wait(&bars[L::bQFull + s], qf, abort_flag, wd))) break;
-                qf ^= 1u;
-                any = true;
-            }
-            Tile nt;
-            int r_next = r;
-            bool merged = false;
-            for (int n = n_first; n <= nmax && ok; ++n) {
-                const bool do_pv = n >= 1 && n - 1 < ns, do_s = n < ns;
-                const uint32_t e_slot = stage, e_par = phase;
-                if (++stage == (uint32_t)L::kEntries) { stage = 0; phase ^= 1u; }
-                ATTN_TL_DECL(long long tp = clock64());
-                if (!(ok = warp_wait(&bars[L::bEFull + e_slot], e_par, abort_flag, wd))) break;
-                if (do_pv) {
-                    if (!(ok = warp_wait(&bars[L::bPFull + s], pf, abort_flag, wd))) break;
-                    if (n - 1 == 0) {
-                        if (!(ok = warp_wait(&bars[L::bOEmpty + s], oe ^ 1u, abort_flag, wd))) break;
-                        oe ^= 1u;
-                    } else if (p.corr_warp) {  // O_s rescaled (or left as is) for step n-1
-                        if (!(ok = warp_wait(&bars[L::bCorr + s], cf, abort_flag, wd))) break;
-                        cf ^= 1u;
-                    }
-                }
-                if (F8 && n >= 1) {  // every entry that carries V: wait until it has been widened
-                    if (!(ok = warp_wait(&bars[L::bVConv + e_slot], (vcv >> e_slot) & 1u, abort_flag, wd))) break;
-                    vcv ^= 1u << e_slot;
-                }
-                // unroll-KV: the next work tile's first entry and Q tile join the last burst
-                bool mg = false;
-                int nns = 0;
-                uint32_t m_slot = 0;
-                if (n == nmax && p.unroll_kv && next_tile(r_next, nt)) {
-                    mg = true;
-                    nns = s ? nt.n[1] : nt.n[0];
-                    m_slot = stage;
-                    const uint32_t m_par = phase;
+                for (int n = 0; n <= nmax && ok; ++n) {
+                    const bool do_pv = n >= 1 && n - 1 < ns, do_s = n < ns;
+                    const uint32_t e_slot = stage, e_par = phase;
                     if (++stage == (uint32_t)L::kEntries) { stage = 0; phase ^= 1u; }
-                    if (!(ok = warp_wait(&bars[L::bEFull + m_slot], m_par, abort_flag, wd))) break;
-                    if (nns > 0) {
-                        if (!(ok = warp_wait(&bars[L::bQFull + s], qf, abort_flag, wd))) break;
-                        qf ^= 1u;
-                        any = true;
+                    ATTN_TL_DECL(long long tp = clock64());
+                    if (!(ok = warp_wait(&bars[L::bEFull + e_slot], e_par, abort_flag, wd))) break;
+                    if (do_pv) {
+                        if (!(ok = warp_wait(&bars[L::bPFull + s], pf, abort_flag, wd))) break;
+                        if (n - 1 == 0) {
+                            if (!(ok = warp_wait(&bars[L::bOEmpty + s], oe ^ 1u, abort_flag, wd))) break;
+                            oe ^= 1u;
+                        }
                     }
-                }
-                // token: burst 0 of step n follows burst 1 of step n-1; burst 1 follows burst 0
-                if (s == 0) {
-                    if (burst > 0 && !(ok = warp_wait(&bars[L::bIssued + 1], (burst - 1) & 1u, abort_flag, wd))) break;
-                } else {
-                    if (!(ok = warp_wait(&bars[L::bIssued + 0], burst & 1u, abort_flag, wd))) break;
-                }
-                ATTN_TL(s ? 4 : 1, 100 + s, n, tp, clock64());
-                tc_fence_after();
-                const uint32_t ent_off = e_slot * L::kEntryBytes;
-                if (do_pv) {
-                    const uint64_t vd = dv0 + (uint64_t)((ent_off + L::kVOff) >> 4);
-                    const uint32_t acc0 = n - 1 > 0 ? 1u : 0u;
-#pragma unroll
-                    for (int k = 0; k < kPA; ++k)  // P stage 1
-                        tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO,
-                                     k == 0 ? acc0 : 1u);
-                    if (!(ok = warp_wait(&bars[L::bPRest + s], pf, abort_flag, wd))) break;
-                    pf ^= 1u;
+                    if (F8 && n >= 1) {  // every entry that carries V: wait until it has been widened
+                        if (!(ok = warp_wait(&bars[L::bVConv + e_slot], (vcv >> e_slot) & 1u, abort_flag, wd))) break;
+                        vcv ^= 1u << e_slot;
+                    }
+                    // token: burst 0 of step n follows burst 1 of step n-1; burst 1 follows burst 0
+                    if (s == 0) {
+                        if (burst > 0 && !(ok = warp_wait(&bars[L::bIssued + 1], (burst - 1) & 1u, abort_flag, wd))) break;
+                    } else {
+                        if (!(ok = warp_wait(&bars[L::bIssued + 0], burst & 1u, abort_flag, wd))) break;
+                    }
+                    ATTN_TL(s ? 4 : 1, 100 + s, n, tp, clock64());
                     tc_fence_after();
-#pragma unroll
-                    for (int k = kPA; k < BN / 16; ++k)  // P stage 2
-                        tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO, 1u);
-                }
-                if (do_s) issue_s(e_slot);
-                __syncwarp();
-                if (mg) {
-                    // this tile's completions first, so that its epilogue starts without waiting
-                    // for the next tile's S(0)
-                    if (do_pv && n - 1 == ns - 1) tc_commit_by(leader, &bars[L::bOFull + s]);
-                    tc_commit_by(leader, &bars[L::bEEmpty + e_slot]);
-                    if (nns > 0) issue_s(m_slot);
+                    const uint32_t ent_off = e_slot * L::kEntryBytes;
+                    if (do_pv) {
+                        const uint64_t vd = dv0 + (uint64_t)((ent_off + L::kVOff) >> 4);
+                        const uint32_t acc0 = n - 1 > 0 ? 1u : 0u;
+    #pragma unroll
+                        for (int k = 0; k < kPA; ++k)  // P stage 1
+                            tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO,
+                                         k == 0 ? acc0 : 1u);
+                        if (!(ok = warp_wait(&bars[L::bPRest + s], pf, abort_flag, wd))) break;
+                        pf ^= 1u;
+                        tc_fence_after();
+    #pragma unroll
+                        for (int k = kPA; k < BN / 16; ++k)  // P stage 2
+                            tc_mma_ts_by(leader, tmem + colO, tmem + colS + k * 8, vd + (uint64_t)(k * (2048 >> 4)), idO, 1u);
+                    }
+                    if (do_s) {
+                        // K steps of 32 bytes (16 bf16 or 32 8-bit elements), 4 per 128-byte chunk
+                        const uint64_t kd = dk0 + (uint64_t)(ent_off >> 4);
+    #pragma unroll
+                        for (int k = 0; k < D * L::kElem / 32; ++k) {
+                            const uint64_t oq = (uint64_t)(((k >> 2) * L::kChunkBytesQ + (k & 3) * 32) >> 4);
+                            const uint64_t ok_ = (uint64_t)(((k >> 2) * L::kChunkBytesKV + (k & 3) * 32) >> 4);
+                            if (F8)
+                                tc_mma_ss_f8_by(leader, tmem + colS, dq + oq, kd + ok_, idS, k > 0 ? 1u : 0u);
+                            else
+                                tc_mma_ss_by(leader, tmem + colS, dq + oq, kd + ok_, idS, k > 0 ? 1u : 0u);
+                        }
+                    }
                     __syncwarp();
-                    if (leader) mbar_arrive(&bars[L::bIssued + s]);
-                    if (nns > 0) tc_commit_by(leader, &bars[L::bSFull + s]);
-                    if (nns == 1) tc_commit_by(leader, &bars[L::bQEmpty + s]);
-                    tc_commit_by(leader, &bars[L::bEEmpty + m_slot]);
-                } else {
                     if (leader) mbar_arrive(&bars[L::bIssued + s]);
                     if (do_s) tc_commit_by(leader, &bars[L::bSFull + s]);
                     if (do_pv && n - 1 == ns - 1) tc_commit_by(leader, &bars[L::bOFull + s]);
                     if (do_s && n == ns - 1) tc_commit_by(leader, &bars[L::bQEmpty + s]);
                     tc_commit_by(leader, &bars[L::bEEmpty + e_slot]);
+                    ATTN_TL(s ? 4 : 1, 200 + s, n, clock64(), 0);
+                    ++burst;
                 }
-                ATTN_TL(s ? 4 : 1, 200 + s, n, clock64(), 0);
-                ++burst;
-                merged = mg;
-            }
-            if (!ok) break;
-            if (merged) {
-                t = nt;
-                r = r_next;
-                n_first = 1;
-            } else {
-                have = next_tile(r, t);
-                n_first = 0;
             }
         }
         if (any) {
@@ -793,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     } else if (warp < 12) {
         // ------------------------------------------------------------------ softmax
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
         const int s = (warp - 4) >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
@@ -802,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + (s ? kColO1 : kColO0);
         const float sl2 = p.scale_log2;
         uint32_t sf = 0, oe = 0;
-        uint32_t c_dec = 0, c_res = 0, c_dec1 = 0, c_ores = 0;  // per warp: far below 2^32
+        uint32_t c_dec = 0, c_res = 0, c_first = 0, c_ores = 0;  // per warp: far below 2^32
         bool ok = true;
         for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
             const int w = snake_index(r);
@@ -815,6 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int qrow = tile_row0 + row;
             const int off = t.Lk - t.Lq;
             float m = -INFINITY, l = 0.0f;
+            ++c_first;
             for (int n = 0; n < ns; ++n) {
                 ATTN_TL_DECL(long long ts0 = clock64());
                 if (!warp_wait(&bars[L::bSFull + s], sf, abort_flag, wd)) { ok = false; break; }
@@ -850,12 +935,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float m_cand = fmaxf(m, mt);
                 const bool need = (m_cand - m) * sl2 > p.rescale_thr;  // NaN (both -inf) is false
                 const bool warp_need = __any_sync(0xffffffffu, need);
-                float alpha = 1.0f;  // rows of a warp that keeps its maxima keep O as it is
+                bool handed = false;  // O's rescale for this step handed to the correction warp
                 if (warp_need) {
-                    alpha = (m == -INFINITY) ? 0.0f : ex2_mufu((m - m_cand) * sl2);
+                    const float alpha = (m == -INFINITY) ? 0.0f : ex2_mufu((m - m_cand) * sl2);
                     if (n > 0) {
                         ++c_ores;
-                        if (!p.corr_warp) {
+                        if constexpr (CORR != 0) {
+                            // the correction warp of this quarter rescales O_s while the
+                            // exponentials below are computed (rows that keep their maximum
+                            // have alpha = 1)
+                            st_a[s * BM + row] = alpha;
+                            if (lane == 0) st_f[4 * s + quarter] = 1;
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&bars[L::bAlpha + 4 * s + quarter]);
+                            handed = true;
+                        } else {
 #pragma unroll 1
                             for (int c = 0; c < DV; c += 16) {
                                 uint32_t o[16];
@@ -873,16 +967,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++c_res;
                 }
                 ++c_dec;
-                if (n > 0) {
-                    ++c_dec1;
-                    if (p.corr_warp) {
-                        // hand the rescale of O_s to the correction warp of this quarter (it runs
-                        // while the exponentials below are computed); alpha = 1 means no change
-                        st_a[s * BM + row] = alpha;
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&bars[L::bAlpha + 4 * s + quarter]);
-                    }
-                }
                 const float neg = (m == -INFINITY) ? 0.0f : -m * sl2;
                 // exponent arguments two at a time (packed FMA), exponentials, packed row sums;
                 // P goes out in two stages (keys 0-95, then 96-127)
@@ -910,7 +994,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[L::bPFull + s]);
+                // P stage 1 is written; in a handed-over step the correction warp passes this on
+                // to the MMA warp once O_s is rescaled
+                if (lane == 0) mbar_arrive(handed ? &bars[L::bPStage + 4 * s + quarter] : &bars[L::bPFull + s]);
 #pragma unroll
                 for (int c = kSA; c < BN; c += 2) exp_pair(c);
                 store_p_cols<kSA / 2, BN / 2>(tS, pk);
@@ -919,6 +1005,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[L::bPRest + s]);
+                if (CORR != 0 && n > 0 && !handed && lane == 0) {
+                    // nothing to correct in this step: tell the correction warp, off the
+                    // critical path (after P is complete)
+                    st_f[4 * s + quarter] = 0;
+                    mbar_arrive(&bars[L::bAlpha + 4 * s + quarter]);
+                }
                 if (quarter == 0) ATTN_TL(2 + s, n, ts0, ts1, clock64());
             }
             if (!ok) break;
@@ -937,52 +1029,57 @@ __global__ void __launch_bounds__(kThreads, 1)
             const unsigned long long poly = POLY_EVERY > 0 ? ex / POLY_EVERY : 0ull;
             atomicAdd(p.counters + 2, poly);
             atomicAdd(p.counters + 3, ex - poly);
-            atomicAdd(p.counters + 4, (unsigned long long)c_dec1);
+            atomicAdd(p.counters + 4, (unsigned long long)(c_dec - c_first));
             atomicAdd(p.counters + 5, (unsigned long long)c_ores);
         }
     } else {
         // ------------------------------------------------------------------ correction + epilogue
-        // Warp 12 + q serves TMEM lane quarter q of both Q tiles. Per KV step it rescales the
-        // quarter's rows of O_s by the factors the softmax warp published, when any of them
-        // changed its maximum ("FlashAttention4 精读" section 3.1, correction warpgroup;
-        // "FlashAttention-4: Blackwell algorithm-pipeline co-design", conditional softmax
-        // rescaling), and signals the MMA warp, which issues the next O += P V only after
-        // that; with 8-bit inputs it also widens V tiles; after the last step it writes O / l
-        // and the LSE.
-        if constexpr (F8 != 0)
-            asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");  // also widens the 8-bit V tiles
-        else
-            asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
+        // Warp 12 + q serves TMEM lane quarter q of both Q tiles: it is the correction warp
+        // ("FlashAttention4 精读" section 3.1, correction warpgroup; "FlashAttention-4:
+        // Blackwell algorithm-pipeline co-design", conditional softmax rescaling), widens
+        // 8-bit V tiles, and writes O / l and the LSE of finished rows. It follows the softmax
+        // warps step by step: for every step after the first of a Q tile the softmax warp of
+        // its quarter reports (bAlpha) whether it raised its rows' maxima by more than the
+        // threshold. Only then does this warp have work: the softmax warp publishes the
+        // factors right after its decision and goes on with its exponentials, this warp
+        // rescales the quarter's rows of O_s in TMEM meanwhile and then passes the softmax
+        // warp's "P stage 1 written" (bPStage) on to the MMA warp (bPFull), so the next
+        // O += P V starts on the rescaled accumulator. In the other steps the report comes
+        // after P is complete, off the critical path, and the MMA warp never waits for this
+        // warp.
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegEpi));
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         uint32_t of[2] = {0, 0}, sp[2] = {0, 0};
-        uint32_t ap = 0;               // bit s: parity of the next phase of this quarter's alpha barrier of tile s
+        uint32_t ap = 0, pst = 0;      // bit s: parity of the next phase of this quarter's bAlpha / bPStage of tile s
         uint32_t stage = 0, v8ph = 0;  // 8-bit inputs: ring slot and per-slot phase bits of bV8Full
         bool ok = true;
-        // O_s of this quarter's rows times the factors of the step just decided (all 1: nothing to do)
-        auto correct = [&](int s) -> bool {
+        // The report of tile s's next step; in a rescaling step O_s of this quarter's rows times
+        // the published factors, then the first P stage on to the MMA warp.
+        auto step = [&](int s) -> bool {
             if (!warp_wait(&bars[L::bAlpha + 4 * s + quarter], (ap >> s) & 1u, abort_flag, wd)) return false;
             ap ^= 1u << s;
+            if (!st_f[4 * s + quarter]) return true;
+            tc_fence_after();
             const float a = st_a[s * BM + row];
-            if (__any_sync(0xffffffffu, a != 1.0f)) {
-                tc_fence_after();
-                const uint32_t tO = tmem + lane_off + (s ? kColO1 : kColO0);
+            const uint32_t tO = tmem + lane_off + (s ? kColO1 : kColO0);
 #pragma unroll 1
-                for (int c = 0; c < DV; c += 16) {
-                    uint32_t o[16];
-                    tmem_ld16(tO + c, o);
-                    tc_wait_ld();
-                    reg_fence(o);
+            for (int c = 0; c < DV; c += 16) {
+                uint32_t o[16];
+                tmem_ld16(tO + c, o);
+                tc_wait_ld();
+                reg_fence(o);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
-                    tmem_st16(tO + c, o);
-                }
-                tc_wait_st();
+                for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+                tmem_st16(tO + c, o);
             }
+            tc_wait_st();
+            if (!warp_wait(&bars[L::bPStage + 4 * s + quarter], (pst >> s) & 1u, abort_flag, wd)) return false;
+            pst ^= 1u << s;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[L::bCorr + s]);
+            if (lane == 0) mbar_arrive(&bars[L::bPFull + s]);
             return true;
         };
         for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
@@ -992,16 +1089,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             get_tile<BN>(p, po, w, t);
             const int nmax = max(t.n[0], t.n[1]);
             if (nmax > 0) {
-                // Per step e: the correction of tile 0, the widening of the 8-bit V tile of ring
-                // entry e + 1 (rows 32*quarter .. +31, in ring order), the correction of tile 1,
-                // in the order the MMA warps need them. The MMA warps wait for the widening
-                // (bVConv) before each P V product and only then release the entry, so the 8-bit
-                // tile is never overwritten while read here.
+                // Per step e: with 8-bit inputs the widening of the V tile of ring entry e + 1
+                // (rows 32*quarter .. +31, in ring order; the MMA warps wait for it (bVConv)
+                // before each P V product and only then release the entry, so the 8-bit tile is
+                // never overwritten while read here), then the step reports of tiles 0 and 1.
                 if constexpr (F8 != 0) {
                     if (++stage == (uint32_t)L::kEntries) stage = 0;  // entry 0 carries no V
                 }
                 for (int e = 0; e < nmax && ok; ++e) {
-                    if (p.corr_warp && e >= 1 && e < t.n[0] && !(ok = correct(0))) break;
                     if constexpr (F8 != 0) {
                         const uint32_t e_slot = stage;
                         if (++stage == (uint32_t)L::kEntries) stage = 0;
@@ -1013,7 +1108,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars[L::bVConv + e_slot]);
                     }
-                    if (p.corr_warp && e >= 1 && e < t.n[1] && !(ok = correct(1))) break;
+                    if (CORR != 0 && e >= 1) {
+                        if (e < t.n[0] && !(ok = step(0))) break;
+                        if (e < t.n[1] && !(ok = step(1))) break;
+                    }
                 }
                 if (!ok) break;
             }
@@ -1077,13 +1175,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, int POLY, int F8, int DV = D, int BNT = BN>
+template <int D, int POLY, int F8, int DV = D, int BNT = BN, int UKV = 0, int CORR = 0>
 cudaError_t launch_t(const FwdTmaps& tm, const FwdParams& p, int grid, cudaStream_t stream) {
     using L = Layout<D, F8, DV, BNT>;
     static std::atomic<bool> attr_set[kMaxAttrDevices];
-    const cudaError_t e = ensure_smem_attr(attn_fwd_kernel<D, POLY, F8, DV, BNT>, L::kAlloc, attr_set);
+    const cudaError_t e = ensure_smem_attr(attn_fwd_kernel<D, POLY, F8, DV, BNT, UKV, CORR>, L::kAlloc, attr_set);
     if (e != cudaSuccess) return e;
-    attn_fwd_kernel<D, POLY, F8, DV, BNT><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.k, tm.v, p);
+    attn_fwd_kernel<D, POLY, F8, DV, BNT, UKV, CORR><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.k, tm.v, p);
     return cudaGetLastError();
 }
 
@@ -1632,7 +1730,9 @@ cudaError_t launch_attn_fwd_hd(const FwdTmaps& tm, const FwdParams& p, int d, in
 cudaError_t launch_attn_fwd(const FwdTmaps& tm, const FwdParams& p, int d, int exp_poly, int grid,
                             cudaStream_t stream) {
     if (d == 128) {
-        return exp_poly ? launch_t<128, 8, 0>(tm, p, grid, stream) : launch_t<128, 0, 0>(tm, p, grid, stream);
+        if (exp_poly) return launch_t<128, 8, 0>(tm, p, grid, stream);
+        if (p.unroll_kv) return launch_t<128, 0, 0, 128, BN, 1>(tm, p, grid, stream);
+        return p.corr_warp ? launch_t<128, 0, 0, 128, BN, 0, 1>(tm, p, grid, stream) : launch_t<128, 0, 0>(tm, p, grid, stream);
     }
     return exp_poly ? launch_t<64, 8, 0>(tm, p, grid, stream) : launch_t<64, 0, 0>(tm, p, grid, stream);
 }
@@ -1640,7 +1740,9 @@ cudaError_t launch_attn_fwd(const FwdTmaps& tm, const FwdParams& p, int d, int e
 cudaError_t launch_attn_fwd_fp8(const FwdTmaps& tm, const FwdParams& p, int d, int fmt, int grid,
                                 cudaStream_t stream) {
     if (d != 128) return cudaErrorInvalidValue;
-    return fmt == 0 ? launch_t<128, 0, 1>(tm, p, grid, stream) : launch_t<128, 0, 2>(tm, p, grid, stream);
+    if (fmt == 0)
+        return p.unroll_kv ? launch_t<128, 0, 1, 128, BN, 1>(tm, p, grid, stream) : launch_t<128, 0, 1>(tm, p, grid, stream);
+    return launch_t<128, 0, 2>(tm, p, grid, stream);
 }
 
 // ------------------------------------------------------------------------------ diagnostics

@@ -148,12 +148,12 @@ def test_options_roundtrip():
         A.attn_set_option("no_such_option", 1)
     with pytest.raises(A.AttnError):
         A.attn_set_option("exp_poly", 3)
-    # forward pipeline switches: on by default, 0 or 1 only
-    for name in ("correction", "unroll_kv", "packed_order"):
-        assert A.attn_get_option(name) == 1.0
-        A.attn_set_option(name, 0)
-        assert A.attn_get_option(name) == 0.0
-        A.attn_set_option(name, 1)
+    # forward pipeline switches: 0 or 1 only
+    for name, default in (("correction", 0), ("unroll_kv", 0), ("packed_order", 1)):
+        assert A.attn_get_option(name) == default
+        A.attn_set_option(name, 1 - default)
+        assert A.attn_get_option(name) == 1 - default
+        A.attn_set_option(name, default)
         with pytest.raises(A.AttnError):
             A.attn_set_option(name, 2)
     assert "sm_103a" in A.attn_version()

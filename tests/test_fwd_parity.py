@@ -174,22 +174,32 @@ def test_counters_report_skipped_rescales(A):
     assert ores < ores_0 and ores_0 > 0 and ores <= dec1 // 10
 
 
+@pytest.mark.parametrize("thr", [8.0, 0.0])
 @pytest.mark.parametrize("corr,unroll", [(0, 0), (0, 1), (1, 0), (1, 1)])
-def test_pipeline_switches_are_exact(A, corr, unroll):
+def test_pipeline_switches_are_exact(A, corr, unroll, thr):
     """The correction role (on or off) and the unroll-KV burst at work-tile boundaries (on or
     off) change only which warp rescales O and when products are issued, never the result
-    beyond rounding: each combination matches the oracle, with many rescales (Q x 4) and many
-    short work tiles per CTA (several 256-row blocks, GQA, ragged tails, packed sequences)."""
+    beyond rounding: each combination matches the oracle, with sharp scores (Q x 4), with
+    threshold 0 (a rescale at nearly every step, so the correction warps serve requests from
+    both Q tiles all the time), and with many short work tiles per CTA (several 256-row blocks,
+    GQA, ragged tails, packed sequences)."""
     A.attn_set_option("correction", corr)
     A.attn_set_option("unroll_kv", unroll)
+    A.attn_set_option("rescale_threshold", thr)
+    A.attn_set_option("count", 1)
     try:
-        check_full(A, case(f"sw_sharp{corr}{unroll}", 2, 8, 2, 1300, 1300, 128, True, 40, 4.0), stress=True)
-        check_full(A, case(f"sw_nc{corr}{unroll}", 1, 4, 4, 700, 900, 64, False, 41))
-        check_full(A, case(f"sw_varlen{corr}{unroll}", 0, 4, 1, 0, 0, 128, True, 42,
-                           lens=[700, 1, 300, 0, 513, 256]))
+        A.attn_read_counters()
+        tag = f"{corr}{unroll}_{int(thr)}"
+        check_full(A, case(f"sw_sharp{tag}", 2, 8, 2, 1300, 1300, 128, True, 40, 4.0), stress=True)
+        check_full(A, case(f"sw_nc{tag}", 1, 4, 4, 700, 900, 64, False, 41))
+        check_full(A, case(f"sw_varlen{tag}", 0, 4, 1, 0, 0, 128, True, 42, lens=[700, 1, 300, 0, 513, 256]))
+        _, _, _, _, dec1, ores = A.attn_read_counters()
+        assert ores > 0 and (thr > 0 or ores > dec1 // 4)
     finally:
-        A.attn_set_option("correction", 1)
-        A.attn_set_option("unroll_kv", 1)
+        A.attn_set_option("correction", 0)
+        A.attn_set_option("unroll_kv", 0)
+        A.attn_set_option("rescale_threshold", 8.0)
+        A.attn_set_option("count", 0)
 
 
 def test_packed_order_switch_is_exact(A):
