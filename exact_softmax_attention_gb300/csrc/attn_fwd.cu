@@ -47,6 +47,7 @@ constexpr int kThreads = 512;
 constexpr int kMaxVarlenB = 1024;
 constexpr int kMaxLevels = 2048;  // 256-row blocks per packed sequence for the level order
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
+constexpr int kReqRescale = 1, kReqEpilogue = 3;  // request codes of the correction role (+ Q tile)
 constexpr uint32_t kTmemCols = 512;
 
 // D: width of queries and keys; DV: width of values and outputs; BNT: keys per K/V tile.
@@ -83,15 +84,14 @@ struct Layout {
     // 8-bit inputs: [kEntries] the entry's 8-bit V tile has landed / has been widened. Only
     // entries that carry V advance them.
     static constexpr int bV8Full = bSFull + 16, bVConv = bV8Full + (F8 ? kEntries : 0);
-    // correction role, [4 s + quarter]: a softmax warp's step after the first of its Q tile is
-    // decided (bAlpha: once per such step, with a flag saying whether it rescales O); in a
-    // rescaling step its first P stage is written (bPStage), after which the correction warp
-    // arrives on bPFull in its place once O is rescaled
-    static constexpr int bAlpha = bVConv + (F8 ? kEntries : 0), bPStage = bAlpha + 8;
+    // correction role: [quarter] a request is posted in the quarter's slot (bReq); [4 s +
+    // quarter] in a step whose O rescale was handed over, the softmax warp's first P stage is
+    // written (bPStage), after which the correction warp arrives on bPFull in its place
+    static constexpr int bReq = bVConv + (F8 ? kEntries : 0), bPStage = bReq + 4;
     static constexpr int kNumBars = bPStage + 8;
     static constexpr int kStatsOff = kBarOff + ((kNumBars * 8 + 15) / 16) * 16;
-    // m[2][128], l[2][128], alpha[2][128], rescale flags [2][4]
-    static constexpr int kMiscOff = kStatsOff + (3 * 2 * BM + 8) * 4;
+    // m[2][128], l[2][128], alpha[2][128], request slots [4]
+    static constexpr int kMiscOff = kStatsOff + (3 * 2 * BM + 4) * 4;
     // misc: tmem base, abort flag, packed-order levels, packed work tiles
     // packed-sequence work order (built once per CTA): pre, lvl, perm, nbs
     static constexpr int kPreOff = kMiscOff + 16;
@@ -470,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
     float* st_m = reinterpret_cast<float*>(smem + L::kStatsOff);  // [2][128]
     float* st_l = st_m + 2 * BM;                                    // [2][128]
-    float* st_a = st_l + 2 * BM;                                    // [2][128] rescale factor of the last step
-    volatile int* st_f = reinterpret_cast<volatile int*>(st_a + 2 * BM);  // [2][4] that step rescales O
+    float* st_a = st_l + 2 * BM;                                    // [2][128] rescale factors handed over
+    int* st_req = reinterpret_cast<int*>(st_a + 2 * BM);            // [4] request slot per lane quarter
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
@@ -499,14 +499,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[L::bOFull + s], 1);
             mbar_init(&bars[L::bOEmpty + s], 4);
             mbar_init(&bars[L::bStats + s], 4);
-            for (int q = 0; q < 4; ++q) {
-                mbar_init(&bars[L::bAlpha + 4 * s + q], 1);
-                mbar_init(&bars[L::bPStage + 4 * s + q], 1);
-            }
+            for (int q = 0; q < 4; ++q) mbar_init(&bars[L::bPStage + 4 * s + q], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[L::bDrain + s], 1);
             mbar_init(&bars[L::bIssued + s], 1);
+        }
+        for (int q = 0; q < 4; ++q) {
+            mbar_init(&bars[L::bReq + q], 1);
+            st_req[q] = 0;
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -941,15 +942,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (n > 0) {
                         ++c_ores;
                         if constexpr (CORR != 0) {
-                            // the correction warp of this quarter rescales O_s while the
-                            // exponentials below are computed (rows that keep their maximum
-                            // have alpha = 1)
+                            // hand the rescale to the correction warp of this quarter, which
+                            // works while the exponentials below are computed (rows that keep
+                            // their maximum have alpha = 1); if the quarter's request slot is
+                            // taken, rescale here
                             st_a[s * BM + row] = alpha;
-                            if (lane == 0) st_f[4 * s + quarter] = 1;
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(&bars[L::bAlpha + 4 * s + quarter]);
-                            handed = true;
-                        } else {
+                            int posted = 0;
+                            if (lane == 0 && atomicCAS(&st_req[quarter], 0, kReqRescale + s) == 0) {
+                                mbar_arrive(&bars[L::bReq + quarter]);
+                                posted = 1;
+                            }
+                            handed = __shfl_sync(0xffffffffu, posted, 0) != 0;
+                        }
+                        if (!handed) {
 #pragma unroll 1
                             for (int c = 0; c < DV; c += 16) {
                                 uint32_t o[16];
@@ -1005,12 +1011,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[L::bPRest + s]);
-                if (CORR != 0 && n > 0 && !handed && lane == 0) {
-                    // nothing to correct in this step: tell the correction warp, off the
-                    // critical path (after P is complete)
-                    st_f[4 * s + quarter] = 0;
-                    mbar_arrive(&bars[L::bAlpha + 4 * s + quarter]);
-                }
                 if (quarter == 0) ATTN_TL(2 + s, n, ts0, ts1, clock64());
             }
             if (!ok) break;
@@ -1020,7 +1020,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_m[s * BM + row] = m;
             st_l[s * BM + row] = l;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[L::bStats + s]);
+            if constexpr (CORR != 0) {
+                // the finished tile is a request too: wait (bounded) until the quarter's slot is
+                // free; the correction warp frees it as soon as it has read the one there
+                int posted = 1;
+                if (lane == 0) {
+                    const uint64_t t0 = global_timer_ns();
+                    while (atomicCAS(&st_req[quarter], 0, kReqEpilogue + s) != 0) {
+                        if (*abort_flag || global_timer_ns() - t0 > wd) {
+                            *abort_flag = 1;
+                            posted = 0;
+                            break;
+                        }
+                    }
+                    if (posted) mbar_arrive(&bars[L::bReq + quarter]);
+                }
+                if (!__shfl_sync(0xffffffffu, posted, 0)) { ok = false; break; }
+            } else {
+                if (lane == 0) mbar_arrive(&bars[L::bStats + s]);
+            }
         }
         if (p.counters && lane == 0) {
             atomicAdd(p.counters + 0, (unsigned long long)c_dec);
@@ -1034,72 +1052,154 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------------ correction + epilogue
-        // Warp 12 + q serves TMEM lane quarter q of both Q tiles: it is the correction warp
-        // ("FlashAttention4 精读" section 3.1, correction warpgroup; "FlashAttention-4:
-        // Blackwell algorithm-pipeline co-design", conditional softmax rescaling), widens
-        // 8-bit V tiles, and writes O / l and the LSE of finished rows. It follows the softmax
-        // warps step by step: for every step after the first of a Q tile the softmax warp of
-        // its quarter reports (bAlpha) whether it raised its rows' maxima by more than the
-        // threshold. Only then does this warp have work: the softmax warp publishes the
-        // factors right after its decision and goes on with its exponentials, this warp
-        // rescales the quarter's rows of O_s in TMEM meanwhile and then passes the softmax
-        // warp's "P stage 1 written" (bPStage) on to the MMA warp (bPFull), so the next
-        // O += P V starts on the rescaled accumulator. In the other steps the report comes
-        // after P is complete, off the critical path, and the MMA warp never waits for this
-        // warp.
+        // Warp 12 + q serves TMEM lane quarter q of both Q tiles: it writes O / l and the LSE
+        // of finished rows and, with 8-bit inputs, widens V tiles. With CORR it is also the
+        // correction warp ("FlashAttention4 精读" section 3.1, correction warpgroup;
+        // "FlashAttention-4: Blackwell algorithm-pipeline co-design", conditional softmax
+        // rescaling) and is driven by requests: the softmax warps of its quarter post, in the
+        // quarter's slot, either "tile s is finished" (once per Q tile) or, in the rare step
+        // where they raise their rows' maxima by more than the threshold, "rescale O_s". For
+        // the latter the softmax warp publishes its factors and goes on with its exponentials,
+        // and this warp rescales the quarter's rows of O_s in TMEM meanwhile, then passes the
+        // softmax warp's "P stage 1 written" (bPStage) on to the MMA warp (bPFull), so the next
+        // O += P V starts on the rescaled accumulator. The warp sleeps on one barrier (bReq)
+        // and is woken only by requests; the MMA warp never waits for it otherwise.
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegEpi));
-        const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        uint32_t of[2] = {0, 0}, sp[2] = {0, 0};
-        uint32_t ap = 0, pst = 0;      // bit s: parity of the next phase of this quarter's bAlpha / bPStage of tile s
-        uint32_t stage = 0, v8ph = 0;  // 8-bit inputs: ring slot and per-slot phase bits of bV8Full
-        bool ok = true;
-        // The report of tile s's next step; in a rescaling step O_s of this quarter's rows times
-        // the published factors, then the first P stage on to the MMA warp.
-        auto step = [&](int s) -> bool {
-            if (!warp_wait(&bars[L::bAlpha + 4 * s + quarter], (ap >> s) & 1u, abort_flag, wd)) return false;
-            ap ^= 1u << s;
-            if (!st_f[4 * s + quarter]) return true;
-            tc_fence_after();
-            const float a = st_a[s * BM + row];
-            const uint32_t tO = tmem + lane_off + (s ? kColO1 : kColO0);
-#pragma unroll 1
-            for (int c = 0; c < DV; c += 16) {
-                uint32_t o[16];
-                tmem_ld16(tO + c, o);
-                tc_wait_ld();
-                reg_fence(o);
+        if constexpr (CORR != 0) {
+            static_assert(F8 == 0, "the correction role is built for 16-bit inputs");
+            const int quarter = warp & 3;
+            const int row = quarter * 32 + lane;
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            volatile int* slot = st_req + quarter;
+            uint32_t rq = 0, pst = 0;  // pst bit s: next phase parity of bPStage of tile s
+            uint32_t of0 = 0, of1 = 0;  // per Q tile: next phase parity of bOFull
+            int cur0 = 0, cur1 = 0;     // per Q tile: next round of the schedule to write out
+            bool ok = true;
+            // Write O / l and the LSE of Q tile s of the next work tile that has keys for it;
+            // rows of work tiles without keys for it on the way get O = 0, LSE = -inf. With
+            // `finish`, only those rows are written, up to the end of the schedule.
+            auto write_out = [&](const int s, int& cur, uint32_t& of, bool finish) -> bool {
+                for (; cur * (int)gridDim.x < total; ++cur) {
+                    const int w = snake_index(cur);
+                    if (w >= total) continue;
+                    Tile t;
+                    get_tile<BN>(p, po, w, t);
+                    const int qrow = t.r0 + s * BM + row;
+                    if (t.r0 + s * BM >= t.Lq) continue;
+                    const bool valid = qrow < t.Lq;
+                    const long long tok = (long long)t.q0 + qrow;
+                    __nv_bfloat16* orow = p.o + (tok * p.Hq + t.h) * DV;
+                    if (t.n[s] == 0) {
+                        if (valid) {
+                            const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
-                tmem_st16(tO + c, o);
-            }
-            tc_wait_st();
-            if (!warp_wait(&bars[L::bPStage + 4 * s + quarter], (pst >> s) & 1u, abort_flag, wd)) return false;
-            pst ^= 1u << s;
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[L::bPFull + s]);
-            return true;
-        };
-        for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
-            const int w = snake_index(r);
-            if (w >= total) continue;
-            Tile t;
-            get_tile<BN>(p, po, w, t);
-            const int nmax = max(t.n[0], t.n[1]);
-            if (nmax > 0) {
-                // Per step e: with 8-bit inputs the widening of the V tile of ring entry e + 1
-                // (rows 32*quarter .. +31, in ring order; the MMA warps wait for it (bVConv)
-                // before each P V product and only then release the entry, so the 8-bit tile is
-                // never overwritten while read here), then the step reports of tiles 0 and 1.
-                if constexpr (F8 != 0) {
-                    if (++stage == (uint32_t)L::kEntries) stage = 0;  // entry 0 carries no V
+                            for (int c = 0; c < DV / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+                            p.lse[tok * p.Hq + t.h] = -INFINITY;
+                        }
+                        continue;
+                    }
+                    if (finish) return false;  // a finished tile nobody reported: a timeout elsewhere
+                    ++cur;
+                    if (!warp_wait(&bars[L::bOFull + s], of, abort_flag, wd)) return false;
+                    of ^= 1u;
+                    tc_fence_after();
+                    const float m = st_m[s * BM + row];
+                    const float l = st_l[s * BM + row];
+                    const float inv = l > 0.0f ? p.out_scale / l : 0.0f;
+                    const uint32_t tO = tmem + lane_off + (s ? kColO1 : kColO0);
+#pragma unroll 1
+                    for (int c = 0; c < DV; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c, o);
+                        tc_wait_ld();
+                        reg_fence(o);
+                        if (valid) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+                            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[L::bOEmpty + s]);
+                    if (valid) p.lse[tok * p.Hq + t.h] = l > 0.0f ? m * p.scale + logf(l) : -INFINITY;
+                    return true;
                 }
-                for (int e = 0; e < nmax && ok; ++e) {
-                    if constexpr (F8 != 0) {
+                return finish;
+            };
+            // tiles this warp will be told about: one per Q tile with keys
+            int pending = 0;
+            for (int r = 0; r * (int)gridDim.x < total; ++r) {
+                const int w = snake_index(r);
+                if (w >= total) continue;
+                Tile t;
+                get_tile<BN>(p, po, w, t);
+                pending += (t.n[0] > 0) + (t.n[1] > 0);
+            }
+            while (pending > 0 && ok) {
+                if (!(ok = warp_wait(&bars[L::bReq + quarter], rq, abort_flag, wd))) break;
+                rq ^= 1u;
+                const int req = *slot;
+                __syncwarp();
+                if (lane == 0) *slot = 0;  // read: the slot may take the next request
+                if (req >= kReqEpilogue) {
+                    ok = req == kReqEpilogue ? write_out(0, cur0, of0, false) : write_out(1, cur1, of1, false);
+                    --pending;
+                } else {
+                    // O_s of this quarter's rows times the published factors, then the softmax
+                    // warp's first P stage on to the MMA warp
+                    const int s = req - kReqRescale;
+                    tc_fence_after();
+                    const float a = st_a[s * BM + row];
+                    const uint32_t tO = tmem + lane_off + (s ? kColO1 : kColO0);
+#pragma unroll 1
+                    for (int c = 0; c < DV; c += 16) {
+                        uint32_t o[16];
+                        tmem_ld16(tO + c, o);
+                        tc_wait_ld();
+                        reg_fence(o);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+                        tmem_st16(tO + c, o);
+                    }
+                    tc_wait_st();
+                    if (!(ok = warp_wait(&bars[L::bPStage + 4 * s + quarter], (pst >> s) & 1u, abort_flag, wd))) break;
+                    pst ^= 1u << s;
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[L::bPFull + s]);
+                }
+            }
+            if (ok) {
+                write_out(0, cur0, of0, true);
+                write_out(1, cur1, of1, true);
+            }
+        } else {
+            const int quarter = warp & 3;
+            const int row = quarter * 32 + lane;
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            uint32_t of[2] = {0, 0}, sp[2] = {0, 0};
+            uint32_t stage = 0, v8ph = 0;  // 8-bit inputs: ring slot and per-slot phase bits of bV8Full
+            bool ok = true;
+            for (int r = 0; r * (int)gridDim.x < total && ok; ++r) {
+                const int w = snake_index(r);
+                if (w >= total) continue;
+                Tile t;
+                get_tile<BN>(p, po, w, t);
+                if constexpr (F8 != 0) {
+                    // Widen this tile's 8-bit V tiles first (rows 32*quarter .. +31 of each), in ring
+                    // order. The MMA warps wait for them (bVConv) before each P V product and only
+                    // then release the entry, so the 8-bit tile is never overwritten while read here.
+                    const int nmax = max(t.n[0], t.n[1]);
+                    for (int e = 0; e <= nmax && nmax > 0 && ok; ++e) {
                         const uint32_t e_slot = stage;
                         if (++stage == (uint32_t)L::kEntries) stage = 0;
+                        if (e == 0) continue;
                         if (!(ok = warp_wait(&bars[L::bV8Full + e_slot], (v8ph >> e_slot) & 1u, abort_flag, wd))) break;
                         v8ph ^= 1u << e_slot;
                         const uint32_t ent = smem_u32(smem + L::kKVOff) + e_slot * L::kEntryBytes;
@@ -1108,57 +1208,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars[L::bVConv + e_slot]);
                     }
-                    if (CORR != 0 && e >= 1) {
-                        if (e < t.n[0] && !(ok = step(0))) break;
-                        if (e < t.n[1] && !(ok = step(1))) break;
-                    }
+                    if (!ok) break;
                 }
-                if (!ok) break;
-            }
-            for (int s = 0; s < 2; ++s) {
-                const int qrow = t.r0 + s * BM + row;
-                if (t.r0 + s * BM >= t.Lq) continue;
-                const bool valid = qrow < t.Lq;
-                const long long tok = (long long)t.q0 + qrow;
-                __nv_bfloat16* orow = p.o + (tok * p.Hq + t.h) * DV;
-                if (t.n[s] == 0) {
-                    if (valid) {
-                        uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-                        for (int c = 0; c < DV / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
-                        p.lse[tok * p.Hq + t.h] = -INFINITY;
+                for (int s = 0; s < 2; ++s) {
+                    const int qrow = t.r0 + s * BM + row;
+                    if (t.r0 + s * BM >= t.Lq) continue;
+                    const bool valid = qrow < t.Lq;
+                    const long long tok = (long long)t.q0 + qrow;
+                    __nv_bfloat16* orow = p.o + (tok * p.Hq + t.h) * DV;
+                    if (t.n[s] == 0) {
+                        if (valid) {
+                            uint4 z = make_uint4(0, 0, 0, 0);
+    #pragma unroll
+                            for (int c = 0; c < DV / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+                            p.lse[tok * p.Hq + t.h] = -INFINITY;
+                        }
+                        continue;
                     }
-                    continue;
-                }
-                if (!warp_wait(&bars[L::bOFull + s], of[s], abort_flag, wd)) { ok = false; break; }
-                of[s] ^= 1u;
-                if (!warp_wait(&bars[L::bStats + s], sp[s], abort_flag, wd)) { ok = false; break; }
-                sp[s] ^= 1u;
-                tc_fence_after();
-                const float m = st_m[s * BM + row];
-                const float l = st_l[s * BM + row];
-                const float inv = l > 0.0f ? p.out_scale / l : 0.0f;
-                const uint32_t tO = tmem + lane_off + (s ? kColO1 : kColO0);
-#pragma unroll 1
-                for (int c = 0; c < DV; c += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c, o);
-                    tc_wait_ld();
-                    reg_fence(o);
-                    if (valid) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-                        uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    if (!warp_wait(&bars[L::bOFull + s], of[s], abort_flag, wd)) { ok = false; break; }
+                    of[s] ^= 1u;
+                    if (!warp_wait(&bars[L::bStats + s], sp[s], abort_flag, wd)) { ok = false; break; }
+                    sp[s] ^= 1u;
+                    tc_fence_after();
+                    const float m = st_m[s * BM + row];
+                    const float l = st_l[s * BM + row];
+                    const float inv = l > 0.0f ? p.out_scale / l : 0.0f;
+                    const uint32_t tO = tmem + lane_off + (s ? kColO1 : kColO0);
+    #pragma unroll 1
+                    for (int c = 0; c < DV; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c, o);
+                        tc_wait_ld();
+                        reg_fence(o);
+                        if (valid) {
+                            uint32_t pk[16];
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+                            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+    #pragma unroll
+                            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        }
                     }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[L::bOEmpty + s]);
+                    if (valid) p.lse[tok * p.Hq + t.h] = l > 0.0f ? m * p.scale + logf(l) : -INFINITY;
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[L::bOEmpty + s]);
-                if (valid) p.lse[tok * p.Hq + t.h] = l > 0.0f ? m * p.scale + logf(l) : -INFINITY;
             }
         }
     }
