@@ -32,6 +32,7 @@ struct Options {
     int packed_order = 1;
     int correction = 0;
     int unroll_kv = 0;
+    int dynamic_order = 1;
 };
 
 std::mutex g_mu;
@@ -112,6 +113,26 @@ Options options() {
 
 int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
 
+// The library's stream-ordered memory pool on the current device (created on first use; it
+// keeps what it has reserved, so later calls take their memory without the driver).
+attn_status_t device_pool(DeviceState* ds, cudaMemPool_t* out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!ds->pool) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+        cudaMemPoolProps props;
+        memset(&props, 0, sizeof props);
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        if (cudaMemPoolCreate(&ds->pool, &props) != cudaSuccess) return ATTN_ERR_CUDA;
+        uint64_t keep = UINT64_MAX;
+        cudaMemPoolSetAttribute(ds->pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    }
+    *out = ds->pool;
+    return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -165,6 +186,9 @@ attn_status_t attn_set_option(const char* name, double value) {
     } else if (!strcmp(name, "unroll_kv")) {
         if (value != 0 && value != 1) return ATTN_ERR_BAD_ARG;
         g_opt.unroll_kv = (int)value;
+    } else if (!strcmp(name, "dynamic_order")) {
+        if (value != 0 && value != 1) return ATTN_ERR_BAD_ARG;
+        g_opt.dynamic_order = (int)value;
     } else {
         return ATTN_ERR_BAD_ARG;
     }
@@ -183,6 +207,7 @@ attn_status_t attn_get_option(const char* name, double* value) {
     else if (!strcmp(name, "packed_order")) *value = g_opt.packed_order;
     else if (!strcmp(name, "correction")) *value = g_opt.correction;
     else if (!strcmp(name, "unroll_kv")) *value = g_opt.unroll_kv;
+    else if (!strcmp(name, "dynamic_order")) *value = g_opt.dynamic_order;
     else return ATTN_ERR_BAD_ARG;
     return ATTN_OK;
 }
@@ -254,8 +279,15 @@ static attn_status_t fwd(const void* q, const void* k, const void* v, void* o, f
         // Section of (batch, head) pairs: all of them unless the tiles make 16 or more waves
         // of the grid; then sections of at least 8 waves each, which keeps the heaviest-first
         // order balanced within a section while fewer key/value heads share the L2.
+        // Head width 256 with the dynamic order: the CTAs take units in order as they become
+        // free, so balance needs no long sections. Measured on the long causal geometry
+        // (B1 H32 N8192): 4-head sections bring DRAM reads to the algorithmic bytes but no
+        // time (the kernel is bounded by shared-memory traffic, not DRAM); 16 heads were the
+        // fastest and still halve the DRAM traffic of the static order.
+        const bool dyn = d == 256 && opt.dynamic_order;
         long long sec = pairs;
         if (opt.sec_heads > 0) sec = opt.sec_heads;
+        else if (dyn) sec = 16;
         else if (nblk > 0 && tiles >= 16LL * grid) sec = cdiv(8LL * grid, nblk);
         sec = ((sec + p.G - 1) / p.G) * p.G;
         if (sec > pairs) sec = pairs;
@@ -272,13 +304,30 @@ static attn_status_t fwd(const void* q, const void* k, const void* v, void* o, f
     }
     if (grid <= 0) return ATTN_OK;
     const cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+    // Head width 256, dynamic order: a unit counter per call, from the library's stream-ordered
+    // pool, zeroed on the call's stream before every launch (so concurrent calls on other
+    // streams never share one) and returned after the last.
+    unsigned int* sched = nullptr;
+    if (d == 256 && opt.dynamic_order) {
+        cudaMemPool_t pool = nullptr;
+        if ((st = device_pool(ds, &pool)) != ATTN_OK) return st;
+        if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&sched), 2 * sizeof(unsigned int), pool, st_) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
     auto launch = [&](const FwdParams& lp) {
-        return fp8 >= 0   ? attn::launch_attn_fwd_fp8(tm, lp, d, fp8, grid, st_)
-               : d != dv  ? attn::launch_attn_fwd_hd(tm, lp, d, dv, grid, st_)
-               : d == 256 ? attn::launch_attn_fwd_wide(tm, lp, grid, st_)
-                          : attn::launch_attn_fwd(tm, lp, d, opt.exp_poly, grid, st_);
+        if (sched && cudaMemsetAsync(sched, 0, 2 * sizeof(unsigned int), st_) != cudaSuccess) return cudaErrorUnknown;
+        FwdParams q = lp;
+        q.sched = sched;
+        return fp8 >= 0   ? attn::launch_attn_fwd_fp8(tm, q, d, fp8, grid, st_)
+               : d != dv  ? attn::launch_attn_fwd_hd(tm, q, d, dv, grid, st_)
+               : d == 256 ? attn::launch_attn_fwd_wide(tm, q, grid, st_)
+                          : attn::launch_attn_fwd(tm, q, d, opt.exp_poly, grid, st_);
     };
-    if (!cu_seqlens) return launch(p) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    auto done = [&](attn_status_t r) {
+        if (sched && cudaFreeAsync(sched, st_) != cudaSuccess && r == ATTN_OK) r = ATTN_ERR_CUDA;
+        return r;
+    };
+    if (!cu_seqlens) return done(launch(p) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA);
     // Packed sequences: one launch builds its work order in shared memory for at most maxB
     // sequences, so a larger batch runs as consecutive launches of maxB sequences each (the
     // offsets in cu_seqlens are absolute rows of q/k, so a launch only needs its slice of them).
@@ -287,9 +336,9 @@ static attn_status_t fwd(const void* q, const void* k, const void* v, void* o, f
         FwdParams lp = p;
         lp.cu_seqlens = cu_seqlens + b0;
         lp.B = B - b0 < maxB ? B - b0 : maxB;
-        if (launch(lp) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (launch(lp) != cudaSuccess) return done(ATTN_ERR_CUDA);
     }
-    return ATTN_OK;
+    return done(ATTN_OK);
 }
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
@@ -404,23 +453,10 @@ static attn_status_t decode_paged(const void* q, const void* k_cache, const void
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     void* ws = nullptr;
     if (max_splits > 1) {
-        {
-            std::lock_guard<std::mutex> lk(g_mu);
-            if (!ds->pool) {
-                int dev = 0;
-                if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-                cudaMemPoolProps props;
-                memset(&props, 0, sizeof props);
-                props.allocType = cudaMemAllocationTypePinned;
-                props.location.type = cudaMemLocationTypeDevice;
-                props.location.id = dev;
-                if (cudaMemPoolCreate(&ds->pool, &props) != cudaSuccess) return ATTN_ERR_CUDA;
-                uint64_t keep = UINT64_MAX;
-                cudaMemPoolSetAttribute(ds->pool, cudaMemPoolAttrReleaseThreshold, &keep);
-            }
-        }
+        cudaMemPool_t pool = nullptr;
+        if ((st = device_pool(ds, &pool)) != ATTN_OK) return st;
         const size_t n_o = (size_t)B * Hq * max_splits * d;
-        if (cudaMallocFromPoolAsync(&ws, attn_decode_workspace_bytes(B, Hq, d, max_splits), ds->pool, s) != cudaSuccess)
+        if (cudaMallocFromPoolAsync(&ws, attn_decode_workspace_bytes(B, Hq, d, max_splits), pool, s) != cudaSuccess)
             return ATTN_ERR_CUDA;
         p.ws_o = reinterpret_cast<float*>(ws);
         p.ws_lse = p.ws_o + n_o;

@@ -1308,12 +1308,15 @@ struct LayoutWide {
     // warp reads either, so P's barriers are per buffer like S's (one phase per use of a buffer).
     static constexpr int bQFull = 0, bQEmpty = 1, bSlot = 2, bSFull = bSlot + kSlots, bPFull = bSFull + 2,
                          bPRest = bPFull + 2, bVDone = bPRest + 2, bOFull = bVDone + 1, bDrain = bOFull + 1;
-    static constexpr int kNumBars = bDrain + 1;
+    // dynamic unit order: [2] a unit index is in the slot / every consumer has read it
+    static constexpr int bUFull = bDrain + 1, bUEmpty = bUFull + 2;
+    static constexpr int kNumBars = bUEmpty + 2;
     static constexpr int kMiscOff = kBarOff + ((kNumBars * 8 + 15) / 16) * 16;
+    // misc: tmem base, abort flag, packed-order levels, work tiles, two unit slots
     // packed-sequence order tables (small: the tiles leave about 2 KB)
     static constexpr int kMaxB = 64;
     static constexpr int kMaxLv = 192;
-    static constexpr int kPreOff = kMiscOff + 16;
+    static constexpr int kPreOff = kMiscOff + 32;
     static constexpr int kLvlOff = kPreOff + ((kMaxB + 1) * 4 + 15) / 16 * 16;
     static constexpr int kPermOff = kLvlOff + ((kMaxLv + 2) * 4 + 15) / 16 * 16;
     static constexpr int kNbOff = kPermOff + kMaxB * 4;
@@ -1410,6 +1413,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         mbar_init(&bars[L::bVDone], 1);
         mbar_init(&bars[L::bOFull], 1);
         mbar_init(&bars[L::bDrain], 1);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&bars[L::bUFull + k], 1);
+            mbar_init(&bars[L::bUEmpty + k], 5);  // the MMA warp and the four softmax warps
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1438,6 +1445,40 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if (p.cu_seqlens) total = misc[3];
     const uint32_t tmem = *tmem_slot;
     const uint64_t wd = p.watchdog_ns;
+    // Units (128-row Q tiles) this CTA works on, the k-th one per call. Static order: the snake
+    // over rounds of the grid. Dynamic order (p.sched, a zeroed counter per call): the warp 0
+    // takes the next unit of the order from the counter when it is ready for one and passes it
+    // to the MMA and softmax warps through two shared-memory slots, so CTAs that finish early
+    // take more units and all CTAs work on neighbouring units (the same few heads) at any time.
+    // Returns false when no unit is left, or on a timeout (then ok = false); u = -1 for a round
+    // without a unit.
+    const int units = 2 * total;
+    volatile int* uslot = misc + 4;
+    auto next_unit = [&](int k, int& u, bool producer, bool& ok) -> bool {
+        if (!p.sched) {
+            if (k * (int)gridDim.x >= units) return false;
+            u = snake_index(k);
+            if (u >= units) u = -1;
+            return true;
+        }
+        const int sl = k & 1;
+        if (producer) {
+            if (k >= 2 && !(ok = warp_wait(&bars[L::bUEmpty + sl], ((k >> 1) & 1) ^ 1, abort_flag, wd))) return false;
+            int v = 0;
+            if (lane == 0) {
+                v = (int)atomicAdd(p.sched, 1u);
+                uslot[sl] = v;
+                mbar_arrive(&bars[L::bUFull + sl]);
+            }
+            u = __shfl_sync(0xffffffffu, v, 0);
+        } else {
+            if (!(ok = warp_wait(&bars[L::bUFull + sl], (k >> 1) & 1, abort_flag, wd))) return false;
+            u = uslot[sl];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[L::bUEmpty + sl]);
+        }
+        return u < units;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
@@ -1447,9 +1488,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         uint32_t n_pv = 0, n_s0 = 0, n_s1 = 0;  // products assigned so far: O += P V steps, S per buffer
         long long item = 0;
         bool ok = true;
-        for (int r = 0; r * (int)gridDim.x < 2 * total && ok; ++r) {
-            const int u = snake_index(r);
-            if (u >= 2 * total) continue;
+        for (int k = 0; ok; ++k) {
+            int u;
+            if (!next_unit(k, u, true, ok)) break;
+            if (u < 0) continue;
             Tile t;
             get_tile<BN>(p, po, u >> 1, t);
             {
@@ -1546,9 +1588,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             }
             return true;
         };
-        for (int r = 0; r * (int)gridDim.x < 2 * total && ok; ++r) {
-            const int u = snake_index(r);
-            if (u >= 2 * total) continue;
+        for (int k = 0; ok; ++k) {
+            int u;
+            if (!next_unit(k, u, false, ok)) break;
+            if (u < 0) continue;
             Tile t;
             get_tile<BN>(p, po, u >> 1, t);
             {
@@ -1633,9 +1676,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         uint32_t sf = 0, of = 0, pv_done = 0;  // sf bit b: S buffer b parity; pv_done: O += P V steps before this tile
         unsigned long long c_dec = 0, c_res = 0, c_dec1 = 0, c_ores = 0;
         bool ok = true;
-        for (int r = 0; r * (int)gridDim.x < 2 * total && ok; ++r) {
-            const int u = snake_index(r);
-            if (u >= 2 * total) continue;
+        for (int k = 0; ok; ++k) {
+            int u;
+            if (!next_unit(k, u, false, ok)) break;
+            if (u < 0) continue;
             Tile t;
             get_tile<BN>(p, po, u >> 1, t);
             {

@@ -50,9 +50,11 @@ struct FwdParams {
     int sec_q;          // scheduling section, a multiple of G: dense, (batch, head) pairs; packed, query heads (divides Hq)
     int total_tiles;    // dense: number of work tiles; varlen: ignored (computed on device)
     int packed_plain;   // packed sequences: 1 = sequences in the caller's order (no heaviest-first sort)
-    int corr_warp;      // 1: O is rescaled by the correction role (epilogue warps); 0: by the softmax warps
+    int corr_warp;      // 1: O is rescaled by the correction role (epilogue warps; a separate instantiation,
+                        // bf16 at d = 128); 0: by the softmax warps
     int unroll_kv;      // 1: the last P V product of a work tile and the first S = Q K^T of the next share a
                         // burst (a separate instantiation, for bf16 and e4m3 inputs at d = 128)
+    unsigned int* sched;  // head width 256: zeroed unit counter of this launch (dynamic order), or nullptr
     int* status;
     unsigned long long* counters;  // nullptr unless counting is enabled
     unsigned long long watchdog_ns;

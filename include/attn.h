@@ -73,7 +73,10 @@ typedef int attn_status_t;
  *           a sequence reaching past Nq or Nk is treated as empty and recorded as
  *           ATTN_ERR_DEVICE_BAD_INDEX)
  * d         head dimension, 64, 128 or 256 (256: one 128-row query tile per CTA at a time,
- *           key/value tiles streamed in 128-column halves)
+ *           key/value tiles streamed in 128-column halves; the CTAs take query tiles from a
+ *           counter as they become free, and the call takes that 8-byte counter from the
+ *           library's stream-ordered pool on `stream`, zeroes it there and returns it there,
+ *           so calls on different streams never share one)
  * scale     multiplier of q.k (typically 1/sqrt(d)); must be finite
  * causal    0: every key is visible. 1: bottom-right aligned mask, key j visible to query
  *           row i of its sequence iff j <= i + (Nk - Nq). Rows that see no key get o = 0
@@ -253,6 +256,17 @@ attn_status_t attn_get_device_status(void* stream);
  *                        waves of the grid); packed sequences, query heads per section
  *   "count"              1: count softmax rescale decisions and exponentials (attn_read_counters)
  *   "watchdog_ms"        device wait limit before a kernel gives up (default 4000)
+ *   "dynamic_order"      head width 256: 1 (default) CTAs take query tiles from a counter in
+ *                        the order of head sections (16 heads unless "sec_heads" says
+ *                        otherwise), heaviest blocks first within each, so that the running
+ *                        CTAs share key/value tiles in the L2 ("FlashAttention4 精读" section
+ *                        3.3, L2-sized sections with LPT); 0 the static order of the other widths
+ *   "correction"         1: the rescale of O is done by a separate correction warp per TMEM lane
+ *                        quarter ("FlashAttention4 精读" section 3.1), bf16 at d = 128 only;
+ *                        0 (default): by the softmax warp itself, in the rare steps that need it
+ *   "unroll_kv"          1: the last O += P V of a work tile and the first S = Q K^T of the next
+ *                        are issued as one burst ("Low-precision FA4" section 2.1.2), bf16 and
+ *                        e4m3 at d = 128; 0 (default): separate bursts
  *   "packed_order"       packed sequences: 1 (default) orders work heaviest first across all
  *                        sequences ("FlashAttention4 精读" section 3.3, LPT for varlen);
  *                        0 keeps the sequences in the caller's order (each sequence's

@@ -122,3 +122,45 @@ def test_d256_varlen_several_launches(A):
     """150 packed sequences at d = 256: three launches of at most 64 sequences."""
     rng = np.random.default_rng(97)
     check(A, case("varlen150", 0, 2, 1, 0, 0, False, 98, lens=[int(x) for x in rng.integers(1, 300, size=150)]))
+
+
+def test_d256_static_order_matches(A):
+    """The static snake order (dynamic_order = 0) and the dynamic unit counter give the same
+    result up to rounding on a ragged, masked, GQA and a packed case."""
+    A.attn_set_option("dynamic_order", 0)
+    try:
+        check(A, case("static_ragged", 2, 4, 1, 333, 333, True, 99))
+        check(A, case("static_varlen", 0, 4, 2, 0, 0, True, 100, lens=[1, 129, 0, 256, 257, 5, 600]))
+    finally:
+        A.attn_set_option("dynamic_order", 1)
+
+
+def test_d256_calls_on_two_streams_at_once(A):
+    """Calls running at the same time on two streams each take their own unit counter: both
+    results equal the ones of calls made one after the other."""
+    cs = [case("s1", 1, 8, 2, 1500, 1500, True, 101), case("s2", 2, 4, 4, 900, 900, False, 102)]
+    ins = [[to_dev(a, DEV) for a in c.generate()] for c in cs]
+    outs = [(torch.empty((c.total_q, c.Hq, D), dtype=torch.bfloat16, device=DEV),
+             torch.empty((c.total_q, c.Hq), dtype=torch.float32, device=DEV)) for c in cs]
+
+    def call(i, stream):
+        c = cs[i]
+        A.attn_fwd(*ins[i], *outs[i], c.B, c.Hq, c.Hkv, c.Nq, c.Nk, D, c.scale, c.causal, None, stream)
+
+    call(0, None)
+    call(1, None)
+    torch.cuda.synchronize()
+    ref = [(o.clone(), l.clone()) for o, l in outs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for _ in range(3):
+        for o, l in outs:
+            o.fill_(float("nan"))
+            l.fill_(float("nan"))
+        torch.cuda.synchronize()
+        for _ in range(4):  # several calls queued on each stream, interleaved
+            call(0, streams[0])
+            call(1, streams[1])
+        torch.cuda.synchronize()
+        assert A.attn_get_device_status() == 0
+        for (o, l), (ro, rl) in zip(outs, ref):
+            assert torch.equal(o, ro) and torch.equal(l, rl)
