@@ -52,6 +52,35 @@ FWDHD_KERNEL = "attn_fwd_kernel<192, 0, 0, 128, 96>"
 FWDW_KERNEL = "attn_fwd_wide_kernel"
 
 
+# Reduced cases for profiler captures: inputs larger than the L2, a few GB at most on the device.
+PROFILE_CASES = {
+    "long_causal_h16": lambda: W.PrefillCase("long_causal_h16", 1, 16, 16, 8192, 8192, 128, 1.0 / math.sqrt(128),
+                                             True, W.long_causal().seed, 2.0),
+    "long_causal_h32": W.long_causal,
+    "long_causal_d256": lambda: W.PrefillCase("long_causal_d256", 1, 32, 32, 8192, 8192, 256, 1.0 / 16.0, True,
+                                              W.long_causal().seed, 2.0),
+}
+
+
+def run_profile_case(name):
+    """attn_fwd four times on one case (the fourth launch is the one to capture)."""
+    import torch
+    import exact_softmax_attention_gb300 as A
+    c = PROFILE_CASES[name]()
+    q, k, v = c.generate()
+    dev = lambda a: torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    Q, K, V = dev(q), dev(k), dev(v)
+    O = torch.empty((c.total_q, c.Hq, c.d), dtype=torch.bfloat16, device="cuda")
+    L = torch.empty((c.total_q, c.Hq), dtype=torch.float32, device="cuda")
+    for _ in range(4):
+        A.attn_fwd(Q, K, V, O, L, c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d, c.scale, c.causal)
+    torch.cuda.synchronize()
+    st = A.attn_get_device_status()
+    if st != 0:
+        raise RuntimeError(A.status_string(st))
+    print(json.dumps({"profile_case": name, "flops_per_call": c.flops()}))
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -62,6 +91,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
                     help="library tuning option (attn_set_option) applied before timing; repeatable")
+    ap.add_argument("--profile-case", default=None, choices=sorted(PROFILE_CASES),
+                    help="run one named workload four times and exit (for ncu captures of one launch)")
     ap.add_argument("--legs", default="all",
                     help="comma-separated legs to run besides the step (decode_fp8, prefill_fp8, prefill_hd, "
                          "prefill_d256, prefill_tiny, prefill_2k, prefill_2k_causal, prefill_varlen_gqa, rescale), "
@@ -83,32 +114,29 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-KERNEL_SOURCES = {FWD_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"],
-                  DEC_KERNEL: ["attn_decode.cu", "ptx.cuh", "kernels.cuh"],
-                  DEC8_KERNEL: ["attn_decode.cu", "ptx.cuh", "kernels.cuh"],
-                  FWD8_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"],
-                  FWDHD_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"],
-                  FWDW_KERNEL: ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"]}
+def kernel_sources(kernel: str):
+    """The source files a kernel is compiled from."""
+    return ["attn_decode.cu" if kernel.startswith("decode") else "attn_fwd.cu", "ptx.cuh", "kernels.cuh"]
 
 
 def source_sha(kernel: str) -> str:
     """Hash of the sources a kernel is compiled from (to tell whether a profile is stale)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_softmax_attention_gb300", "csrc")
-    for name in KERNEL_SOURCES[kernel]:
+    for name in kernel_sources(kernel):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str):
-    """Per-launch DRAM bytes of ``kernel`` from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+def ncu_traffic(leg: str):
+    """Per-launch DRAM bytes of the kernel of a bench leg (``step_prefill``, ``step_decode``, or
+    the leg's key in the JSON line) from the committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
-            t = json.load(f)
-        e = t[kernel]
-        return float(e["dram_bytes_per_launch"]) if e.get("source_sha") == source_sha(kernel) else None
+            e = json.load(f)[leg]
+        return float(e["dram_bytes_per_launch"]) if e.get("source_sha") == source_sha(e["kernel"]) else None
     except (OSError, KeyError, ValueError):
         return None
 
@@ -367,7 +395,7 @@ def tensor_leg(name, workload, flops, ms, calls, launches, peak, peak_source, ke
     leg = {"value": world * ach, "unit": "TFLOP/s", "ms_per_call": ms, "calls": calls, "gpu_launches": launches,
            "workload": workload, "flops_per_call": flops,
            "roofline": {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
-                        "traffic": ncu_traffic(kernel) if kernel in KERNEL_SOURCES else None, "kernel": kernel,
+                        "traffic": ncu_traffic(name), "kernel": kernel,
                         "peak_source": peak_source}}
     if extra:
         leg.update(extra)
@@ -495,7 +523,7 @@ def run_ours(args):
             "workload": "paged decode as above with e4m3 key/value caches (per-tensor descales)",
             "bytes_per_call": dc8.bytes(), "speedup_vs_bf16_decode": (dec_ms / K_) / ms,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                         "traffic": ncu_traffic(DEC8_KERNEL), "kernel": DEC8_KERNEL, "peak_source": f"{src} copy"}}
+                         "traffic": ncu_traffic("decode_fp8"), "kernel": DEC8_KERNEL, "peak_source": f"{src} copy"}}
         del KC8, VC8
 
     if want("prefill_fp8"):
@@ -660,10 +688,10 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
                    "decode_splits_max": max_splits, "forward_options": opts},
         "roofline": {"bound": "tensor", "achieved": f_ach, "peak": bf16, "unit": "TFLOP/s", "frac": f_ach / bf16,
-                     "traffic": ncu_traffic(FWD_KERNEL), "kernel": FWD_KERNEL, "peak_source": f"{src} bf16 burst"},
+                     "traffic": ncu_traffic("step_prefill"), "kernel": FWD_KERNEL, "peak_source": f"{src} bf16 burst"},
         "decode": {"value": dvalue, "unit": "GB/s", "ms_per_step": dec_ms / K_,
                    "roofline": {"bound": "hbm", "achieved": d_ach, "peak": hbm, "unit": "GB/s", "frac": d_ach / hbm,
-                                "traffic": ncu_traffic(DEC_KERNEL), "kernel": DEC_KERNEL,
+                                "traffic": ncu_traffic("step_decode"), "kernel": DEC_KERNEL,
                                 "peak_source": f"{src} copy"}},
         "prefill_ms_per_step": fwd_ms / K_,
         "gpu_launches": K_ * launches_per_step,
@@ -775,7 +803,9 @@ def run_e2e(torch, A, dev, stream, barrier, world, steps, fc, dc, fin, din, fdev
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
