@@ -95,8 +95,8 @@ def parse():
                     help="run one named workload four times and exit (for ncu captures of one launch)")
     ap.add_argument("--legs", default="all",
                     help="comma-separated legs to run besides the step (decode_fp8, prefill_fp8, prefill_hd, "
-                         "prefill_d256, prefill_tiny, prefill_2k, prefill_2k_causal, prefill_varlen_gqa, rescale), "
-                         "'all' or 'none'")
+                         "prefill_d256, prefill_tiny, prefill_2k, prefill_2k_causal, prefill_varlen_gqa, "
+                         "prefill_correction_warp, prefill_unroll_kv, rescale), 'all' or 'none'")
     return ap.parse_args()
 
 
@@ -631,6 +631,24 @@ def run_ours(args):
                                  lx)[1]
         del CQ, CK, CV, CO, CL
     del flush_buf
+
+    # the two measured design alternatives of the long causal forward, each as its own leg:
+    # the correction warp (option correction = 1) and unroll-KV (option unroll_kv = 1)
+    for name, opt, desc in (("prefill_correction_warp", "correction",
+                             "long causal prefill as the step, O rescaled by a request-driven correction warp"),
+                            ("prefill_unroll_kv", "unroll_kv",
+                             "long causal prefill as the step, last P V of a work tile and first S of the next "
+                             "in one burst")):
+        if not want(name):
+            continue
+        before = A.attn_get_option(opt)
+        A.attn_set_option(opt, 1)
+        try:
+            ms = mx(timer.per_call_ms(fwd, K_, args.warmup, f"the {name} leg"))
+        finally:
+            A.attn_set_option(opt, before)
+        extra[name] = tensor_leg(name, desc, fc.flops(), ms, K_, K_, bf16, f"{src} bf16 burst", FWD_KERNEL, world,
+                                 {"vs_default_step": (fwd_ms / K_) / ms})[1]
 
     # ---------------------------------------------------------------- rescale rate (untimed)
     if want("rescale"):
