@@ -390,10 +390,19 @@ __device__ __forceinline__ void lds64(uint32_t addr, uint32_t* w) {
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(addr) : "memory");
 }
 
-template <int D, int GN, int NST, int FMT>
-// Four CTAs per SM (48 KB of rings each): at most 128 registers per thread.
-__global__ void __launch_bounds__(kWarps * 32, 4) decode_split_fp8_kernel(const DecodeParams p) {
-    constexpr int kTile = kGroup * D;   // bytes of one K or V warp-stage tile
+// TG tokens per warp-stage (16 or 32). Launch bound: as many CTAs per SM as their rings fit in
+// shared memory, at most four.
+template <int D, int TG, int NST>
+constexpr int fp8_min_blocks() {
+    return (232448 / (kWarps * NST * 2 * TG * D)) < 4 ? (232448 / (kWarps * NST * 2 * TG * D)) : 4;
+}
+
+template <int D, int GN, int NST, int FMT, int TG>
+__global__ void __launch_bounds__(kWarps * 32, (fp8_min_blocks<D, TG, NST>())) decode_split_fp8_kernel(const DecodeParams p) {
+    static_assert(TG == 16 || TG == 32, "tokens per warp-stage");
+    constexpr int kTile = TG * D;       // bytes of one K or V warp-stage tile
+    constexpr int NT = TG / 8;          // n-tiles of 8 tokens in S = Q K^T
+    constexpr int KS = TG / 16;         // k-steps of 16 tokens in O^T += V^T P^T
     constexpr int kChunks = D / 16;     // 16-byte chunks per cache row
     extern __shared__ __align__(128) uint8_t smem[];
     const int kvh = (int)(blockIdx.x % (unsigned)p.Hkv), split = (int)(blockIdx.x / (unsigned)p.Hkv), b = blockIdx.y;
@@ -440,21 +449,21 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_split_fp8_kernel(const 
     // ---- per-warp ring of NST stages x (K tile, V tile), 16 rows of D bytes each
     uint8_t* ring = smem + warp * NST * 2 * kTile;
     const uint32_t ring_s = smem_u32(ring);
-    const long long row_stride = (long long)p.Hkv * D;  // bytes between consecutive cache rows
     const uint8_t* kc = reinterpret_cast<const uint8_t*>(p.k_cache);
     const uint8_t* vc = reinterpret_cast<const uint8_t*>(p.v_cache);
     const int* pt = p.page_table + (long long)b * p.max_pages;
     constexpr int kRowsPerIter = 32 / kChunks;
-    constexpr int kIters = kGroup / kRowsPerIter;
+    constexpr int kIters = TG / kRowsPerIter;
     const int my_chunk = lane % kChunks;
     const int my_row0 = lane / kChunks;
-    const int n_groups_total = cdiv(t_end - t_begin, kGroup);
+    const int n_groups_total = cdiv(t_end - t_begin, TG);
     const int my_groups = n_groups_total > warp ? cdiv(n_groups_total - warp, kWarps) : 0;
 
+    const long long row_stride = (long long)p.Hkv * D;  // bytes between consecutive cache rows
     auto issue = [&](int i) {
         const int slot = i % NST;
-        const int g = t_begin + kGroup * (warp + kWarps * i);
-        const int tok = g + (lane & 15);
+        const int g = t_begin + TG * (warp + kWarps * i);
+        const int tok = g + (lane & (TG - 1));
         long long off = 0;
         int ok = 0;
         if (tok < t_end) {
@@ -503,31 +512,44 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_split_fp8_kernel(const 
         const int slot = i % NST;
         const uint32_t kt = ring_s + slot * 2 * kTile;
         const uint32_t vt = kt + kTile;
-        const int g = t_begin + kGroup * (warp + kWarps * i);
+        const int g = t_begin + TG * (warp + kWarps * i);
 
-        // K operand bytes: tokens g0 and g0 + 8, bytes [(D/4) qd, (D/4) qd + D/4) of the row
-        uint32_t kw[2][D / 16];
+        // K operand bytes: tokens g0 + 8 nt, bytes [(D/4) qd, (D/4) qd + D/4) of the row
+        uint32_t kw[NT][D / 16];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int j = 0; j < D / 64; ++j) lds128(kt + swz8<D>(g0 + 8 * nt, (D / 64) * qd + j), &kw[nt][4 * j]);
-        // S = Q K^T : rows = heads, columns = 16 tokens (two n8 tiles)
-        float sc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+        // S = Q K^T : rows = heads, columns = TG tokens (NT n8 tiles)
+        float sc[NT][4] = {};
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            mma_f16_16816(sc[0], aq[kk], fp8x2_to_f16x2<FMT>(kw[0][kk]), fp8x2_to_f16x2<FMT>(kw[0][kk] >> 16));
-            mma_f16_16816(sc[1], aq[kk], fp8x2_to_f16x2<FMT>(kw[1][kk]), fp8x2_to_f16x2<FMT>(kw[1][kk] >> 16));
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                mma_f16_16816(sc[nt], aq[kk], fp8x2_to_f16x2<FMT>(kw[nt][kk]), fp8x2_to_f16x2<FMT>(kw[nt][kk] >> 16));
         const int tk = g + 2 * qd;
+        if (TG == 16 || g + TG > t_end) {  // (the 16-token form is the one measured fastest at d = 128)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (tk + nt * 8 + (e & 1) >= t_end) sc[nt][e] = -INFINITY;
+                for (int e = 0; e < 4; ++e)
+                    if (tk + nt * 8 + (e & 1) >= t_end) sc[nt][e] = -INFINITY;
+        }
 
         // online softmax per head row (row0 = head g0, row1 = head g0 + 8)
-        float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-        float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+        float mx0, mx1;
+        if constexpr (TG == 16) {
+            mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+            mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+        } else {
+            mx0 = fmaxf(sc[0][0], sc[0][1]);
+            mx1 = fmaxf(sc[0][2], sc[0][3]);
+#pragma unroll
+            for (int nt = 1; nt < NT; ++nt) {
+                mx0 = max3f(mx0, sc[nt][0], sc[nt][1]);
+                mx1 = max3f(mx1, sc[nt][2], sc[nt][3]);
+            }
+        }
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
@@ -565,42 +587,48 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_split_fp8_kernel(const 
         }
         const float n0 = (m0 == -INFINITY) ? 0.0f : -m0 * sl2;
         const float n1 = (m1 == -INFINITY) ? 0.0f : -m1 * sl2;
-        float pr[2][4];
+        float pr[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < NT; ++nt) {
             pr[nt][0] = ex2_mufu(fmaf(sc[nt][0], sl2, n0));
             pr[nt][1] = ex2_mufu(fmaf(sc[nt][1], sl2, n0));
             pr[nt][2] = ex2_mufu(fmaf(sc[nt][2], sl2, n1));
             pr[nt][3] = ex2_mufu(fmaf(sc[nt][3], sl2, n1));
         }
-        l0 += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-        l1 += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
-        const uint32_t pb0 = pack_f16x2(pr[0][0], pr[0][1]);
-        const uint32_t pb1 = pack_f16x2(pr[1][0], pr[1][1]);
-        const uint32_t pb2 = pack_f16x2(pr[0][2], pr[0][3]);
-        const uint32_t pb3 = pack_f16x2(pr[1][2], pr[1][3]);
-
-        // V operand bytes: tokens 2qd, 2qd+1, 2qd+8, 2qd+9; bytes [(D/8) g0, (D/8) g0 + D/8).
-        // Row 16 mt + g0 of V^T is d = (D/8) g0 + 2 mt, row 16 mt + g0 + 8 is d + 1.
-        uint32_t vw[4][D / 32];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int tok = 2 * qd + (t & 1) + 8 * (t >> 1);
-            if (D == 128)
-                lds128(vt + swz8<D>(tok, g0), vw[t]);
-            else
-                lds64(vt + swz8<D>(tok, g0 >> 1) + (g0 & 1) * 8, vw[t]);
+        for (int ks = 0; ks < KS; ++ks) {
+            l0 += (pr[2 * ks][0] + pr[2 * ks][1]) + (pr[2 * ks + 1][0] + pr[2 * ks + 1][1]);
+            l1 += (pr[2 * ks][2] + pr[2 * ks][3]) + (pr[2 * ks + 1][2] + pr[2 * ks + 1][3]);
         }
-        // O^T += V^T P^T : rows = permuted d (16 per m-tile), k = 16 tokens
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;  // bytes 2j and 2j+1 of both tokens
-            const uint32_t lo = __byte_perm(vw[0][mt >> 1], vw[1][mt >> 1], sel);
-            const uint32_t hi = __byte_perm(vw[2][mt >> 1], vw[3][mt >> 1], sel);
-            const uint32_t a[4] = {fp8x2_to_f16x2<FMT>(lo), fp8x2_to_f16x2<FMT>(lo >> 16), fp8x2_to_f16x2<FMT>(hi),
-                                   fp8x2_to_f16x2<FMT>(hi >> 16)};
-            mma_f16_16816(oacc[0][mt], a, pb0, pb1);
-            if (GN == 16) mma_f16_16816(oacc[NH - 1][mt], a, pb2, pb3);
+        for (int ks = 0; ks < KS; ++ks) {
+            // the P^T operand of tokens 16 ks .. 16 ks + 15 (n-tiles 2 ks and 2 ks + 1)
+            const uint32_t pb0 = pack_f16x2(pr[2 * ks][0], pr[2 * ks][1]);
+            const uint32_t pb1 = pack_f16x2(pr[2 * ks + 1][0], pr[2 * ks + 1][1]);
+            const uint32_t pb2 = pack_f16x2(pr[2 * ks][2], pr[2 * ks][3]);
+            const uint32_t pb3 = pack_f16x2(pr[2 * ks + 1][2], pr[2 * ks + 1][3]);
+            // V operand bytes: tokens 16 ks + {2qd, 2qd+1, 2qd+8, 2qd+9}; bytes [(D/8) g0, (D/8) g0 + D/8).
+            // Row 16 mt + g0 of V^T is d = (D/8) g0 + 2 mt, row 16 mt + g0 + 8 is d + 1.
+            uint32_t vw[4][D / 32];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int tok = 16 * ks + 2 * qd + (t & 1) + 8 * (t >> 1);
+                if (D == 128)
+                    lds128(vt + swz8<D>(tok, g0), vw[t]);
+                else
+                    lds64(vt + swz8<D>(tok, g0 >> 1) + (g0 & 1) * 8, vw[t]);
+            }
+            // O^T += V^T P^T : rows = permuted d (16 per m-tile), k = 16 tokens
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;  // bytes 2j and 2j+1 of both tokens
+                const uint32_t lo = __byte_perm(vw[0][mt >> 1], vw[1][mt >> 1], sel);
+                const uint32_t hi = __byte_perm(vw[2][mt >> 1], vw[3][mt >> 1], sel);
+                const uint32_t a[4] = {fp8x2_to_f16x2<FMT>(lo), fp8x2_to_f16x2<FMT>(lo >> 16), fp8x2_to_f16x2<FMT>(hi),
+                                       fp8x2_to_f16x2<FMT>(hi >> 16)};
+                mma_f16_16816(oacc[0][mt], a, pb0, pb1);
+                if (GN == 16) mma_f16_16816(oacc[NH - 1][mt], a, pb2, pb3);
+            }
         }
     }
     cp_async_wait<0>();
@@ -682,16 +710,16 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
     return e;
 }
 
-template <int D, int GN, int NST, int FMT>
+template <int D, int GN, int NST, int FMT, int TG>
 cudaError_t launch_fp8_t(const DecodeParams& p, cudaStream_t stream) {
-    constexpr int ring = kWarps * NST * 2 * kGroup * D;
+    constexpr int ring = kWarps * NST * 2 * TG * D;
     constexpr int merge = (kWarps * GN * D + 2 * kWarps * GN) * 4;
     constexpr int bytes = ring > merge ? ring : merge;
     static std::atomic<bool> attr_set[kMaxAttrDevices];
-    cudaError_t e = ensure_smem_attr(decode_split_fp8_kernel<D, GN, NST, FMT>, bytes, attr_set);
+    cudaError_t e = ensure_smem_attr(decode_split_fp8_kernel<D, GN, NST, FMT, TG>, bytes, attr_set);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(p.max_splits * p.Hkv), p.B);  // kv heads of one split side by side
-    decode_split_fp8_kernel<D, GN, NST, FMT><<<grid, kWarps * 32, bytes, stream>>>(p);
+    decode_split_fp8_kernel<D, GN, NST, FMT, TG><<<grid, kWarps * 32, bytes, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.max_splits > 1) {
@@ -702,12 +730,16 @@ cudaError_t launch_fp8_t(const DecodeParams& p, cudaStream_t stream) {
     return e;
 }
 
+// Tokens per warp-stage of the 8-bit kernels, three stages each: 16 at d = 128 (48 KB of rings per
+// CTA, four CTAs per SM), 32 at d = 64 (the same 48 KB). Measured on the paged decode workload
+// with e4m3 caches: d = 128, 16 tokens 6100 GB/s against 5755 for 32 (two CTAs per SM) and 6070
+// for 32 tokens in two stages; d = 64 (Hkv 16), 32 tokens 6178 against 5250 for 16.
 template <int FMT>
 cudaError_t launch_fp8_fmt(const DecodeParams& p, int d, cudaStream_t stream) {
-    constexpr int NST = 3;  // 48 KB of rings: 4 CTAs per SM (deeper rings measured slower)
+    constexpr int NST = 3;
     if (d == 128)
-        return p.G <= 8 ? launch_fp8_t<128, 8, NST, FMT>(p, stream) : launch_fp8_t<128, 16, NST, FMT>(p, stream);
-    return p.G <= 8 ? launch_fp8_t<64, 8, NST, FMT>(p, stream) : launch_fp8_t<64, 16, NST, FMT>(p, stream);
+        return p.G <= 8 ? launch_fp8_t<128, 8, NST, FMT, 16>(p, stream) : launch_fp8_t<128, 16, NST, FMT, 16>(p, stream);
+    return p.G <= 8 ? launch_fp8_t<64, 8, NST, FMT, 32>(p, stream) : launch_fp8_t<64, 16, NST, FMT, 32>(p, stream);
 }
 
 }  // namespace
