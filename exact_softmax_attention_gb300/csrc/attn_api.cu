@@ -424,6 +424,8 @@ static attn_status_t decode_paged(const void* q, const void* k_cache, const void
     int chunk = 0, max_splits = 0;
     st = attn_decode_plan(B, Hkv, max_pages_per_seq, page_size, num_splits, ds->num_sms, &chunk, &max_splits);
     if (st != ATTN_OK) return st;
+    // one grid column per (split, kv head, group of 16 query heads)
+    if ((long long)max_splits * Hkv * ((Hq / Hkv + 15) / 16) > INT32_MAX) return ATTN_ERR_BAD_SHAPE;
     const Options opt = options();
     DecodeParams p;
     memset(&p, 0, sizeof p);
@@ -438,7 +440,7 @@ static attn_status_t decode_paged(const void* q, const void* k_cache, const void
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.G = Hq / Hkv;
-    p.g_stride = Hq / Hkv;  // the launchers split G > 16 into groups of 16
+    p.g_stride = Hq / Hkv;  // more than 16 per kv head run as groups of 16 within one launch
     p.page_size = page_size;
     p.max_pages = max_pages_per_seq;
     p.num_pages = num_pages;

@@ -55,7 +55,7 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 template <int D, int GN, bool PERM_D>
 __device__ __forceinline__ void merge_and_store(const DecodeParams& p, uint8_t* smem, float (&oacc)[GN / 8][D / 16][4],
                                                 float m0, float m1, float l0, float l1, int split, int nsplit, int kvh,
-                                                int b, float out_scale) {
+                                                int b, float out_scale, int G, int g_base) {
     constexpr int NH = GN / 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g0 = lane >> 2;
@@ -95,7 +95,7 @@ __device__ __forceinline__ void merge_and_store(const DecodeParams& p, uint8_t* 
     __syncthreads();
 
     const bool direct = nsplit == 1;
-    for (int idx = threadIdx.x; idx < p.G * D; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
         const int hh = idx / D, d = idx - hh * D;
         float mm = -INFINITY;
 #pragma unroll
@@ -111,7 +111,7 @@ __device__ __forceinline__ void merge_and_store(const DecodeParams& p, uint8_t* 
         }
         const float o = ll > 0.0f ? acc / ll * out_scale : 0.0f;
         const float lse = ll > 0.0f ? mm * p.scale + logf(ll) : -INFINITY;
-        const long long bh = (long long)b * p.Hq + kvh * p.g_stride + p.g_base + hh;
+        const long long bh = (long long)b * p.Hq + kvh * p.g_stride + g_base + hh;
         if (direct) {
             p.o[bh * D + d] = __float2bfloat16(o);
             if (d == 0) p.lse[bh] = lse;
@@ -126,7 +126,13 @@ template <int D, int GN, int NST>
 __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeParams p) {
     using L = DecLayout<D>;
     extern __shared__ __align__(128) uint8_t smem[];
-    const int kvh = (int)(blockIdx.x % (unsigned)p.Hkv), split = (int)(blockIdx.x / (unsigned)p.Hkv), b = blockIdx.y;
+    // blockIdx.x = (split * Hkv + kv head) * n_groups + group of 16 query heads: the groups of one kv
+    // head are neighbours in launch order, so they read the same cache rows at about the same time
+    // and all but the first find them in the L2.
+    const int grp = (int)(blockIdx.x % (unsigned)p.n_groups), rest = (int)(blockIdx.x / (unsigned)p.n_groups);
+    const int kvh = rest % p.Hkv, split = rest / p.Hkv, b = blockIdx.y;
+    const int g_base = 16 * grp;
+    const int G = p.n_groups > 1 ? min(16, p.g_stride - g_base) : p.g_stride;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long max_len = (long long)p.max_pages * p.page_size;
 
@@ -140,11 +146,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeP
     if (len == 0) {
         // No cached keys: the output is 0 and the log-sum-exp is -inf (written by split 0).
         if (split == 0) {
-            for (int i = threadIdx.x; i < p.G * D; i += blockDim.x) {
-                const int h = kvh * p.g_stride + p.g_base + i / D;
+            for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+                const int h = kvh * p.g_stride + g_base + i / D;
                 p.o[((long long)b * p.Hq + h) * D + (i % D)] = __float2bfloat16(0.0f);
             }
-            if (threadIdx.x < p.G) p.lse[(long long)b * p.Hq + kvh * p.g_stride + p.g_base + threadIdx.x] = -INFINITY;
+            if (threadIdx.x < G) p.lse[(long long)b * p.Hq + kvh * p.g_stride + g_base + threadIdx.x] = -INFINITY;
         }
         return;
     }
@@ -153,8 +159,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeP
 
     // ---- query fragments: rows = query heads of this kv head (padded to 16), k = d
     const int g0 = lane >> 2;
-    const int h0 = kvh * p.g_stride + p.g_base + g0, h1 = kvh * p.g_stride + p.g_base + g0 + 8;
-    const bool v0 = g0 < p.G, v1 = (GN == 16) && (g0 + 8 < p.G);
+    const int h0 = kvh * p.g_stride + g_base + g0, h1 = kvh * p.g_stride + g_base + g0 + 8;
+    const bool v0 = g0 < G, v1 = (GN == 16) && (g0 + 8 < G);
     const uint32_t* q0p = reinterpret_cast<const uint32_t*>(p.q + ((long long)b * p.Hq + h0) * D);
     const uint32_t* q1p = reinterpret_cast<const uint32_t*>(p.q + ((long long)b * p.Hq + h1) * D);
     uint32_t aq[D / 16][4];
@@ -325,7 +331,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeP
         }
     }
     cp_async_wait<0>();
-    merge_and_store<D, GN, false>(p, smem, oacc, m0, m1, l0, l1, split, nsplit, kvh, b, 1.0f);
+    merge_and_store<D, GN, false>(p, smem, oacc, m0, m1, l0, l1, split, nsplit, kvh, b, 1.0f, G, g_base);
 }
 
 // ---------------------------------------------------------------------------- FP8 caches
@@ -405,7 +411,13 @@ __global__ void __launch_bounds__(kWarps * 32, (fp8_min_blocks<D, TG, NST>())) d
     constexpr int KS = TG / 16;         // k-steps of 16 tokens in O^T += V^T P^T
     constexpr int kChunks = D / 16;     // 16-byte chunks per cache row
     extern __shared__ __align__(128) uint8_t smem[];
-    const int kvh = (int)(blockIdx.x % (unsigned)p.Hkv), split = (int)(blockIdx.x / (unsigned)p.Hkv), b = blockIdx.y;
+    // blockIdx.x = (split * Hkv + kv head) * n_groups + group of 16 query heads: the groups of one kv
+    // head are neighbours in launch order, so they read the same cache rows at about the same time
+    // and all but the first find them in the L2.
+    const int grp = (int)(blockIdx.x % (unsigned)p.n_groups), rest = (int)(blockIdx.x / (unsigned)p.n_groups);
+    const int kvh = rest % p.Hkv, split = rest / p.Hkv, b = blockIdx.y;
+    const int g_base = 16 * grp;
+    const int G = p.n_groups > 1 ? min(16, p.g_stride - g_base) : p.g_stride;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long max_len = (long long)p.max_pages * p.page_size;
 
@@ -418,11 +430,11 @@ __global__ void __launch_bounds__(kWarps * 32, (fp8_min_blocks<D, TG, NST>())) d
     const int t_begin = split * p.chunk;
     if (len == 0) {
         if (split == 0) {
-            for (int i = threadIdx.x; i < p.G * D; i += blockDim.x) {
-                const int h = kvh * p.g_stride + p.g_base + i / D;
+            for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+                const int h = kvh * p.g_stride + g_base + i / D;
                 p.o[((long long)b * p.Hq + h) * D + (i % D)] = __float2bfloat16(0.0f);
             }
-            if (threadIdx.x < p.G) p.lse[(long long)b * p.Hq + kvh * p.g_stride + p.g_base + threadIdx.x] = -INFINITY;
+            if (threadIdx.x < G) p.lse[(long long)b * p.Hq + kvh * p.g_stride + g_base + threadIdx.x] = -INFINITY;
         }
         return;
     }
@@ -432,8 +444,8 @@ __global__ void __launch_bounds__(kWarps * 32, (fp8_min_blocks<D, TG, NST>())) d
     // ---- query fragments (f16), rows = query heads of this kv head. Permuted d: column
     // 2 qd + e of k-step kk is d = (D/4) qd + 4 kk + e, column 2 qd + 8 + e is that + 2.
     const int g0 = lane >> 2, qd = lane & 3;
-    const int h0 = kvh * p.g_stride + p.g_base + g0, h1 = kvh * p.g_stride + p.g_base + g0 + 8;
-    const bool v0 = g0 < p.G, v1 = (GN == 16) && (g0 + 8 < p.G);
+    const int h0 = kvh * p.g_stride + g_base + g0, h1 = kvh * p.g_stride + g_base + g0 + 8;
+    const bool v0 = g0 < G, v1 = (GN == 16) && (g0 + 8 < G);
     const uint32_t* q0p = reinterpret_cast<const uint32_t*>(p.q + ((long long)b * p.Hq + h0) * D);
     const uint32_t* q1p = reinterpret_cast<const uint32_t*>(p.q + ((long long)b * p.Hq + h1) * D);
     uint32_t aq[D / 16][4];
@@ -632,7 +644,7 @@ __global__ void __launch_bounds__(kWarps * 32, (fp8_min_blocks<D, TG, NST>())) d
         }
     }
     cp_async_wait<0>();
-    merge_and_store<D, GN, true>(p, smem, oacc, m0, m1, l0, l1, split, nsplit, kvh, b, p.v_descale);
+    merge_and_store<D, GN, true>(p, smem, oacc, m0, m1, l0, l1, split, nsplit, kvh, b, p.v_descale, G, g_base);
 }
 
 // One warp per (sequence, query head of this launch): LSE = log sum_s exp(lse_s) (max-shifted,
@@ -698,7 +710,8 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
     static std::atomic<bool> attr_set[kMaxAttrDevices];
     cudaError_t e = ensure_smem_attr(decode_split_kernel<D, GN, NST>, bytes, attr_set);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)(p.max_splits * p.Hkv), p.B);  // kv heads of one split side by side
+    // head groups of one kv head, then the kv heads of one split, side by side
+    const dim3 grid((unsigned)(p.max_splits * p.Hkv * p.n_groups), p.B);
     decode_split_kernel<D, GN, NST><<<grid, kWarps * 32, bytes, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -718,7 +731,8 @@ cudaError_t launch_fp8_t(const DecodeParams& p, cudaStream_t stream) {
     static std::atomic<bool> attr_set[kMaxAttrDevices];
     cudaError_t e = ensure_smem_attr(decode_split_fp8_kernel<D, GN, NST, FMT, TG>, bytes, attr_set);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)(p.max_splits * p.Hkv), p.B);  // kv heads of one split side by side
+    // head groups of one kv head, then the kv heads of one split, side by side
+    const dim3 grid((unsigned)(p.max_splits * p.Hkv * p.n_groups), p.B);
     decode_split_fp8_kernel<D, GN, NST, FMT, TG><<<grid, kWarps * 32, bytes, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -746,28 +760,27 @@ cudaError_t launch_fp8_fmt(const DecodeParams& p, int d, cudaStream_t stream) {
 
 // The query heads of a kv head are the rows of the kernels' tensor-core products (at most 16):
 // more than 16 run as one launch (split kernel, then combine) per group of 16.
+// The split kernels take at most 16 query heads of a kv head (the rows of their tensor-core
+// products); more run as groups of 16 in the same launch, one CTA per group, neighbours in the
+// grid (so the groups share the cache rows in the L2). The combine then merges all heads.
+static DecodeParams grouped(const DecodeParams& p_in) {
+    DecodeParams p = p_in;
+    p.n_groups = (p_in.g_stride + 15) / 16;
+    p.g_base = 0;
+    p.G = p_in.g_stride;
+    return p;
+}
+
 cudaError_t launch_attn_decode_fp8(const DecodeParams& p_in, int d, int fmt, cudaStream_t stream) {
-    for (int g0 = 0; g0 < p_in.g_stride; g0 += 16) {
-        DecodeParams p = p_in;
-        p.g_base = g0;
-        p.G = p_in.g_stride - g0 < 16 ? p_in.g_stride - g0 : 16;
-        const cudaError_t e = fmt == 0 ? launch_fp8_fmt<0>(p, d, stream) : launch_fp8_fmt<1>(p, d, stream);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    const DecodeParams p = grouped(p_in);
+    return fmt == 0 ? launch_fp8_fmt<0>(p, d, stream) : launch_fp8_fmt<1>(p, d, stream);
 }
 
 cudaError_t launch_attn_decode(const DecodeParams& p_in, int d, cudaStream_t stream) {
     constexpr int NST = 3;
-    for (int g0 = 0; g0 < p_in.g_stride; g0 += 16) {  // groups of at most 16 query heads, as above
-        DecodeParams p = p_in;
-        p.g_base = g0;
-        p.G = p_in.g_stride - g0 < 16 ? p_in.g_stride - g0 : 16;
-        const cudaError_t e = d == 128 ? (p.G <= 8 ? launch_t<128, 8, NST>(p, stream) : launch_t<128, 16, NST>(p, stream))
-                                       : (p.G <= 8 ? launch_t<64, 8, NST>(p, stream) : launch_t<64, 16, NST>(p, stream));
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    const DecodeParams p = grouped(p_in);
+    return d == 128 ? (p.G <= 8 ? launch_t<128, 8, NST>(p, stream) : launch_t<128, 16, NST>(p, stream))
+                    : (p.G <= 8 ? launch_t<64, 8, NST>(p, stream) : launch_t<64, 16, NST>(p, stream));
 }
 
 }  // namespace attn

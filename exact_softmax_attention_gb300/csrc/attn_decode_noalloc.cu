@@ -63,6 +63,8 @@ extern "C" attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_
     int chunk = 0, max_splits = 0;
     st = attn_decode_plan(B, Hkv, max_pages_per_seq, page_size, num_splits, num_sms, &chunk, &max_splits);
     if (st != ATTN_OK) return st;
+    // one grid column per (split, kv head, group of 16 query heads)
+    if ((long long)max_splits * Hkv * ((Hq / Hkv + 15) / 16) > INT32_MAX) return ATTN_ERR_BAD_SHAPE;
     const size_t n_o = (size_t)B * Hq * max_splits * d;
     const size_t n_l = (size_t)B * Hq * max_splits;
     if (max_splits > 1 && (n_o + n_l) * sizeof(float) > kScratchBytes) return ATTN_ERR_SCRATCH_TOO_SMALL;
@@ -88,7 +90,7 @@ extern "C" attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.G = Hq / Hkv;
-    p.g_stride = Hq / Hkv;  // the launcher splits G > 16 into groups of 16
+    p.g_stride = Hq / Hkv;  // more than 16 per kv head run as groups of 16 within one launch
     p.page_size = page_size;
     p.max_pages = max_pages_per_seq;
     p.num_pages = num_pages;

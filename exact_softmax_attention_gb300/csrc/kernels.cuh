@@ -89,9 +89,10 @@ struct DecodeParams {
     float* ws_o;                   // [B, Hq, max_splits, d] partial outputs
     float* ws_lse;                 // [B, Hq, max_splits] partial LSE
     int B, Hq, Hkv, page_size, max_pages, num_pages;
-    // Query heads: one launch handles heads g_base .. g_base + G - 1 (G <= 16) of every kv head;
-    // g_stride = Hq / Hkv is their spacing in memory (query head h reads kv head h / g_stride).
-    int G, g_base, g_stride;
+    // Query heads: g_stride = Hq / Hkv per kv head (query head h reads kv head h / g_stride). The
+    // split kernels take them in n_groups groups of at most 16 (one CTA each); the combine
+    // merges heads g_base .. g_base + G - 1 of every kv head (all of them: g_base 0, G = g_stride).
+    int G, g_base, g_stride, n_groups;
     int chunk;       // tokens per split (multiple of 64)
     int max_splits;  // splits per sequence the workspace holds
     float scale, scale_log2, rescale_thr;

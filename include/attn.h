@@ -147,7 +147,8 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
  * page_size  tokens per page, >= 1 (any value)
  * o          device, bf16 [B, Hq, d] (written);  lse device, fp32 [B, Hq] (written)
  * B, Hq, Hkv, d  as for attn_fwd (d = 64 or 128); the query heads of a kv head are the rows
- *            of one tile, so more than 16 per kv head run as one launch per group of 16
+ *            of one tile, so more than 16 per kv head run as groups of 16 (one CTA each, in the
+ *            same launch, neighbours in the grid so that they share the cache rows in the L2)
  * max_pages_per_seq  columns of page_table (>= 1)
  * num_pages  physical pages in each cache (>= 1); a page index outside [0, num_pages) is
  *            not read: its rows count as zeros and ATTN_ERR_DEVICE_BAD_INDEX is recorded
