@@ -457,7 +457,7 @@ def run_ours(args):
     def dec():
         dec_on(DQ, KC, VC, PT, SL, DO, DLSE)
 
-    _, max_splits = A.attn_decode_plan(dc.B, dc.Hkv, dc.max_pages, dc.page_size, 0)
+    _, max_splits = A.attn_decode_plan(dc.B, dc.Hq, dc.Hkv, dc.max_pages, dc.page_size, 0)
     launches_per_step = 1 + (2 if max_splits > 1 else 1)
 
     def barrier():

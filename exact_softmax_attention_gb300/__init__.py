@@ -65,7 +65,7 @@ lib.attn_decode_paged_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp
 lib.attn_decode_paged_fp8.restype = _i
 lib.attn_decode_paged_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i]
 lib.attn_decode_paged_noalloc.restype = _i
-lib.attn_decode_plan.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]
+lib.attn_decode_plan.argtypes = [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]
 lib.attn_decode_plan.restype = _i
 lib.attn_decode_workspace_bytes.argtypes = [_i, _i, _i, _i]
 lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
@@ -178,11 +178,11 @@ def attn_decode_paged_noalloc(q, k_cache, v_cache, page_table, seqlens, page_siz
     return _check(rc, "attn_decode_paged_noalloc", raise_on_error)
 
 
-def attn_decode_plan(B, Hkv, max_pages_per_seq, page_size, num_splits=0, num_sms=0):
+def attn_decode_plan(B, Hq, Hkv, max_pages_per_seq, page_size, num_splits=0, num_sms=0):
     """(chunk tokens per split, splits per sequence) chosen by the library."""
     c, s = _i(), _i()
-    rc = lib.attn_decode_plan(int(B), int(Hkv), int(max_pages_per_seq), int(page_size), int(num_splits), int(num_sms),
-                              ctypes.byref(c), ctypes.byref(s))
+    rc = lib.attn_decode_plan(int(B), int(Hq), int(Hkv), int(max_pages_per_seq), int(page_size), int(num_splits),
+                              int(num_sms), ctypes.byref(c), ctypes.byref(s))
     _check(rc, "attn_decode_plan", True)
     return c.value, s.value
 

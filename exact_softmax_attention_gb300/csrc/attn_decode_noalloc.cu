@@ -61,7 +61,7 @@ extern "C" attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_
     attn_status_t st = attn::current_device_info(&status, &num_sms);
     if (st != ATTN_OK) return st;
     int chunk = 0, max_splits = 0;
-    st = attn_decode_plan(B, Hkv, max_pages_per_seq, page_size, num_splits, num_sms, &chunk, &max_splits);
+    st = attn_decode_plan(B, Hq, Hkv, max_pages_per_seq, page_size, num_splits, num_sms, &chunk, &max_splits);
     if (st != ATTN_OK) return st;
     // one grid column per (split, kv head, group of 16 query heads)
     if ((long long)max_splits * Hkv * ((Hq / Hkv + 15) / 16) > INT32_MAX) return ATTN_ERR_BAD_SHAPE;

@@ -216,11 +216,14 @@ attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_cache, cons
  * Host-side split choice of attn_decode_paged (the num_splits = 0 heuristic of "Faster,
  * more flexible FA4 for LLM inference", PR 1940 section; the pages give no formula).
  * Writes the tokens per split (*chunk, a multiple of 64) and the splits the workspace
- * holds per sequence (*max_splits) for the given sizes. num_sms <= 0 uses the current
- * device's SM count. Pure host arithmetic; needs no GPU when num_sms > 0.
+ * holds per sequence (*max_splits) for the given sizes. The heuristic aims at about 32
+ * (sequence, kv head, split) items per SM, with at least 256 and at least 128 * Hq / Hkv
+ * tokens per split (so that the fp32 partials of the query heads stay small next to the
+ * cache bytes of a split) and at most 8192. num_sms <= 0 uses the current device's SM
+ * count. Pure host arithmetic; needs no GPU when num_sms > 0.
  */
-attn_status_t attn_decode_plan(int B, int Hkv, int max_pages_per_seq, int page_size, int num_splits, int num_sms,
-                               int* chunk, int* max_splits);
+attn_status_t attn_decode_plan(int B, int Hq, int Hkv, int max_pages_per_seq, int page_size, int num_splits,
+                               int num_sms, int* chunk, int* max_splits);
 
 /*
  * Bytes of split-KV workspace attn_decode_paged takes for these sizes: B * Hq * max_splits

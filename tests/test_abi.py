@@ -85,7 +85,7 @@ def test_decode_workspace_bytes():
     assert A.attn_decode_workspace_bytes(64, 32, 128, 19) == 64 * 32 * 19 * 129 * 4
     assert A.attn_decode_workspace_bytes(64, 32, 128, 1) == 0  # one split writes o and lse directly
     assert A.attn_decode_workspace_bytes(0, 32, 128, 4) == 0
-    _, splits = A.attn_decode_plan(64, 8, 2048, 16, 0, 152)
+    _, splits = A.attn_decode_plan(64, 32, 8, 2048, 16, 0, 152)
     assert A.attn_decode_workspace_bytes(64, 32, 128, splits) < 32 << 20  # the decode workload fits the no-alloc array
 
 
@@ -127,16 +127,25 @@ def test_fp8_decode_host_validation(lib):
     assert _dec8(lib, fmt=1, B=0) == A.ATTN_OK
 
 
-@pytest.mark.parametrize("B,Hkv,mp,ps,ns", [(64, 8, 2048, 16, 0), (1, 1, 1, 1, 0), (3, 2, 10, 7, 4),
-                                            (64, 8, 2048, 16, 5), (8, 1, 100, 1, 1)])
-def test_decode_plan(B, Hkv, mp, ps, ns):
+@pytest.mark.parametrize("B,Hq,Hkv,mp,ps,ns", [(64, 32, 8, 2048, 16, 0), (1, 1, 1, 1, 1, 0), (3, 4, 2, 10, 7, 4),
+                                               (64, 32, 8, 2048, 16, 5), (8, 8, 1, 100, 1, 1), (64, 32, 1, 2048, 16, 0)])
+def test_decode_plan(B, Hq, Hkv, mp, ps, ns):
     import exact_softmax_attention_gb300 as A
-    chunk, splits = A.attn_decode_plan(B, Hkv, mp, ps, ns, num_sms=152)
+    chunk, splits = A.attn_decode_plan(B, Hq, Hkv, mp, ps, ns, num_sms=152)
     lmax = mp * ps
     assert chunk % 64 == 0 and chunk >= 64
     assert splits * chunk >= lmax and (splits - 1) * chunk < lmax
     if ns > 0:
         assert splits <= ns
+    elif lmax >= 128 * (Hq // Hkv):
+        assert chunk >= 128 * (Hq // Hkv)  # partials of many query heads per kv head stay small
+
+
+def test_decode_plan_rejects_bad_heads():
+    import exact_softmax_attention_gb300 as A
+    for hq, hkv in ((0, 1), (6, 4)):
+        with pytest.raises(A.AttnError):
+            A.attn_decode_plan(2, hq, hkv, 10, 16, 0, num_sms=152)
 
 
 def test_options_roundtrip():

@@ -45,7 +45,7 @@ def lib():
         f.restype = i
     L.attn_get_device_status.argtypes = [vp]
     L.attn_get_device_status.restype = i
-    L.attn_decode_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+    L.attn_decode_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
     L.attn_decode_plan.restype = i
     return L
 
@@ -58,7 +58,8 @@ def make_case(seed, B, Hq, Hkv, d, page_size, lo, hi):
 
 def splits_of(L, c):
     chunk, splits = ctypes.c_int(), ctypes.c_int()
-    assert L.attn_decode_plan(c.B, c.Hkv, c.max_pages, c.page_size, 0, 0, ctypes.byref(chunk), ctypes.byref(splits)) == 0
+    assert L.attn_decode_plan(c.B, c.Hq, c.Hkv, c.max_pages, c.page_size, 0, 0, ctypes.byref(chunk),
+                              ctypes.byref(splits)) == 0
     return splits.value
 
 
