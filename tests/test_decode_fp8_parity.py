@@ -61,8 +61,12 @@ CASES = [
     (fcase("e4m3_g12", 3, 24, 2, 128, 32, 100, 2000, 28, "e4m3"), 2),
     (fcase("e5m2_g1", 4, 4, 4, 64, 16, 1, 900, 29, "e5m2"), 0),
     (fcase("e4m3_edges", 0, 8, 2, 128, 16, 0, 0, 30, "e4m3", lens=[0, 1, 15, 16, 17, 63, 64, 65, 1024, 1025]), 0),
-    (fcase("e4m3_g32_mqa", 3, 32, 1, 128, 16, 100, 3000, 31, "e4m3"), 0),   # two launches of 16 heads
+    (fcase("e4m3_g32_mqa", 3, 32, 1, 128, 16, 100, 3000, 31, "e4m3"), 0),   # two groups of 16 heads
     (fcase("e5m2_g20_split2", 2, 40, 2, 64, 16, 1500, 3000, 32, "e5m2"), 2),  # 16 + 4 heads per kv head
+    # head width 64 runs 32-token stages: lengths around multiples of 32 and of the page size
+    (fcase("e4m3_edges_d64", 0, 8, 2, 64, 16, 0, 0, 33, "e4m3",
+           lens=[0, 1, 31, 32, 33, 47, 63, 64, 65, 95, 96, 97, 1023, 1024, 1025]), 0),
+    (fcase("e5m2_edges_d64_split3", 0, 8, 2, 64, 5, 0, 0, 34, "e5m2", lens=[1, 33, 95, 130, 1000, 1600]), 3),
 ]
 
 

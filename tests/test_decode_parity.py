@@ -67,7 +67,7 @@ CASES = [
     (dcase("g1", 4, 4, 4, 64, 16, 1, 900, 7), 0),
     (dcase("edge_lengths", 0, 8, 2, 128, 16, 0, 0, 8, lens=[0, 1, 15, 16, 17, 63, 64, 65, 1024, 1025]), 0),
     (dcase("one_split", 4, 8, 2, 128, 16, 1, 4000, 9), 1),
-    (dcase("g32_mqa", 3, 32, 1, 128, 16, 100, 3000, 13), 0),     # two launches of 16 heads
+    (dcase("g32_mqa", 3, 32, 1, 128, 16, 100, 3000, 13), 0),     # two groups of 16 heads
     (dcase("g24_d64", 3, 48, 2, 64, 8, 1, 2500, 14), 0),       # 16 + 8 heads per kv head
     (dcase("g40_split2", 2, 40, 1, 128, 16, 2000, 4000, 15), 2),
 ]
