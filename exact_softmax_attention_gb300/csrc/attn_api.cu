@@ -33,6 +33,7 @@ struct Options {
     int correction = 0;
     int unroll_kv = 0;
     int dynamic_order = 1;
+    int decode_order = 1;
 };
 
 std::mutex g_mu;
@@ -189,6 +190,9 @@ attn_status_t attn_set_option(const char* name, double value) {
     } else if (!strcmp(name, "dynamic_order")) {
         if (value != 0 && value != 1) return ATTN_ERR_BAD_ARG;
         g_opt.dynamic_order = (int)value;
+    } else if (!strcmp(name, "decode_order")) {
+        if (value != 0 && value != 1) return ATTN_ERR_BAD_ARG;
+        g_opt.decode_order = (int)value;
     } else {
         return ATTN_ERR_BAD_ARG;
     }
@@ -208,6 +212,7 @@ attn_status_t attn_get_option(const char* name, double* value) {
     else if (!strcmp(name, "correction")) *value = g_opt.correction;
     else if (!strcmp(name, "unroll_kv")) *value = g_opt.unroll_kv;
     else if (!strcmp(name, "dynamic_order")) *value = g_opt.dynamic_order;
+    else if (!strcmp(name, "decode_order")) *value = g_opt.decode_order;
     else return ATTN_ERR_BAD_ARG;
     return ATTN_OK;
 }
@@ -387,10 +392,16 @@ attn_status_t attn_decode_plan(int B, int Hq, int Hkv, int max_pages_per_seq, in
     } else if (opt.decode_chunk > 0) {
         c = opt.decode_chunk;
     } else {
-        // Enough (sequence, kv head, split) items for ~32 per SM, assuming the average
-        // sequence fills half of its page-table row; at least 256 tokens per split.
+        // About 18 (sequence, kv head, split) items per SM, assuming the average sequence fills
+        // half of its page-table row; at least 256 tokens per split. Each split costs a few
+        // microseconds beyond its bytes (pipeline fill and drain, the warp merge), and the split
+        // kernels start every sequence's last split after all the others, so fewer, longer
+        // splits win until the last wave gets coarse. Measured on 64 sequences of U[1K, 32K]
+        // tokens, 8 kv heads: 1728 / 2048 / 2560 / 3072 / 3456 tokens per split (32 to 16 items
+        // per SM) gave 6093 / 6186 / 6274 / 6287 / 6221 GB/s with e4m3 caches and 6883 / 6897 /
+        // 6952 / 6990 / 6963 GB/s with bf16 caches.
         const long long work = (long long)(B > 0 ? B : 1) * Hkv * ((lmax + 1) / 2);
-        const long long items = 32LL * num_sms;
+        const long long items = 18LL * num_sms;
         c = (work + items - 1) / items;
         if (c < 256) c = 256;
         // Each split writes d + 1 floats per query head; with few kv heads (MQA) small splits
@@ -455,6 +466,7 @@ static attn_status_t decode_paged(const void* q, const void* k_cache, const void
     p.scale = (float)score_scale;
     p.scale_log2 = (float)(score_scale * 1.4426950408889634);
     p.rescale_thr = (float)opt.rescale_threshold;
+    p.order = opt.decode_order;
     p.v_descale = kv_format < 0 ? 1.0f : v_descale;
     p.status = ds->status;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

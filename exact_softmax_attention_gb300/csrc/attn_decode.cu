@@ -14,8 +14,12 @@
 // section 02) runs per warp over its tokens; the warps of a CTA and then the splits
 // are merged with the same max-shifted LSE weighting.
 //
-// Split kernel: grid (split x kv head, sequence) with the kv heads of one split adjacent,
-// so CTAs running side by side read neighbouring pieces of the same cache rows; 4 warps.
+// Split kernel: one CTA of 4 warps per (sequence, split, kv head), the kv heads of one split
+// adjacent in the grid, so CTAs running side by side read neighbouring pieces of the same
+// cache rows. The grid lists every split but the last of each sequence first and the last
+// splits (shorter in general) after them, longest first, so that they fill the SMs freed
+// while the last full-length splits finish (LPT); the combine kernel is launched as a
+// programmatic dependent and waits on the device, not behind a launch.
 // Each warp owns a private cp.async ring of NST stages of 16 tokens (K and V rows,
 // 128-byte XOR swizzle) and processes token groups w, w+4, w+8, ... of the split, so the
 // main loop needs no CTA-wide barrier. Scores S = Q K^T use m16n8k16 bf16 MMAs with the (up to 16) query
@@ -45,6 +49,73 @@ struct DecLayout {
 template <int D>
 __device__ __forceinline__ uint32_t swz(int r, int c) {
     return (uint32_t)(r * (D * 2) + ((c ^ (r & 7)) << 4));
+}
+
+// Sequence whose last split has rank `rank` in decreasing length (ties: lower sequence index
+// first), and its length as stored (*raw_len). Every thread of the CTA calls it; scratch holds
+// 2 B + 2 ints of shared memory.
+__device__ __forceinline__ int seq_of_rank(const DecodeParams& p, int rank, uint8_t* scratch, int* raw_len) {
+    int* key = reinterpret_cast<int*>(scratch);
+    int* raw = key + p.B;
+    int* sel = raw + p.B;
+    const long long max_len = (long long)p.max_pages * p.page_size;
+    for (int t = threadIdx.x; t < p.B; t += blockDim.x) {
+        const int r = __ldg(p.seqlens + t);
+        const int len = r < 0 ? 0 : (r > max_len ? (int)max_len : r);
+        const int ns = cdiv(len, p.chunk);
+        key[t] = len - (ns > 0 ? ns - 1 : 0) * p.chunk;  // tokens of the last split
+        raw[t] = r;
+    }
+    if (threadIdx.x == 0) sel[0] = 0;
+    __syncthreads();
+    for (int t = threadIdx.x; t < p.B; t += blockDim.x) {
+        const int kt = key[t];
+        int r = 0;
+        for (int u = 0; u < p.B; ++u) {
+            const int ku = key[u];
+            r += (ku > kt) || (ku == kt && u < t);
+        }
+        if (r == rank) sel[0] = t;
+    }
+    __syncthreads();
+    const int b = sel[0];
+    *raw_len = raw[b];
+    __syncthreads();  // the scratch is the ring's memory
+    return b;
+}
+
+// Work item of a split-kernel CTA: sequence, split (or -1: the sequence's last split) and
+// head-group index hg = kv head * n_groups + group. The grid lists every split but the last
+// of each sequence (row = sequence, column = split * HG + hg) before the last splits, which
+// are shorter in general: CTAs start in grid order, so the short items fill the SMs that
+// free up while the last full-length ones finish, the longest first when p.lpt is set.
+// Returns false (for the whole CTA) when the CTA has no item. has_len: len holds the
+// sequence length as stored (read while ranking).
+struct DecItem {
+    int b, split, hg, len;
+    bool has_len;
+};
+__device__ __forceinline__ bool decode_item(const DecodeParams& p, uint8_t* scratch, DecItem& it) {
+    const int HG = p.Hkv * p.n_groups;
+    it.has_len = false;
+    it.len = 0;
+    if (p.full_rows < 0 || (int)blockIdx.y < p.full_rows) {
+        it.b = blockIdx.y;
+        it.split = (int)(blockIdx.x / (unsigned)HG);
+        it.hg = (int)(blockIdx.x % (unsigned)HG);
+        return true;
+    }
+    const long long j = (long long)(blockIdx.y - p.full_rows) * gridDim.x + blockIdx.x;
+    if (j >= (long long)p.B * HG) return false;
+    it.hg = (int)(j % HG);
+    if (p.lpt) {
+        it.b = seq_of_rank(p, (int)(j / HG), scratch, &it.len);
+        it.has_len = true;
+    } else {
+        it.b = (int)(j / HG);
+    }
+    it.split = -1;
+    return true;
 }
 
 // Merge the 4 warps' partial results of a split kernel (max-shifted LSE weighting) and
@@ -124,24 +195,31 @@ __device__ __forceinline__ void merge_and_store(const DecodeParams& p, uint8_t* 
 
 template <int D, int GN, int NST>
 __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeParams p) {
+    grid_dependents_launch();  // the combine kernel may be scheduled once every split CTA runs
     using L = DecLayout<D>;
     extern __shared__ __align__(128) uint8_t smem[];
-    // blockIdx.x = (split * Hkv + kv head) * n_groups + group of 16 query heads: the groups of one kv
-    // head are neighbours in launch order, so they read the same cache rows at about the same time
-    // and all but the first find them in the L2.
-    const int grp = (int)(blockIdx.x % (unsigned)p.n_groups), rest = (int)(blockIdx.x / (unsigned)p.n_groups);
-    const int kvh = rest % p.Hkv, split = rest / p.Hkv, b = blockIdx.y;
+    // hg = kv head * n_groups + group of 16 query heads: the groups of one kv head are neighbours
+    // in launch order, so they read the same cache rows at about the same time and all but the
+    // first find them in the L2.
+    DecItem item;
+    if (!decode_item(p, smem, item)) return;
+    const int grp = item.hg % p.n_groups, kvh = item.hg / p.n_groups, b = item.b;
     const int g_base = 16 * grp;
     const int G = p.n_groups > 1 ? min(16, p.g_stride - g_base) : p.g_stride;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long max_len = (long long)p.max_pages * p.page_size;
 
-    int len = __ldg(p.seqlens + b);
+    int len = item.has_len ? item.len : __ldg(p.seqlens + b);
     if (len < 0 || len > max_len) {
         if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevBadIndex);
         len = len < 0 ? 0 : (int)max_len;
     }
     const int nsplit = cdiv(len, p.chunk);
+    int split = item.split;
+    if (split < 0)
+        split = nsplit > 0 ? nsplit - 1 : 0;
+    else if (p.full_rows >= 0 && split >= nsplit - 1)
+        return;  // the last split has its own CTA after the full rows
     const int t_begin = split * p.chunk;
     if (len == 0) {
         // No cached keys: the output is 0 and the log-sum-exp is -inf (written by split 0).
@@ -405,28 +483,35 @@ constexpr int fp8_min_blocks() {
 
 template <int D, int GN, int NST, int FMT, int TG>
 __global__ void __launch_bounds__(kWarps * 32, (fp8_min_blocks<D, TG, NST>())) decode_split_fp8_kernel(const DecodeParams p) {
+    grid_dependents_launch();  // the combine kernel may be scheduled once every split CTA runs
     static_assert(TG == 16 || TG == 32, "tokens per warp-stage");
     constexpr int kTile = TG * D;       // bytes of one K or V warp-stage tile
     constexpr int NT = TG / 8;          // n-tiles of 8 tokens in S = Q K^T
     constexpr int KS = TG / 16;         // k-steps of 16 tokens in O^T += V^T P^T
     constexpr int kChunks = D / 16;     // 16-byte chunks per cache row
     extern __shared__ __align__(128) uint8_t smem[];
-    // blockIdx.x = (split * Hkv + kv head) * n_groups + group of 16 query heads: the groups of one kv
-    // head are neighbours in launch order, so they read the same cache rows at about the same time
-    // and all but the first find them in the L2.
-    const int grp = (int)(blockIdx.x % (unsigned)p.n_groups), rest = (int)(blockIdx.x / (unsigned)p.n_groups);
-    const int kvh = rest % p.Hkv, split = rest / p.Hkv, b = blockIdx.y;
+    // hg = kv head * n_groups + group of 16 query heads: the groups of one kv head are neighbours
+    // in launch order, so they read the same cache rows at about the same time and all but the
+    // first find them in the L2.
+    DecItem item;
+    if (!decode_item(p, smem, item)) return;
+    const int grp = item.hg % p.n_groups, kvh = item.hg / p.n_groups, b = item.b;
     const int g_base = 16 * grp;
     const int G = p.n_groups > 1 ? min(16, p.g_stride - g_base) : p.g_stride;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long max_len = (long long)p.max_pages * p.page_size;
 
-    int len = __ldg(p.seqlens + b);
+    int len = item.has_len ? item.len : __ldg(p.seqlens + b);
     if (len < 0 || len > max_len) {
         if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevBadIndex);
         len = len < 0 ? 0 : (int)max_len;
     }
     const int nsplit = cdiv(len, p.chunk);
+    int split = item.split;
+    if (split < 0)
+        split = nsplit > 0 ? nsplit - 1 : 0;
+    else if (p.full_rows >= 0 && split >= nsplit - 1)
+        return;  // the last split has its own CTA after the full rows
     const int t_begin = split * p.chunk;
     if (len == 0) {
         if (split == 0) {
@@ -648,51 +733,80 @@ __global__ void __launch_bounds__(kWarps * 32, (fp8_min_blocks<D, TG, NST>())) d
 }
 
 // One warp per (sequence, query head of this launch): LSE = log sum_s exp(lse_s) (max-shifted,
-// warp shuffles over the splits), O = sum_s exp(lse_s - LSE) O_s.
+// warp shuffles over the splits), O = sum_s exp(lse_s - LSE) O_s, summed in split order.
+// Launched as a programmatic dependent of the split kernel: its CTAs may start while the last
+// split CTAs run. What the split kernel does not write (the lengths) is read before waiting for
+// that grid to finish; after it, the split LSEs and the first 8 partial rows are loaded together.
 template <int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // row (b, kv head, g) of this launch's heads -> query row b * Hq + kvh * g_stride + g_base + g
     const long long row = (long long)blockIdx.x * 4 + warp;
     const long long per_b = (long long)p.Hkv * p.G;
-    if (row >= (long long)p.B * per_b) return;
-    const int b = (int)(row / per_b);
-    const int rem = (int)(row - b * per_b);
+    const bool active = row < (long long)p.B * per_b;
+    const int b = active ? (int)(row / per_b) : 0;
+    const int rem = active ? (int)(row - b * per_b) : 0;
     const long long bh = (long long)b * p.Hq + (long long)(rem / p.G) * p.g_stride + p.g_base + rem % p.G;
     const long long max_len = (long long)p.max_pages * p.page_size;
-    int len = __ldg(p.seqlens + b);
+    int len = active ? __ldg(p.seqlens + b) : 0;
     len = len < 0 ? 0 : (len > max_len ? (int)max_len : len);
     const int ns = cdiv(len, p.chunk);
+    grid_dependency_wait();
     if (ns <= 1) return;  // written directly by the split kernel
+    constexpr int PER = D / 32;
+    constexpr int UNR = 8;  // partial rows loaded before any is accumulated
     const float* wl = p.ws_lse + bh * p.max_splits;
-    float mx = -INFINITY;
-    for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, wl[s]);
+    const float* wo = p.ws_o + bh * p.max_splits * D + lane * PER;
+    auto load_rows = [&](int s0, int cnt, float (&v)[UNR][PER]) {
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            const float* src = wo + (long long)(s0 + min(u, cnt - 1)) * D;  // clamped: always a valid row
+            if (PER == 4) {
+                const float4 t = *reinterpret_cast<const float4*>(src);
+                v[u][0] = t.x;
+                v[u][1 % PER] = t.y;
+                v[u][2 % PER] = t.z;
+                v[u][3 % PER] = t.w;
+            } else {
+                const float2 t = *reinterpret_cast<const float2*>(src);
+                v[u][0] = t.x;
+                v[u][1 % PER] = t.y;
+            }
+        }
+    };
+    float v[UNR][PER];
+    const float l_first = lane < ns ? wl[lane] : -INFINITY;
+    load_rows(0, min(UNR, ns), v);
+    float mx = l_first;
+    for (int s = lane + 32; s < ns; s += 32) mx = fmaxf(mx, wl[s]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float sum = 0.0f;
-    if (mx != -INFINITY)
-        for (int s = lane; s < ns; s += 32) sum += __expf(wl[s] - mx);
+    if (mx != -INFINITY) {
+        sum = lane < ns ? __expf(l_first - mx) : 0.0f;
+        for (int s = lane + 32; s < ns; s += 32) sum += __expf(wl[s] - mx);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     const float lse = sum > 0.0f ? mx + logf(sum) : -INFINITY;
-    constexpr int PER = D / 32;
     float acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.0f;
     if (sum > 0.0f) {
-        const float* wo = p.ws_o + bh * p.max_splits * D;
-        for (int s = 0; s < ns; ++s) {
-            const float w = __expf(wl[s] - lse);
-            if (PER == 4) {
-                const float4 v = *reinterpret_cast<const float4*>(wo + (long long)s * D + lane * 4);
-                acc[0] += w * v.x;
-                acc[1 % PER] += w * v.y;
-                acc[2 % PER] += w * v.z;
-                acc[3 % PER] += w * v.w;
-            } else {
-                const float2 v = *reinterpret_cast<const float2*>(wo + (long long)s * D + lane * 2);
-                acc[0] += w * v.x;
-                acc[1 % PER] += w * v.y;
+        for (int s0 = 0; s0 < ns; s0 += 32) {
+            const int cnt32 = min(32, ns - s0);  // warp-uniform
+            // the weight of split s0 + i sits in lane i
+            const float w_lane = lane < cnt32 ? __expf((s0 == 0 ? l_first : wl[s0 + lane]) - lse) : 0.0f;
+            for (int j = 0; j < cnt32; j += UNR) {
+                if (s0 + j > 0) load_rows(s0 + j, min(UNR, cnt32 - j), v);
+#pragma unroll
+                for (int u = 0; u < UNR; ++u) {
+                    const float w = __shfl_sync(0xffffffffu, w_lane, (j + u) & 31);
+                    if (j + u < cnt32) {
+#pragma unroll
+                        for (int e = 0; e < PER; ++e) acc[e] += w * v[u][e];
+                    }
+                }
             }
         }
     }
@@ -702,45 +816,74 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
     if (lane == 0) p.lse[bh] = lse;
 }
 
+// Grid of a split kernel, and the work order it encodes (p.full_rows, p.lpt): rows 0..B-1
+// hold the splits before the last of each sequence (column = split * HG + head group), the
+// rows after them the last split of every sequence, HG columns each, in decreasing length for
+// up to 256 sequences (each CTA of that part ranks the B lengths). Within a row the head
+// groups of one kv head, then the kv heads of one split, are neighbours. With too many rows
+// for the grid (more than 32767 sequences), or with p.order = 0, row b holds all splits of
+// sequence b.
+dim3 split_grid(DecodeParams& p) {
+    const long long HG = (long long)p.Hkv * p.n_groups;
+    const long long X = (p.max_splits > 1 ? p.max_splits - 1 : 1) * HG;
+    const long long full_rows = p.max_splits > 1 ? p.B : 0;
+    const long long part_rows = ((long long)p.B * HG + X - 1) / X;
+    if (p.order != 0 && full_rows + part_rows <= 65535) {
+        p.full_rows = (int)full_rows;
+        p.lpt = p.B <= 256;
+        return dim3((unsigned)X, (unsigned)(full_rows + part_rows));
+    }
+    p.full_rows = -1;
+    p.lpt = 0;
+    return dim3((unsigned)(p.max_splits * HG), (unsigned)p.B);
+}
+
+// The combine kernel after a split kernel on the same stream, as its programmatic dependent.
+template <int D>
+cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
+    const long long rows = (long long)p.B * p.Hkv * p.G;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, p);
+}
+
 template <int D, int GN, int NST>
-cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_t(DecodeParams p, cudaStream_t stream) {
     constexpr int ring = kWarps * NST * 2 * DecLayout<D>::kTileBytes;
     constexpr int merge = (kWarps * GN * D + 2 * kWarps * GN) * 4;
     constexpr int bytes = ring > merge ? ring : merge;
     static std::atomic<bool> attr_set[kMaxAttrDevices];
     cudaError_t e = ensure_smem_attr(decode_split_kernel<D, GN, NST>, bytes, attr_set);
     if (e != cudaSuccess) return e;
-    // head groups of one kv head, then the kv heads of one split, side by side
-    const dim3 grid((unsigned)(p.max_splits * p.Hkv * p.n_groups), p.B);
+    const dim3 grid = split_grid(p);
     decode_split_kernel<D, GN, NST><<<grid, kWarps * 32, bytes, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (p.max_splits > 1) {
-        const long long rows = (long long)p.B * p.Hkv * p.G;
-        decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
-        e = cudaGetLastError();
-    }
+    if (p.max_splits > 1) e = launch_combine<D>(p, stream);
     return e;
 }
 
 template <int D, int GN, int NST, int FMT, int TG>
-cudaError_t launch_fp8_t(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_fp8_t(DecodeParams p, cudaStream_t stream) {
     constexpr int ring = kWarps * NST * 2 * TG * D;
     constexpr int merge = (kWarps * GN * D + 2 * kWarps * GN) * 4;
     constexpr int bytes = ring > merge ? ring : merge;
     static std::atomic<bool> attr_set[kMaxAttrDevices];
     cudaError_t e = ensure_smem_attr(decode_split_fp8_kernel<D, GN, NST, FMT, TG>, bytes, attr_set);
     if (e != cudaSuccess) return e;
-    // head groups of one kv head, then the kv heads of one split, side by side
-    const dim3 grid((unsigned)(p.max_splits * p.Hkv * p.n_groups), p.B);
+    const dim3 grid = split_grid(p);
     decode_split_fp8_kernel<D, GN, NST, FMT, TG><<<grid, kWarps * 32, bytes, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (p.max_splits > 1) {
-        const long long rows = (long long)p.B * p.Hkv * p.G;
-        decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
-        e = cudaGetLastError();
-    }
+    if (p.max_splits > 1) e = launch_combine<D>(p, stream);
     return e;
 }
 

@@ -72,6 +72,8 @@ extern "C" attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_
     if ((st = scratch_address(&scratch)) != ATTN_OK) return st;
     double rescale = 8.0;
     attn_get_option("rescale_threshold", &rescale);
+    double order = 1.0;
+    attn_get_option("decode_order", &order);
 
     attn::DecodeParams p;
     memset(&p, 0, sizeof p);
@@ -99,6 +101,7 @@ extern "C" attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_
     p.scale = scale;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     p.rescale_thr = (float)rescale;
+    p.order = (int)order;
     p.status = status;
     const cudaError_t e = attn::launch_attn_decode(p, d, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

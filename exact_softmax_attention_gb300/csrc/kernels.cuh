@@ -95,6 +95,12 @@ struct DecodeParams {
     int G, g_base, g_stride, n_groups;
     int chunk;       // tokens per split (multiple of 64)
     int max_splits;  // splits per sequence the workspace holds
+    // Work order of the split kernels. order (set by the caller): 1 = the last split of every
+    // sequence after all the others, 0 = one grid row per sequence with all its splits. The
+    // launcher derives full_rows and lpt: grid rows y < full_rows list the splits of sequence y
+    // before its last one, the rows after them the last split of every sequence (in decreasing
+    // length when lpt != 0); full_rows < 0: row y holds all splits of sequence y.
+    int order, full_rows, lpt;
     float scale, scale_log2, rescale_thr;
     float v_descale;  // FP8 caches: value descale applied to the output (bf16 caches: unused)
     int* status;

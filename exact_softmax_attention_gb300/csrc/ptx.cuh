@@ -60,18 +60,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Probe that may suspend the thread for up to about hint_ns (or until the phase completes).
-__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
+// Programmatic dependent launch: a grid launched with programmatic stream serialization may
+// start before the grid ahead of it on the stream ends. The earlier grid lets it start by
+// executing grid_dependents_launch in each of its CTAs (or by ending); the later one waits in
+// grid_dependency_wait until the earlier grid has completed and its memory writes are visible.
+// Without a programmatic launch both are no-ops.
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Non-blocking probe of the phase with the given parity.
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {

@@ -275,6 +275,11 @@ attn_status_t attn_get_device_status(void* stream);
  *                        sequences ("FlashAttention4 精读" section 3.3, LPT for varlen);
  *                        0 keeps the sequences in the caller's order (each sequence's
  *                        blocks still heaviest first), for measuring what the sort gains
+ *   "decode_order"       paged decode: 1 (default) the CTAs of every sequence's last split
+ *                        (shorter than the others in general) start after all other splits,
+ *                        longest first for up to 256 sequences, so they fill the SMs that the
+ *                        last full-length splits leave idle (LPT, as for the forward); 0 the
+ *                        splits sequence by sequence
  * Returns ATTN_ERR_BAD_ARG for an unknown name or an invalid value.
  */
 attn_status_t attn_set_option(const char* name, double value);

@@ -158,7 +158,8 @@ def test_options_roundtrip():
     with pytest.raises(A.AttnError):
         A.attn_set_option("exp_poly", 3)
     # forward pipeline switches: 0 or 1 only
-    for name, default in (("correction", 0), ("unroll_kv", 0), ("packed_order", 1), ("dynamic_order", 1)):
+    for name, default in (("correction", 0), ("unroll_kv", 0), ("packed_order", 1), ("dynamic_order", 1),
+                          ("decode_order", 1)):
         assert A.attn_get_option(name) == default
         A.attn_set_option(name, 1 - default)
         assert A.attn_get_option(name) == 1 - default

@@ -116,6 +116,26 @@ def test_fp8_split_count_does_not_change_result(A):
         assert (lse - outs[0][1]).abs().max().item() <= 2e-3
 
 
+@pytest.mark.parametrize("fmt,d,seed", [("e4m3", 128, 35), ("e5m2", 64, 36)])
+def test_fp8_decode_order_switch_is_exact(A, fmt, d, seed):
+    """Both split orders give the same bytes (splits move between CTAs, tokens stay in their
+    split), and those match the oracle."""
+    c = fcase("order_" + fmt, 29, 16, 4, d, 16, 1, 7000, seed, fmt)
+    q, kc8, vc8, pt, sl, kds, vds = c.generate_fp8()
+    outs = []
+    try:
+        for order in (0, 1):
+            A.attn_set_option("decode_order", order)
+            outs.append(run(A, c, q, kc8, vc8, pt, sl, kds, vds))
+    finally:
+        A.attn_set_option("decode_order", 1)
+    (o0, l0), (o1, l1) = outs
+    assert torch.equal(o0.view(torch.int16), o1.view(torch.int16)) and torch.equal(l0, l1)
+    ro, rl = reference(c, q, kc8, vc8, pt, sl, kds, vds)
+    do, dl = compare(o1, l1, ro, rl)
+    assert do <= TOL_O and dl <= TOL_LSE, f"max|dO|={do:.3e} max|dLSE|={dl:.3e}"
+
+
 def test_fp8_decode_workload_full(A):
     """The full e4m3 decode workload (64 sequences, lengths up to 32768), every sequence and head."""
     c = W.decode_fp8()

@@ -70,6 +70,7 @@ CASES = [
     (dcase("g32_mqa", 3, 32, 1, 128, 16, 100, 3000, 13), 0),     # two groups of 16 heads
     (dcase("g24_d64", 3, 48, 2, 64, 8, 1, 2500, 14), 0),       # 16 + 8 heads per kv head
     (dcase("g40_split2", 2, 40, 1, 128, 16, 2000, 4000, 15), 2),
+    (dcase("b300_unranked", 300, 4, 2, 64, 16, 1, 700, 16), 3),  # over 256 sequences: last splits unsorted
 ]
 
 
@@ -111,3 +112,26 @@ def test_bad_page_index_is_reported(A):
                                       c.max_pages, c.scale)
     do, dl = compare(o[:1], lse[:1], ro[:1], rl[:1])
     assert do <= TOL_O and dl <= TOL_LSE
+
+
+@pytest.mark.parametrize("c,ns", [(dcase("order_mix", 37, 16, 4, 128, 16, 1, 6000, 17), 0),
+                                  (dcase("order_b300", 300, 8, 2, 64, 8, 1, 900, 18), 4),
+                                  (dcase("order_one_split", 5, 8, 2, 128, 16, 1, 900, 19), 1)],
+                         ids=["mix", "b300", "one_split"])
+def test_decode_order_switch_is_exact(A, c, ns):
+    """The work order moves splits between CTAs, not tokens between splits: both orders give
+    the same bytes, and those match the oracle."""
+    q, kc, vc, pt, sl = c.generate()
+    outs = []
+    try:
+        for order in (0, 1):
+            A.attn_set_option("decode_order", order)
+            outs.append(run_decode(A, c, q, kc, vc, pt, sl, ns))
+    finally:
+        A.attn_set_option("decode_order", 1)
+    assert A.attn_get_device_status() == 0
+    (o0, l0), (o1, l1) = outs
+    assert torch.equal(o0.view(torch.int16), o1.view(torch.int16)) and torch.equal(l0, l1)
+    ro, rl = oracle.attn_decode_paged(q, kc, vc, pt, sl, c.page_size, c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.scale)
+    do, dl = compare(o1, l1, ro, rl)
+    assert do <= TOL_O and dl <= TOL_LSE, f"{c.name}: max|dO|={do:.3e} max|dLSE|={dl:.3e}"
