@@ -26,6 +26,7 @@ sample of the same workload on this machine's host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -59,14 +60,21 @@ PROFILE_CASES = {
     "long_causal_h32": W.long_causal,
     "long_causal_d256": lambda: W.PrefillCase("long_causal_d256", 1, 32, 32, 8192, 8192, 256, 1.0 / 16.0, True,
                                               W.long_causal().seed, 2.0),
+    # the paged decode workload's first 16 sequences (864 MB of bf16 cache, 432 MB of e4m3)
+    "decode_b16": lambda: dataclasses.replace(W.decode(), name="decode_b16", B=16, seqlens=W.decode().seqlens[:16]),
+    "decode_b16_e4m3": lambda: dataclasses.replace(W.decode_fp8(), name="decode_b16_e4m3", B=16,
+                                                   seqlens=W.decode().seqlens[:16]),
 }
 
 
 def run_profile_case(name):
-    """attn_fwd four times on one case (the fourth launch is the one to capture)."""
+    """attn_fwd (or the paged decode) four times on one case (the fourth launch is the one to capture)."""
     import torch
     import exact_softmax_attention_gb300 as A
     c = PROFILE_CASES[name]()
+    if isinstance(c, W.DecodeCase):
+        run_profile_decode(A, c)
+        return
     q, k, v = c.generate()
     dev = lambda a: torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
     Q, K, V = dev(q), dev(k), dev(v)
@@ -79,6 +87,32 @@ def run_profile_case(name):
     if st != 0:
         raise RuntimeError(A.status_string(st))
     print(json.dumps({"profile_case": name, "flops_per_call": c.flops()}))
+
+
+def run_profile_decode(A, c):
+    import torch
+    dev16 = lambda a: torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    if c.kv_fmt == "bf16":
+        q, kc, vc, pt, sl = c.generate()
+        KC, VC = dev16(kc), dev16(vc)
+    else:
+        q, kc, vc, pt, sl, kds, vds = c.generate_fp8()
+        KC, VC = torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
+    Q, PT, SL = dev16(q), torch.from_numpy(pt).cuda(), torch.from_numpy(sl).cuda()
+    O = torch.empty((c.B, c.Hq, c.d), dtype=torch.bfloat16, device="cuda")
+    L = torch.empty((c.B, c.Hq), dtype=torch.float32, device="cuda")
+    for _ in range(4):
+        if c.kv_fmt == "bf16":
+            A.attn_decode_paged(Q, KC, VC, PT, SL, c.page_size, O, L, None, c.B, c.Hq, c.Hkv, c.d, c.max_pages,
+                                c.num_pages, c.scale, 0)
+        else:
+            A.attn_decode_paged_fp8(Q, KC, VC, PT, SL, c.page_size, O, L, None, c.B, c.Hq, c.Hkv, c.d, c.max_pages,
+                                    c.num_pages, c.scale, 0, c.kv_fmt, kds, vds)
+    torch.cuda.synchronize()
+    st = A.attn_get_device_status()
+    if st != 0:
+        raise RuntimeError(A.status_string(st))
+    print(json.dumps({"profile_case": c.name, "bytes_per_call": c.bytes()}))
 
 
 def parse():

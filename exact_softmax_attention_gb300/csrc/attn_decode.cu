@@ -38,6 +38,16 @@ constexpr int kGroup = 16;  // tokens per warp-stage
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
+// Page-table index and slot of token tok (0 <= tok < 2^31) without an integer division: the
+// launcher's multiplier m = ceil(2^(31+k) / page_size), k = ceil(log2 page_size), makes
+// floor(tok * m / 2^(31+k)) the exact quotient for every 31-bit tok (Granlund and Montgomery,
+// "Division by invariant integers using multiplication", 1994).
+__device__ __forceinline__ int page_index(const DecodeParams& p, int tok, int& slot) {
+    const int q = p.ps_magic ? (int)(__umulhi((unsigned)tok, p.ps_magic) >> p.ps_shift) : tok;
+    slot = tok - q * p.page_size;
+    return q;
+}
+
 template <int D>
 struct DecLayout {
     static constexpr int kRowBytes = D * 2;
@@ -254,12 +264,13 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeP
     // ---- per-warp ring
     uint8_t* ring = smem + warp * NST * 2 * L::kTileBytes;
     const uint32_t ring_s = smem_u32(ring);
-    const long long row_stride = (long long)p.Hkv * D;  // elements between consecutive cache rows
+    const int row_stride = p.Hkv * D;  // elements between consecutive cache rows
     const int* pt = p.page_table + (long long)b * p.max_pages;
     constexpr int kRowsPerIter = 32 / L::kChunksPerRow;
     constexpr int kIters = kGroup / kRowsPerIter;
     const int my_chunk = lane % L::kChunksPerRow;
     const int my_row0 = lane / L::kChunksPerRow;
+    const int col = kvh * D + my_chunk * 8;  // this lane's chunk of its kv head's row (Hkv * D < 2^23)
 
     // groups handled by this warp: t_begin + 16 * (warp + 4 * i)
     const int n_groups_total = cdiv(t_end - t_begin, kGroup);
@@ -270,28 +281,26 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeP
         const int g = t_begin + kGroup * (warp + kWarps * i);
         // lane r (r < 16) resolves row r of the group once; others mirror lanes 0-15
         const int tok = g + (lane & 15);
-        long long off = 0;
-        int ok = 0;
+        int row = -1;  // cache row (page * page_size + slot) of this lane's token, -1: none
         if (tok < t_end) {
-            const int pg = __ldg(pt + tok / p.page_size);
-            if (pg >= 0 && pg < p.num_pages) {
-                off = ((long long)pg * p.page_size + (tok % p.page_size)) * row_stride + (long long)kvh * D;
-                ok = 1;
-            } else {
+            int pslot;
+            const int pg = __ldg(pt + page_index(p, tok, pslot));
+            if (pg >= 0 && pg < p.num_pages)
+                row = pg * p.page_size + pslot;  // < num_pages * page_size <= INT32_MAX
+            else
                 atomicCAS(p.status, 0, kDevBadIndex);
-            }
         }
         const uint32_t kdst = ring_s + slot * 2 * L::kTileBytes;
         const uint32_t vdst = kdst + L::kTileBytes;
 #pragma unroll
         for (int it = 0; it < kIters; ++it) {
             const int r = it * kRowsPerIter + my_row0;
-            const long long ro = __shfl_sync(0xffffffffu, off, r);
-            const int rok = __shfl_sync(0xffffffffu, ok, r);
-            const __nv_bfloat16* ks = rok ? p.k_cache + ro + my_chunk * 8 : p.k_cache;
-            const __nv_bfloat16* vs = rok ? p.v_cache + ro + my_chunk * 8 : p.v_cache;
-            cp_async16(kdst + swz<D>(r, my_chunk), ks, rok ? 16u : 0u);
-            cp_async16(vdst + swz<D>(r, my_chunk), vs, rok ? 16u : 0u);
+            const int rr = __shfl_sync(0xffffffffu, row, r);
+            const long long ro = (long long)rr * row_stride + col;
+            const __nv_bfloat16* ks = rr >= 0 ? p.k_cache + ro : p.k_cache;
+            const __nv_bfloat16* vs = rr >= 0 ? p.v_cache + ro : p.v_cache;
+            cp_async16(kdst + swz<D>(r, my_chunk), ks, rr >= 0 ? 16u : 0u);
+            cp_async16(vdst + swz<D>(r, my_chunk), vs, rr >= 0 ? 16u : 0u);
         }
     };
 
@@ -553,34 +562,33 @@ __global__ void __launch_bounds__(kWarps * 32, (fp8_min_blocks<D, TG, NST>())) d
     constexpr int kIters = TG / kRowsPerIter;
     const int my_chunk = lane % kChunks;
     const int my_row0 = lane / kChunks;
+    const int col = kvh * D + my_chunk * 16;  // this lane's chunk of its kv head's row (Hkv * D < 2^23)
     const int n_groups_total = cdiv(t_end - t_begin, TG);
     const int my_groups = n_groups_total > warp ? cdiv(n_groups_total - warp, kWarps) : 0;
 
-    const long long row_stride = (long long)p.Hkv * D;  // bytes between consecutive cache rows
+    const int row_stride = p.Hkv * D;  // bytes between consecutive cache rows
     auto issue = [&](int i) {
         const int slot = i % NST;
         const int g = t_begin + TG * (warp + kWarps * i);
         const int tok = g + (lane & (TG - 1));
-        long long off = 0;
-        int ok = 0;
+        int row = -1;  // cache row (page * page_size + slot) of this lane's token, -1: none
         if (tok < t_end) {
-            const int pg = __ldg(pt + tok / p.page_size);
-            if (pg >= 0 && pg < p.num_pages) {
-                off = ((long long)pg * p.page_size + (tok % p.page_size)) * row_stride + (long long)kvh * D;
-                ok = 1;
-            } else {
+            int pslot;
+            const int pg = __ldg(pt + page_index(p, tok, pslot));
+            if (pg >= 0 && pg < p.num_pages)
+                row = pg * p.page_size + pslot;  // < num_pages * page_size <= INT32_MAX
+            else
                 atomicCAS(p.status, 0, kDevBadIndex);
-            }
         }
         const uint32_t kdst = ring_s + slot * 2 * kTile;
         const uint32_t vdst = kdst + kTile;
 #pragma unroll
         for (int it = 0; it < kIters; ++it) {
             const int r = it * kRowsPerIter + my_row0;
-            const long long ro = __shfl_sync(0xffffffffu, off, r);
-            const int rok = __shfl_sync(0xffffffffu, ok, r);
-            cp_async16(kdst + swz8<D>(r, my_chunk), rok ? kc + ro + my_chunk * 16 : kc, rok ? 16u : 0u);
-            cp_async16(vdst + swz8<D>(r, my_chunk), rok ? vc + ro + my_chunk * 16 : vc, rok ? 16u : 0u);
+            const int rr = __shfl_sync(0xffffffffu, row, r);
+            const long long ro = (long long)rr * row_stride + col;
+            cp_async16(kdst + swz8<D>(r, my_chunk), rr >= 0 ? kc + ro : kc, rr >= 0 ? 16u : 0u);
+            cp_async16(vdst + swz8<D>(r, my_chunk), rr >= 0 ? vc + ro : vc, rr >= 0 ? 16u : 0u);
         }
     };
 
@@ -908,6 +916,16 @@ cudaError_t launch_fp8_fmt(const DecodeParams& p, int d, cudaStream_t stream) {
 // grid (so the groups share the cache rows in the L2). The combine then merges all heads.
 static DecodeParams grouped(const DecodeParams& p_in) {
     DecodeParams p = p_in;
+    // page divisor: m = ceil(2^(31+k) / page_size) < 2^32 with k = ceil(log2 page_size)
+    p.ps_magic = 0;
+    p.ps_shift = 0;
+    if (p.page_size > 1) {
+        int k = 0;
+        while ((1LL << k) < p.page_size) ++k;
+        const unsigned long long num = 1ULL << (31 + k);
+        p.ps_magic = (unsigned)((num + (unsigned long long)p.page_size - 1) / (unsigned long long)p.page_size);
+        p.ps_shift = k - 1;
+    }
     p.n_groups = (p_in.g_stride + 15) / 16;
     p.g_base = 0;
     p.G = p_in.g_stride;

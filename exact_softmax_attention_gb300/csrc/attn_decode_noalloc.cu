@@ -51,6 +51,7 @@ extern "C" attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128) || page_size <= 0 ||
         max_pages_per_seq <= 0 || num_pages <= 0 || num_splits < 0 || B > 65535 || Hkv > 65535)
         return ATTN_ERR_BAD_SHAPE;
+    if ((long long)num_pages * page_size > INT32_MAX) return ATTN_ERR_BAD_SHAPE;  // cache rows are 32-bit indices
     if (!isfinite(scale)) return ATTN_ERR_BAD_SHAPE;
     if (!aligned(q, 16) || !aligned(o, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(lse, 4) ||
         !aligned(page_table, 4) || !aligned(seqlens, 4))

@@ -101,6 +101,10 @@ struct DecodeParams {
     // before its last one, the rows after them the last split of every sequence (in decreasing
     // length when lpt != 0); full_rows < 0: row y holds all splits of sequence y.
     int order, full_rows, lpt;
+    // tok / page_size for 0 <= tok < 2^31 is __umulhi(tok, ps_magic) >> ps_shift (set by the
+    // launcher; page_size 1: ps_magic = 0 and the quotient is tok).
+    unsigned int ps_magic;
+    int ps_shift;
     float scale, scale_log2, rescale_thr;
     float v_descale;  // FP8 caches: value descale applied to the output (bf16 caches: unused)
     int* status;

@@ -150,8 +150,9 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
  *            of one tile, so more than 16 per kv head run as groups of 16 (one CTA each, in the
  *            same launch, neighbours in the grid so that they share the cache rows in the L2)
  * max_pages_per_seq  columns of page_table (>= 1)
- * num_pages  physical pages in each cache (>= 1); a page index outside [0, num_pages) is
- *            not read: its rows count as zeros and ATTN_ERR_DEVICE_BAD_INDEX is recorded
+ * num_pages  physical pages in each cache (>= 1, num_pages * page_size <= 2^31 - 1 cache rows);
+ *            a page index outside [0, num_pages) is not read: its rows count as zeros and
+ *            ATTN_ERR_DEVICE_BAD_INDEX is recorded
  * scale      as for attn_fwd
  * num_splits 0: choose the number of key splits from the SM count and the sizes;
  *            n > 0: split every sequence's keys into at most n chunks.

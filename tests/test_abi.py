@@ -77,6 +77,7 @@ def test_decode_host_validation(lib):
     assert _dec(lib, ns=-1) == A.ATTN_ERR_BAD_SHAPE
     assert _dec(lib, kc=0x1004) == A.ATTN_ERR_ALIGN
     assert _dec(lib, sl=0x1002) == A.ATTN_ERR_ALIGN
+    assert _dec(lib, ps=1 << 16, npg=1 << 15) == A.ATTN_ERR_BAD_SHAPE  # 2^31 cache rows: indices are 32-bit
     assert _dec(lib, B=0) == A.ATTN_OK
 
 
@@ -124,6 +125,7 @@ def test_fp8_decode_host_validation(lib):
     assert _dec8(lib, pt=None) == A.ATTN_ERR_NULL_PTR
     assert _dec8(lib, d=96) == A.ATTN_ERR_BAD_SHAPE
     assert _dec8(lib, vc=0x1008) == A.ATTN_ERR_ALIGN
+    assert _dec8(lib, ps=3, npg=(1 << 31) // 3 + 1) == A.ATTN_ERR_BAD_SHAPE
     assert _dec8(lib, fmt=1, B=0) == A.ATTN_OK
 
 
@@ -168,3 +170,23 @@ def test_options_roundtrip():
             A.attn_set_option(name, 2)
     assert "sm_103a" in A.attn_version()
     assert A.status_string(A.ATTN_ERR_DEVICE_TIMEOUT).startswith("a kernel gave up")
+
+
+def test_page_divisor_scheme():
+    """The decode kernels divide token indices by the page size with a multiply and a shift:
+    m = ceil(2^(31+k) / page_size), k = ceil(log2 page_size), quotient (tok * m >> 32) >> (k - 1).
+    Exact for every 31-bit tok (the bound the launcher relies on), checked here on the edges."""
+    import random
+    rng = random.Random(5)
+    sizes = list(range(2, 2100)) + [2 ** j for j in range(1, 31)] + [2 ** j + 1 for j in range(1, 31)] + \
+        [2 ** j - 1 for j in range(2, 32)] + [rng.randrange(2, 2 ** 31) for _ in range(300)]
+    for d in sizes:
+        k = (d - 1).bit_length()
+        m = -(-(1 << (31 + k)) // d)
+        assert m < 1 << 32
+        top = (1 << 31) - 1
+        ns = {0, 1, d - 1, d, d + 1, top, top - top % d, top - top % d - 1} | {rng.randrange(0, 1 << 31) for _ in range(20)}
+        for n in ns:
+            if 0 <= n <= top:
+                assert ((n * m) >> 32) >> (k - 1) == n // d, (d, n)
+

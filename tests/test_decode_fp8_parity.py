@@ -67,6 +67,9 @@ CASES = [
     (fcase("e4m3_edges_d64", 0, 8, 2, 64, 16, 0, 0, 33, "e4m3",
            lens=[0, 1, 31, 32, 33, 47, 63, 64, 65, 95, 96, 97, 1023, 1024, 1025]), 0),
     (fcase("e5m2_edges_d64_split3", 0, 8, 2, 64, 5, 0, 0, 34, "e5m2", lens=[1, 33, 95, 130, 1000, 1600]), 3),
+    (fcase("e4m3_p3", 5, 8, 2, 128, 3, 1, 2000, 37, "e4m3"), 0),   # page sizes that are not powers of two
+    (fcase("e4m3_p100_d64", 4, 8, 1, 64, 100, 1, 5000, 38, "e4m3"), 0),
+    (fcase("e5m2_p1000", 3, 8, 2, 128, 1000, 500, 7000, 39, "e5m2"), 2),
 ]
 
 

@@ -71,6 +71,9 @@ CASES = [
     (dcase("g24_d64", 3, 48, 2, 64, 8, 1, 2500, 14), 0),       # 16 + 8 heads per kv head
     (dcase("g40_split2", 2, 40, 1, 128, 16, 2000, 4000, 15), 2),
     (dcase("b300_unranked", 300, 4, 2, 64, 16, 1, 700, 16), 3),  # over 256 sequences: last splits unsorted
+    (dcase("p3", 5, 8, 2, 128, 3, 1, 2000, 20), 0),              # page sizes that are not powers of two
+    (dcase("p100_d64", 4, 8, 1, 64, 100, 1, 5000, 21), 0),
+    (dcase("p1000", 3, 8, 2, 128, 1000, 500, 7000, 22), 2),
 ]
 
 
