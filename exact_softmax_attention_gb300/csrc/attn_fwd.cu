@@ -1275,7 +1275,8 @@ template <int D, int POLY, int F8, int DV = D, int BNT = BN, int UKV = 0, int CO
 cudaError_t launch_t(const FwdTmaps& tm, const FwdParams& p, int grid, cudaStream_t stream) {
     using L = Layout<D, F8, DV, BNT>;
     static std::atomic<bool> attr_set[kMaxAttrDevices];
-    const cudaError_t e = ensure_smem_attr(attn_fwd_kernel<D, POLY, F8, DV, BNT, UKV, CORR>, L::kAlloc, attr_set);
+    // the warp groups' setmaxnreg shares add up to the launch's 512 x 128 registers
+    const cudaError_t e = ensure_smem_attr(attn_fwd_kernel<D, POLY, F8, DV, BNT, UKV, CORR>, L::kAlloc, attr_set, 128);
     if (e != cudaSuccess) return e;
     attn_fwd_kernel<D, POLY, F8, DV, BNT, UKV, CORR><<<grid, kThreads, L::kAlloc, stream>>>(tm.q, tm.k, tm.v, p);
     return cudaGetLastError();

@@ -15,11 +15,21 @@ namespace attn {
 // attribute twice is harmless, so a race only repeats that call.
 constexpr int kMaxAttrDevices = 64;
 template <typename Kernel>
-inline cudaError_t ensure_smem_attr(Kernel kernel, int bytes, std::atomic<bool> (&done)[kMaxAttrDevices]) {
+// min_regs: registers per thread the kernel must have been built with (a kernel that moves
+// registers between warp groups with setmaxnreg hands out exactly the launch's total); a build
+// with fewer is refused (cudaErrorInvalidConfiguration) instead of launched.
+inline cudaError_t ensure_smem_attr(Kernel kernel, int bytes, std::atomic<bool> (&done)[kMaxAttrDevices],
+                                    int min_regs = 0) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxAttrDevices && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    if (min_regs > 0) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kernel);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs < min_regs) return cudaErrorInvalidConfiguration;
+    }
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess && dev >= 0 && dev < kMaxAttrDevices) done[dev].store(true, std::memory_order_release);
     return e;
