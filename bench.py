@@ -60,6 +60,13 @@ PROFILE_CASES = {
     "long_causal_h32": W.long_causal,
     "long_causal_d256": lambda: W.PrefillCase("long_causal_d256", 1, 32, 32, 8192, 8192, 256, 1.0 / 16.0, True,
                                               W.long_causal().seed, 2.0),
+    "long_causal_hd": lambda: dataclasses.replace(W.long_causal(), name="long_causal_hd", d=192,
+                                                  scale=1.0 / math.sqrt(192), dv=128),
+    "long_causal_e4m3": W.long_causal,  # Q/K/V as e4m3 codes
+    "prefill_2k": lambda: W.prefill(False),
+    "prefill_2k_causal": lambda: W.prefill(True),
+    "varlen_gqa": W.varlen_gqa,
+    "tiny": W.tiny,
     # the paged decode workload's first 16 sequences (864 MB of bf16 cache, 432 MB of e4m3)
     "decode_b16": lambda: dataclasses.replace(W.decode(), name="decode_b16", B=16, seqlens=W.decode().seqlens[:16]),
     "decode_b16_e4m3": lambda: dataclasses.replace(W.decode_fp8(), name="decode_b16_e4m3", B=16,
@@ -67,21 +74,38 @@ PROFILE_CASES = {
 }
 
 
-def run_profile_case(name):
-    """attn_fwd (or the paged decode) four times on one case (the fourth launch is the one to capture)."""
+def run_profile_case(name, options=()):
+    """attn_fwd (attn_fwd_hd, attn_fwd_fp8 or the paged decode, as the case needs) four times on
+    one case, after the library options given; the fourth launch is the one to capture."""
     import torch
     import exact_softmax_attention_gb300 as A
+    for opt in options:
+        n, v = opt.split("=", 1)
+        A.attn_set_option(n, float(v))
     c = PROFILE_CASES[name]()
     if isinstance(c, W.DecodeCase):
         run_profile_decode(A, c)
         return
-    q, k, v = c.generate()
-    dev = lambda a: torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
-    Q, K, V = dev(q), dev(k), dev(v)
-    O = torch.empty((c.total_q, c.Hq, c.d), dtype=torch.bfloat16, device="cuda")
+    fp8 = name.endswith("_e4m3")
+    dev16 = lambda a: torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    if fp8:
+        q8, k8, v8, qs, ks, vs = c.generate_fp8("e4m3")
+        Q, K, V = (torch.from_numpy(a).cuda() for a in (q8, k8, v8))
+    else:
+        q, k, v = c.generate()
+        Q, K, V = dev16(q), dev16(k), dev16(v)
+    dv = c.dv if c.dv else c.d
+    O = torch.empty((c.total_q, c.Hq, dv), dtype=torch.bfloat16, device="cuda")
     L = torch.empty((c.total_q, c.Hq), dtype=torch.float32, device="cuda")
+    CU = None if c.cu_seqlens is None else torch.from_numpy(c.cu_seqlens).cuda()
+    nq, nk = (c.Nq, c.Nk) if CU is None else (c.total_q, c.total_k)
     for _ in range(4):
-        A.attn_fwd(Q, K, V, O, L, c.B, c.Hq, c.Hkv, c.Nq, c.Nk, c.d, c.scale, c.causal)
+        if fp8:
+            A.attn_fwd_fp8(Q, K, V, O, L, c.B, c.Hq, c.Hkv, nq, nk, c.d, c.scale, c.causal, CU, None, "e4m3", qs, ks, vs)
+        elif dv != c.d:
+            A.attn_fwd_hd(Q, K, V, O, L, c.B, c.Hq, c.Hkv, nq, nk, c.d, dv, c.scale, c.causal, CU, None)
+        else:
+            A.attn_fwd(Q, K, V, O, L, c.B, c.Hq, c.Hkv, nq, nk, c.d, c.scale, c.causal, CU)
     torch.cuda.synchronize()
     st = A.attn_get_device_status()
     if st != 0:
@@ -856,7 +880,7 @@ def run_e2e(torch, A, dev, stream, barrier, world, steps, fc, dc, fin, din, fdev
 def main():
     args = parse()
     if args.profile_case:
-        run_profile_case(args.profile_case)
+        run_profile_case(args.profile_case, args.option)
     elif args.impl == "reference":
         run_reference(args)
     else:
