@@ -158,6 +158,11 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
  *            n > 0: split every sequence's keys into at most n chunks.
  * Workspace: partial outputs of the splits live in memory taken from a library-owned
  * stream-ordered pool on `stream` and returned to it on `stream` after the combine.
+ * Launches: a split kernel and, when a sequence has more than one split, a combine kernel
+ * launched as its programmatic dependent (it may start while the split kernel finishes and
+ * waits on the device for its results). Work after the call on `stream` sees both done, as
+ * for any pair of launches; a kernel the caller launches with programmatic stream
+ * serialization must wait (griddepcontrol.wait) before it reads o or lse.
  * Alignment: q, o, k_cache, v_cache 16 bytes; lse, page_table, seqlens 4 bytes.
  */
 attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* page_table,
