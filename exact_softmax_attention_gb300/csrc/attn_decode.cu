@@ -2,9 +2,9 @@
 //
 // "Faster, more flexible FA4 for LLM inference":
 //  - PR 1999/2104: pages of any size are gathered with per-thread cp.async rather than
-//    TMA, and the 64-bit row addresses are generated once per row and handed out by
-//    warp shuffles ("transposed" address generation) instead of being recomputed by
-//    every thread that copies a piece of the row;
+//    TMA, and each row's location (page-table lookup, then a 32-bit cache row index) is
+//    resolved once per row and handed out by warp shuffles ("transposed" address
+//    generation) instead of being recomputed by every thread that copies a piece of it;
 //  - PR 1940: split-KV (Flash-Decoding): several CTAs share one sequence's keys, each
 //    writes a partial output and its log-sum-exp, and a separate combine kernel merges
 //    them; num_splits = 0 picks the split size from the SM count and the lengths;
