@@ -174,7 +174,9 @@ def peaks():
 
 def kernel_sources(kernel: str):
     """The source files a kernel is compiled from."""
-    return ["attn_decode.cu" if kernel.startswith("decode") else "attn_fwd.cu", "ptx.cuh", "kernels.cuh"]
+    if kernel.startswith("decode"):
+        return ["attn_decode.cu", "decode_maps.cuh", "ptx.cuh", "kernels.cuh"]
+    return ["attn_fwd.cu", "ptx.cuh", "kernels.cuh"]
 
 
 def source_sha(kernel: str) -> str:

@@ -2,6 +2,7 @@
 // the device status word and process-wide options. Every compute step runs in the
 // kernels of attn_fwd.cu and attn_decode.cu.
 #include "attn.h"
+#include "decode_maps.cuh"
 #include "kernels.cuh"
 
 #include <cudaTypedefs.h>
@@ -34,6 +35,7 @@ struct Options {
     int unroll_kv = 0;
     int dynamic_order = 1;
     int decode_order = 1;
+    int decode_maps = 1;
 };
 
 std::mutex g_mu;
@@ -101,6 +103,19 @@ attn_status_t make_map(CUtensorMap* m, const void* base, long long rows, int hea
     CUresult r = g_encode(m, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
                           const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// 2-D map over a paged cache of 8-bit codes viewed as [rows, row_bytes] (row_bytes = Hkv * d):
+// box d bytes x 16 rows, 128-byte swizzle (the layout the decode kernel's rings use).
+attn_status_t make_cache_map(CUtensorMap* m, const void* base, long long rows, int row_bytes, int d) {
+    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)d, (cuuint32_t)attn::kDecodeMapRows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -193,6 +208,9 @@ attn_status_t attn_set_option(const char* name, double value) {
     } else if (!strcmp(name, "decode_order")) {
         if (value != 0 && value != 1) return ATTN_ERR_BAD_ARG;
         g_opt.decode_order = (int)value;
+    } else if (!strcmp(name, "decode_maps")) {
+        if (value != 0 && value != 1) return ATTN_ERR_BAD_ARG;
+        g_opt.decode_maps = (int)value;
     } else {
         return ATTN_ERR_BAD_ARG;
     }
@@ -213,6 +231,7 @@ attn_status_t attn_get_option(const char* name, double* value) {
     else if (!strcmp(name, "unroll_kv")) *value = g_opt.unroll_kv;
     else if (!strcmp(name, "dynamic_order")) *value = g_opt.dynamic_order;
     else if (!strcmp(name, "decode_order")) *value = g_opt.decode_order;
+    else if (!strcmp(name, "decode_maps")) *value = g_opt.decode_maps;
     else return ATTN_ERR_BAD_ARG;
     return ATTN_OK;
 }
@@ -481,7 +500,22 @@ static attn_status_t decode_paged(const void* q, const void* k_cache, const void
         p.ws_o = reinterpret_cast<float*>(ws);
         p.ws_lse = p.ws_o + n_o;
     }
-    const cudaError_t e = kv_format < 0 ? attn::launch_attn_decode(p, d, s) : attn::launch_attn_decode_fp8(p, d, kv_format, s);
+    cudaError_t e;
+    if (kv_format < 0) {
+        e = attn::launch_attn_decode(p, d, s);
+    } else if (d == 128 && page_size % attn::kDecodeMapRows == 0 && opt.decode_maps) {
+        // the 16 tokens of a token group lie in one page: one map load per group and tensor
+        attn::DecodeTmaps tm;
+        if ((st = encode_fn()) != ATTN_OK ||
+            (st = make_cache_map(&tm.k, k_cache, (long long)num_pages * page_size, Hkv * d, d)) != ATTN_OK ||
+            (st = make_cache_map(&tm.v, v_cache, (long long)num_pages * page_size, Hkv * d, d)) != ATTN_OK) {
+            if (ws) cudaFreeAsync(ws, s);
+            return st;
+        }
+        e = attn::launch_attn_decode_fp8_maps(p, tm, d, kv_format, s);
+    } else {
+        e = attn::launch_attn_decode_fp8(p, d, kv_format, s);
+    }
     if (ws) cudaFreeAsync(ws, s);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

@@ -25,6 +25,7 @@
 // main loop needs no CTA-wide barrier. Scores S = Q K^T use m16n8k16 bf16 MMAs with the (up to 16) query
 // heads of the group as rows; O^T += V^T P^T reuses the score accumulators as the B
 // operand directly.
+#include "decode_maps.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -483,6 +484,31 @@ __device__ __forceinline__ void lds64(uint32_t addr, uint32_t* w) {
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(addr) : "memory");
 }
 
+// 2-D tiled tensor load into shared memory (dst: shared-window address, 1024-byte aligned for
+// the 128-byte swizzle), completing on an mbarrier.
+__device__ __forceinline__ void map_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+        "[%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// Orders this thread's earlier shared-memory accesses before its later bulk copies into shared
+// memory (the copies write through the async proxy).
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Bounded wait for a token group's map loads: false after kStageWaitNs of global time.
+constexpr uint64_t kStageWaitNs = 2000000000ull;
+__device__ __forceinline__ bool stage_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 15u && global_timer_ns() - t0 > kStageWaitNs) return false;
+    }
+}
+
 // TG tokens per warp-stage (16 or 32). Launch bound: as many CTAs per SM as their rings fit in
 // shared memory, at most four.
 template <int D, int TG, int NST>
@@ -490,15 +516,21 @@ constexpr int fp8_min_blocks() {
     return (232448 / (kWarps * NST * 2 * TG * D)) < 4 ? (232448 / (kWarps * NST * 2 * TG * D)) : 4;
 }
 
-template <int D, int GN, int NST, int FMT, int TG>
-__global__ void __launch_bounds__(kWarps * 32, (fp8_min_blocks<D, TG, NST>())) decode_split_fp8_kernel(const DecodeParams p) {
+// TM: the K/V rows of a token group come from one tensor-map load each (the group lies within
+// one page); else every lane copies 16-byte pieces of its token's rows with cp.async.
+template <int D, int GN, int NST, int FMT, int TG, bool TM>
+__global__ void __launch_bounds__(kWarps * 32, (fp8_min_blocks<D, TG, NST>()))
+    decode_split_fp8_kernel(const DecodeParams p, const __grid_constant__ DecodeTmaps tm) {
     grid_dependents_launch();  // the combine kernel may be scheduled once every split CTA runs
     static_assert(TG == 16 || TG == 32, "tokens per warp-stage");
+    static_assert(!TM || (D == 128 && TG == kDecodeMapRows), "map loads: 128-byte rows, one group per load");
     constexpr int kTile = TG * D;       // bytes of one K or V warp-stage tile
     constexpr int NT = TG / 8;          // n-tiles of 8 tokens in S = Q K^T
     constexpr int KS = TG / 16;         // k-steps of 16 tokens in O^T += V^T P^T
     constexpr int kChunks = D / 16;     // 16-byte chunks per cache row
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    // map loads write the 128-byte swizzle relative to 1024-byte boundaries: the rings start on one
+    uint8_t* smem = TM ? smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) : smem_raw;
     // hg = kv head * n_groups + group of 16 query heads: the groups of one kv head are neighbours
     // in launch order, so they read the same cache rows at about the same time and all but the
     // first find them in the L2.
@@ -592,6 +624,36 @@ __global__ void __launch_bounds__(kWarps * 32, (fp8_min_blocks<D, TG, NST>())) d
         }
     };
 
+    // map loads: one barrier per warp-stage after the rings (one arrival: lane 0, with the bytes)
+    uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + kWarps * NST * 2 * kTile) + warp * NST;
+    if constexpr (TM) {
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < NST; ++i) mbar_init(&sbar[i], 1);
+            fence_mbar_init();
+        }
+        __syncwarp();
+    }
+    auto issue_map = [&](int i) {
+        if (lane == 0) {
+            const int slot = i % NST;
+            const int g = t_begin + TG * (warp + kWarps * i);  // a multiple of 16: the group lies in one page
+            int pslot;
+            const int pg = __ldg(pt + page_index(p, g, pslot));
+            int row0 = 0;
+            if (pg >= 0 && pg < p.num_pages)
+                row0 = pg * p.page_size + pslot;
+            else
+                atomicCAS(p.status, 0, kDevBadIndex);
+            uint64_t* bar = &sbar[slot];
+            fence_async_smem();  // the warp's reads of this slot (ordered by __syncwarp) before the copies
+            mbar_arrive_expect_tx(bar, 2 * kTile);
+            const uint32_t kdst = ring_s + slot * 2 * kTile;
+            map_load_2d(kdst, &tm.k, bar, kvh * D, row0);
+            map_load_2d(kdst + kTile, &tm.v, bar, kvh * D, row0);
+        }
+    };
+
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
     constexpr int NH = GN / 8;
     float oacc[NH][D / 16][4];
@@ -603,21 +665,47 @@ __global__ void __launch_bounds__(kWarps * 32, (fp8_min_blocks<D, TG, NST>())) d
             for (int e = 0; e < 4; ++e) oacc[nh][mt][e] = 0.0f;
     const float sl2 = p.scale_log2;
 
+    if constexpr (TM) {
+        for (int i = 0; i < NST - 1 && i < my_groups; ++i) issue_map(i);
+    } else {
 #pragma unroll
-    for (int i = 0; i < NST - 1; ++i) {
-        if (i < my_groups) issue(i);
-        cp_async_commit();
+        for (int i = 0; i < NST - 1; ++i) {
+            if (i < my_groups) issue(i);
+            cp_async_commit();
+        }
     }
     for (int i = 0; i < my_groups; ++i) {
-        cp_async_wait<NST - 2>();
-        __syncwarp();
-        if (i + NST - 1 < my_groups) issue(i + NST - 1);
-        cp_async_commit();
-
         const int slot = i % NST;
         const uint32_t kt = ring_s + slot * 2 * kTile;
         const uint32_t vt = kt + kTile;
         const int g = t_begin + TG * (warp + kWarps * i);
+        if constexpr (TM) {
+            if (!__all_sync(0xffffffffu, stage_wait(&sbar[slot], (uint32_t)(i / NST) & 1u))) {
+                // loads that never landed: report, let the groups in flight land (bounded), and
+                // leave the loop (the warp still takes part in the merge's barriers)
+                if (lane == 0) atomicCAS(p.status, 0, kDevTimeout);
+                for (int j = i + 1; j < i + NST - 1 && j < my_groups; ++j) stage_wait(&sbar[j % NST], (uint32_t)(j / NST) & 1u);
+                break;
+            }
+            __syncwarp();
+            if (i + NST - 1 < my_groups) issue_map(i + NST - 1);
+            if (g + TG > t_end) {
+                // rows past the sequence's end come from the same page but need not hold finite
+                // codes: zero their V rows (their scores are masked below)
+                const int nv = t_end - g;
+                for (int c = lane; c < (TG - nv) * kChunks; c += 32)
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vt + (nv + c / kChunks) * D +
+                                                                                 (c % kChunks) * 16),
+                                 "r"(0u)
+                                 : "memory");
+                __syncwarp();
+            }
+        } else {
+            cp_async_wait<NST - 2>();
+            __syncwarp();
+            if (i + NST - 1 < my_groups) issue(i + NST - 1);
+            cp_async_commit();
+        }
 
         // K operand bytes: tokens g0 + 8 nt, bytes [(D/4) qd, (D/4) qd + D/4) of the row
         uint32_t kw[NT][D / 16];
@@ -736,7 +824,7 @@ __global__ void __launch_bounds__(kWarps * 32, (fp8_min_blocks<D, TG, NST>())) d
             }
         }
     }
-    cp_async_wait<0>();
+    if constexpr (!TM) cp_async_wait<0>();
     merge_and_store<D, GN, true>(p, smem, oacc, m0, m1, l0, l1, split, nsplit, kvh, b, p.v_descale, G, g_base);
 }
 
@@ -879,16 +967,17 @@ cudaError_t launch_t(DecodeParams p, cudaStream_t stream) {
     return e;
 }
 
-template <int D, int GN, int NST, int FMT, int TG>
-cudaError_t launch_fp8_t(DecodeParams p, cudaStream_t stream) {
+template <int D, int GN, int NST, int FMT, int TG, bool TM>
+cudaError_t launch_fp8_t(DecodeParams p, const DecodeTmaps& tm, cudaStream_t stream) {
     constexpr int ring = kWarps * NST * 2 * TG * D;
     constexpr int merge = (kWarps * GN * D + 2 * kWarps * GN) * 4;
-    constexpr int bytes = ring > merge ? ring : merge;
+    // map loads: the stage barriers after the rings, and up to 1 KB to align the rings
+    constexpr int bytes = (ring > merge ? ring : merge) + (TM ? kWarps * NST * 8 + 1024 : 0);
     static std::atomic<bool> attr_set[kMaxAttrDevices];
-    cudaError_t e = ensure_smem_attr(decode_split_fp8_kernel<D, GN, NST, FMT, TG>, bytes, attr_set);
+    cudaError_t e = ensure_smem_attr(decode_split_fp8_kernel<D, GN, NST, FMT, TG, TM>, bytes, attr_set);
     if (e != cudaSuccess) return e;
     const dim3 grid = split_grid(p);
-    decode_split_fp8_kernel<D, GN, NST, FMT, TG><<<grid, kWarps * 32, bytes, stream>>>(p);
+    decode_split_fp8_kernel<D, GN, NST, FMT, TG, TM><<<grid, kWarps * 32, bytes, stream>>>(p, tm);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.max_splits > 1) e = launch_combine<D>(p, stream);
@@ -899,12 +988,22 @@ cudaError_t launch_fp8_t(DecodeParams p, cudaStream_t stream) {
 // CTA, four CTAs per SM), 32 at d = 64 (the same 48 KB). Measured on the paged decode workload
 // with e4m3 caches: d = 128, 16 tokens 6100 GB/s against 5755 for 32 (two CTAs per SM) and 6070
 // for 32 tokens in two stages; d = 64 (Hkv 16), 32 tokens 6178 against 5250 for 16.
+// Map loads (tm != nullptr) against per-row copies, e4m3 paged decode workload (64 sequences of
+// U[1024, 32768] tokens, page 16): 4 query heads per kv head 6450 against 6415 GB/s, 32 (two
+// groups of 16) 2526 against 2437; 16 query heads per kv head 5420 against 5470, so that shape
+// keeps the per-row copies.
 template <int FMT>
-cudaError_t launch_fp8_fmt(const DecodeParams& p, int d, cudaStream_t stream) {
+cudaError_t launch_fp8_fmt(const DecodeParams& p, const DecodeTmaps* tm, int d, cudaStream_t stream) {
     constexpr int NST = 3;
+    static const DecodeTmaps no_maps = {};
+    if (d == 128 && tm && (p.G <= 8 || p.n_groups > 1))
+        return p.G <= 8 ? launch_fp8_t<128, 8, NST, FMT, 16, true>(p, *tm, stream)
+                        : launch_fp8_t<128, 16, NST, FMT, 16, true>(p, *tm, stream);
     if (d == 128)
-        return p.G <= 8 ? launch_fp8_t<128, 8, NST, FMT, 16>(p, stream) : launch_fp8_t<128, 16, NST, FMT, 16>(p, stream);
-    return p.G <= 8 ? launch_fp8_t<64, 8, NST, FMT, 32>(p, stream) : launch_fp8_t<64, 16, NST, FMT, 32>(p, stream);
+        return p.G <= 8 ? launch_fp8_t<128, 8, NST, FMT, 16, false>(p, no_maps, stream)
+                        : launch_fp8_t<128, 16, NST, FMT, 16, false>(p, no_maps, stream);
+    return p.G <= 8 ? launch_fp8_t<64, 8, NST, FMT, 32, false>(p, no_maps, stream)
+                    : launch_fp8_t<64, 16, NST, FMT, 32, false>(p, no_maps, stream);
 }
 
 }  // namespace
@@ -934,7 +1033,14 @@ static DecodeParams grouped(const DecodeParams& p_in) {
 
 cudaError_t launch_attn_decode_fp8(const DecodeParams& p_in, int d, int fmt, cudaStream_t stream) {
     const DecodeParams p = grouped(p_in);
-    return fmt == 0 ? launch_fp8_fmt<0>(p, d, stream) : launch_fp8_fmt<1>(p, d, stream);
+    return fmt == 0 ? launch_fp8_fmt<0>(p, nullptr, d, stream) : launch_fp8_fmt<1>(p, nullptr, d, stream);
+}
+
+cudaError_t launch_attn_decode_fp8_maps(const DecodeParams& p_in, const DecodeTmaps& tm, int d, int fmt,
+                                        cudaStream_t stream) {
+    if (d != 128 || p_in.page_size % kDecodeMapRows != 0) return cudaErrorInvalidValue;
+    const DecodeParams p = grouped(p_in);
+    return fmt == 0 ? launch_fp8_fmt<0>(p, &tm, d, stream) : launch_fp8_fmt<1>(p, &tm, d, stream);
 }
 
 cudaError_t launch_attn_decode(const DecodeParams& p_in, int d, cudaStream_t stream) {

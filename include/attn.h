@@ -286,6 +286,12 @@ attn_status_t attn_get_device_status(void* stream);
  *                        longest first for up to 256 sequences, so they fill the SMs that the
  *                        last full-length splits leave idle (LPT, as for the forward); 0 the
  *                        splits sequence by sequence
+ *   "decode_maps"        8-bit paged decode at d = 128 with a page size that is a multiple of
+ *                        16 and at most 8 or more than 16 query heads per kv head: 1 (default)
+ *                        each group of 16 tokens (within one page) is loaded per kv head with
+ *                        one tensor-map copy for K and one for V; 0 every lane copies 16-byte
+ *                        pieces of its token's rows (the path of the other shapes). Both give
+ *                        the same bytes
  * Returns ATTN_ERR_BAD_ARG for an unknown name or an invalid value.
  */
 attn_status_t attn_set_option(const char* name, double value);

@@ -161,7 +161,7 @@ def test_options_roundtrip():
         A.attn_set_option("exp_poly", 3)
     # forward pipeline switches: 0 or 1 only
     for name, default in (("correction", 0), ("unroll_kv", 0), ("packed_order", 1), ("dynamic_order", 1),
-                          ("decode_order", 1)):
+                          ("decode_order", 1), ("decode_maps", 1)):
         assert A.attn_get_option(name) == default
         A.attn_set_option(name, 1 - default)
         assert A.attn_get_option(name) == 1 - default

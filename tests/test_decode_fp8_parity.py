@@ -162,3 +162,77 @@ def test_fp8_rejects_unknown_format_and_bad_descales(A):
         assert rc == A.ATTN_ERR_BAD_ARG
         torch.cuda.synchronize()
         assert torch.isnan(o.float()).all()
+
+
+MAP_CASES = [
+    (fcase("maps_p16_g4", 13, 32, 8, 128, 16, 1, 4000, 41, "e4m3"), 0),
+    (fcase("maps_p32_g12_split2", 5, 24, 2, 128, 32, 100, 3000, 42, "e5m2"), 2),
+    (fcase("maps_p64_g32", 3, 32, 1, 128, 64, 1, 5000, 43, "e4m3"), 0),
+    (fcase("maps_p48_edges", 0, 8, 2, 128, 48, 0, 0, 44, "e4m3", lens=[0, 1, 15, 16, 17, 47, 48, 49, 1023, 1025]), 3),
+]
+
+
+@pytest.mark.parametrize("c,ns", MAP_CASES, ids=[c.name for c, _ in MAP_CASES])
+def test_fp8_decode_maps_switch_is_exact(A, c, ns):
+    """Page sizes that are multiples of 16 load each token group through the caches' tensor maps
+    (option decode_maps, default 1; at most 8 or more than 16 query heads per kv head, the 12-head
+    case checks that the switch leaves the other shapes alone); the per-row copies (0) must give
+    the same bytes, and both the oracle's result."""
+    q, kc8, vc8, pt, sl, kds, vds = c.generate_fp8()
+    outs = []
+    try:
+        for maps in (0, 1):
+            A.attn_set_option("decode_maps", maps)
+            outs.append(run(A, c, q, kc8, vc8, pt, sl, kds, vds, ns))
+    finally:
+        A.attn_set_option("decode_maps", 1)
+    (o0, l0), (o1, l1) = outs
+    assert torch.equal(o0.view(torch.int16), o1.view(torch.int16)) and torch.equal(l0, l1)
+    ro, rl = reference(c, q, kc8, vc8, pt, sl, kds, vds)
+    do, dl = compare(o1, l1, ro, rl)
+    assert do <= TOL_O and dl <= TOL_LSE, f"{c.name}: max|dO|={do:.3e} max|dLSE|={dl:.3e}"
+
+
+@pytest.mark.parametrize("maps", [1, 0])
+def test_fp8_nan_codes_past_the_length_never_count(A, maps):
+    """NaN codes in the slots of a sequence's last page past its length (a map load brings those
+    rows into shared memory with the group's others) and in unreferenced pages leave the result
+    finite and equal to the oracle's."""
+    c = fcase("tail_canary", 7, 16, 4, 128, 32, 1, 3000, 45, "e4m3", extra=5,
+              lens=[1, 17, 31, 33, 100, 1000, 2047])
+    q, kc8, vc8, pt, sl, kds, vds = c.generate_fp8()
+    used_rows = np.zeros((c.num_pages, c.page_size), dtype=bool)
+    for b in range(c.B):
+        for t in range(int(sl[b])):
+            used_rows[pt[b, t // c.page_size], t % c.page_size] = True
+    kc8[~used_rows] = 0x7F  # NaN codes
+    vc8[~used_rows] = 0x7F
+    try:
+        A.attn_set_option("decode_maps", maps)
+        o, lse = run(A, c, q, kc8, vc8, pt, sl, kds, vds)
+    finally:
+        A.attn_set_option("decode_maps", 1)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    ro, rl = reference(c, q, kc8, vc8, pt, sl, kds, vds)
+    do, dl = compare(o, lse, ro, rl)
+    assert do <= TOL_O and dl <= TOL_LSE, f"max|dO|={do:.3e} max|dLSE|={dl:.3e}"
+
+
+def test_fp8_bad_page_index_is_reported(A):
+    """An out-of-range page-table entry on the map-load path is reported, and the sequences that
+    do not use it are unaffected."""
+    c = fcase("badpage8", 2, 8, 2, 128, 16, 40, 60, 46, "e4m3")
+    q, kc8, vc8, pt, sl, kds, vds = c.generate_fp8()
+    pt = pt.copy()
+    pt[1, 1] = c.num_pages + 5
+    o = torch.full((c.B, c.Hq, c.d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((c.B, c.Hq), float("nan"), dtype=torch.float32, device=DEV)
+    A.attn_decode_paged_fp8(to_dev(q, DEV), torch.from_numpy(kc8).to(DEV), torch.from_numpy(vc8).to(DEV),
+                            torch.from_numpy(pt).to(DEV), torch.from_numpy(sl).to(DEV), c.page_size, o, lse, None,
+                            c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.num_pages, c.scale, 0, c.kv_fmt, kds, vds)
+    assert A.attn_get_device_status() == A.ATTN_ERR_DEVICE_BAD_INDEX
+    assert A.attn_get_device_status() == 0
+    ro, rl = oracle.attn_decode_paged_fp8(q[:1], kc8, vc8, c.kv_fmt, kds, vds, pt[:1], sl[:1], c.page_size, 1, c.Hq,
+                                          c.Hkv, c.d, c.max_pages, c.scale)
+    do, dl = compare(o[:1], lse[:1], ro, rl)
+    assert do <= TOL_O and dl <= TOL_LSE
