@@ -1,6 +1,8 @@
-"""Calls captured into a CUDA graph. The forward (d = 128 and the separate d = 256 kernel) and the
-allocation-free decode are captured once into one graph; replays give the same bytes as eager
-calls, and after new inputs are copied into the captured buffers a replay follows them. A
+"""Calls captured into a CUDA graph. The forward (d = 128 and the separate d = 256 kernel), the
+allocation-free decode and the 8-bit decode (split workspace from the library's stream-ordered
+pool, caches loaded through tensor maps) are captured once into one graph; replays give the same
+bytes as eager calls, and after new inputs are copied into the captured buffers a replay follows
+them. A
 serving loop drives the library this way instead of paying the host cost of each call (argument
 checks, tensor-map encoding, launch planning) every step."""
 import math
@@ -27,7 +29,8 @@ def A():
 
 
 class Problem:
-    """Device buffers of one forward (d = 128), one forward (d = 256) and one paged decode."""
+    """Device buffers of one forward (d = 128), one forward (d = 256), one paged decode and one
+    paged decode over e4m3 caches."""
 
     def __init__(self, seed):
         self.f = W.PrefillCase("g128", 1, 4, 2, 600, 600, 128, 1.0 / math.sqrt(128), True, seed)
@@ -40,6 +43,12 @@ class Problem:
         q, kc, vc, pt, sl = self.d.generate()
         self.din = [to_dev(q, DEV), to_dev(kc, DEV), to_dev(vc, DEV), torch.from_numpy(pt).to(DEV),
                     torch.from_numpy(sl).to(DEV)]
+        # e4m3 caches, page 16, 4 query heads per kv head: tensor-map loads; lengths up to 3000
+        # tokens make several splits, so the call takes its workspace from the pool
+        self.e = W.DecodeCase("gdec8", 4, 8, 2, 128, 16, lens, mp, 1.0 / math.sqrt(128), seed + 5, kv_fmt="e4m3")
+        q8, kc8, vc8, pt8, sl8, self.kds, self.vds = self.e.generate_fp8()
+        self.ein = [to_dev(q8, DEV), torch.from_numpy(kc8).to(DEV), torch.from_numpy(vc8).to(DEV),
+                    torch.from_numpy(pt8).to(DEV), torch.from_numpy(sl8).to(DEV)]
         bf, f32 = torch.bfloat16, torch.float32
         self.fo = torch.empty((self.f.total_q, 4, 128), dtype=bf, device=DEV)
         self.fl = torch.empty((self.f.total_q, 4), dtype=f32, device=DEV)
@@ -47,6 +56,8 @@ class Problem:
         self.wl = torch.empty((self.w.total_q, 2), dtype=f32, device=DEV)
         self.do = torch.empty((4, 8, 128), dtype=bf, device=DEV)
         self.dl = torch.empty((4, 8), dtype=f32, device=DEV)
+        self.eo = torch.empty((4, 8, 128), dtype=bf, device=DEV)
+        self.el = torch.empty((4, 8), dtype=f32, device=DEV)
 
     def run(self, A):
         f, w, d = self.f, self.w, self.d
@@ -55,12 +66,15 @@ class Problem:
         q, kc, vc, pt, sl = self.din
         A.attn_decode_paged_noalloc(q, kc, vc, pt, sl, d.page_size, self.do, self.dl, None, d.B, d.Hq, d.Hkv, d.d,
                                     d.max_pages, d.num_pages, d.scale)
+        e = self.e
+        A.attn_decode_paged_fp8(*self.ein, e.page_size, self.eo, self.el, None, e.B, e.Hq, e.Hkv, e.d, e.max_pages,
+                                e.num_pages, e.scale, 0, "e4m3", self.kds, self.vds)
 
     def outputs(self):
-        return [t.clone() for t in (self.fo, self.fl, self.wo, self.wl, self.do, self.dl)]
+        return [t.clone() for t in (self.fo, self.fl, self.wo, self.wl, self.do, self.dl, self.eo, self.el)]
 
     def poison(self):
-        for t in (self.fo, self.fl, self.wo, self.wl, self.do, self.dl):
+        for t in (self.fo, self.fl, self.wo, self.wl, self.do, self.dl, self.eo, self.el):
             t.fill_(float("nan"))
 
 
@@ -82,9 +96,11 @@ def test_graph_replay_matches_eager(A):
     for got, want in zip(p.outputs(), ref):
         assert torch.equal(got, want)
 
-    # new inputs in the captured buffers: the replay computes on them
+    # new inputs in the captured buffers: the replay computes on them (the descales are call
+    # arguments, fixed in the graph, so the eager reference takes the captured ones)
     q = Problem(77)
-    for dst, src in zip(p.fin + p.win + p.din, q.fin + q.win + q.din):
+    q.kds, q.vds = p.kds, p.vds
+    for dst, src in zip(p.fin + p.win + p.din + p.ein, q.fin + q.win + q.din + q.ein):
         dst.copy_(src)
     q.run(A)
     torch.cuda.synchronize()
