@@ -504,7 +504,8 @@ static attn_status_t decode_paged(const void* q, const void* k_cache, const void
     if (kv_format < 0) {
         e = attn::launch_attn_decode(p, d, s);
     } else if (d == 128 && page_size % attn::kDecodeMapRows == 0 && opt.decode_maps) {
-        // the 16 tokens of a token group lie in one page: one map load per group and tensor
+        // the 16 tokens of a token group lie in one page: one map load per group and tensor (the
+        // launcher keeps the per-row copies for the head counts where those measured faster)
         attn::DecodeTmaps tm;
         if ((st = encode_fn()) != ATTN_OK ||
             (st = make_cache_map(&tm.k, k_cache, (long long)num_pages * page_size, Hkv * d, d)) != ATTN_OK ||
