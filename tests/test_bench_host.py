@@ -1,5 +1,5 @@
 """Host logic of bench.py on the CPU: the cross-rank maximum with two gloo ranks, the decode
-sample workload, and the reference arm's JSON line."""
+sample workload, the reference arm's JSON line, and the source hashes of the traffic records."""
 import importlib.util
 import json
 import os
@@ -72,3 +72,24 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_traffic_records_cover_their_kernel_sources():
+    """Every committed DRAM-traffic record names a kernel whose source files exist, and the
+    hash that marks a record as current covers each file the kernel is compiled from (a change
+    to any of them makes the bench report the traffic as null until it is captured again)."""
+    b = _bench()
+    csrc = os.path.join(ROOT, "exact_softmax_attention_gb300", "csrc")
+    with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+        recs = json.load(f)
+    assert {"step_prefill", "step_decode", "decode_fp8"} <= set(recs)
+    for leg, e in recs.items():
+        files = b.kernel_sources(e["kernel"])
+        assert all(os.path.exists(os.path.join(csrc, n)) for n in files), leg
+        assert e["dram_bytes_per_launch"] > 0 and len(e["source_sha"]) == 16
+    # the decode kernels include their tensor-map header; the forward kernels do not
+    assert "decode_maps.cuh" in b.kernel_sources("decode_split_fp8_kernel")
+    assert "decode_maps.cuh" not in b.kernel_sources("attn_fwd_kernel")
+    # the hash changes with the contents of any listed file
+    sha = b.source_sha("decode_split_kernel")
+    assert sha == b.source_sha("decode_split_kernel") and sha != b.source_sha("attn_fwd_kernel")
