@@ -640,7 +640,10 @@ __global__ void __launch_bounds__(kWarps * 32, (fp8_min_blocks<D, TG, NST>()))
             const int g = t_begin + TG * (warp + kWarps * i);  // a multiple of 16: the group lies in one page
             int pslot;
             const int pg = __ldg(pt + page_index(p, g, pslot));
-            int row0 = 0;
+            // a page index out of range is not read: the copy starts at the first row past the
+            // cache (num_pages * page_size <= INT32_MAX), so the map fills the rows with zeros,
+            // as the per-row copies do
+            int row0 = p.num_pages * p.page_size;
             if (pg >= 0 && pg < p.num_pages)
                 row0 = pg * p.page_size + pslot;
             else

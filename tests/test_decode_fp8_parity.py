@@ -218,21 +218,32 @@ def test_fp8_nan_codes_past_the_length_never_count(A, maps):
     assert do <= TOL_O and dl <= TOL_LSE, f"max|dO|={do:.3e} max|dLSE|={dl:.3e}"
 
 
-def test_fp8_bad_page_index_is_reported(A):
-    """An out-of-range page-table entry on the map-load path is reported, and the sequences that
-    do not use it are unaffected."""
+@pytest.mark.parametrize("maps", [1, 0])
+def test_fp8_bad_page_index_is_reported(A, maps):
+    """An out-of-range page-table entry is reported and not read: its rows count as zeros (with
+    the map loads and with the per-row copies), and the sequences that do not use it are
+    unaffected."""
     c = fcase("badpage8", 2, 8, 2, 128, 16, 40, 60, 46, "e4m3")
     q, kc8, vc8, pt, sl, kds, vds = c.generate_fp8()
     pt = pt.copy()
     pt[1, 1] = c.num_pages + 5
     o = torch.full((c.B, c.Hq, c.d), float("nan"), dtype=torch.bfloat16, device=DEV)
     lse = torch.full((c.B, c.Hq), float("nan"), dtype=torch.float32, device=DEV)
-    A.attn_decode_paged_fp8(to_dev(q, DEV), torch.from_numpy(kc8).to(DEV), torch.from_numpy(vc8).to(DEV),
-                            torch.from_numpy(pt).to(DEV), torch.from_numpy(sl).to(DEV), c.page_size, o, lse, None,
-                            c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.num_pages, c.scale, 0, c.kv_fmt, kds, vds)
+    try:
+        A.attn_set_option("decode_maps", maps)
+        A.attn_decode_paged_fp8(to_dev(q, DEV), torch.from_numpy(kc8).to(DEV), torch.from_numpy(vc8).to(DEV),
+                                torch.from_numpy(pt).to(DEV), torch.from_numpy(sl).to(DEV), c.page_size, o, lse, None,
+                                c.B, c.Hq, c.Hkv, c.d, c.max_pages, c.num_pages, c.scale, 0, c.kv_fmt, kds, vds)
+    finally:
+        A.attn_set_option("decode_maps", 1)
     assert A.attn_get_device_status() == A.ATTN_ERR_DEVICE_BAD_INDEX
     assert A.attn_get_device_status() == 0
-    ro, rl = oracle.attn_decode_paged_fp8(q[:1], kc8, vc8, c.kv_fmt, kds, vds, pt[:1], sl[:1], c.page_size, 1, c.Hq,
-                                          c.Hkv, c.d, c.max_pages, c.scale)
-    do, dl = compare(o[:1], lse[:1], ro, rl)
-    assert do <= TOL_O and dl <= TOL_LSE
+    # the oracle with the bad entry pointing at a page of zero codes (+0.0 in both formats)
+    zero = np.zeros((1,) + kc8.shape[1:], dtype=kc8.dtype)
+    kz, vz = np.concatenate([kc8, zero]), np.concatenate([vc8, zero])
+    pz = pt.copy()
+    pz[1, 1] = c.num_pages
+    ro, rl = oracle.attn_decode_paged_fp8(q, kz, vz, c.kv_fmt, kds, vds, pz, sl, c.page_size, c.B, c.Hq, c.Hkv, c.d,
+                                          c.max_pages, c.scale)
+    do, dl = compare(o, lse, ro, rl)
+    assert do <= TOL_O and dl <= TOL_LSE, f"max|dO|={do:.3e} max|dLSE|={dl:.3e}"
